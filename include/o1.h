@@ -1,0 +1,162 @@
+/*
+ * o1.h — C ABI of the sealed O(1) layer attention library (libo1.so, CUDA,
+ * sm_103a).
+ *
+ * A sealed layer's attention: every query row attends to
+ *   (1) a few sink keys,
+ *   (2) a ring-buffer window of recent keys (the causal rows of the call
+ *       included), and
+ *   (3) a constant-size far field that summarises every key evicted from the
+ *       ring: per (group, head, landmark query b) a running max M_b, mass Z_b
+ *       and value sum T_b of exp(scale * qt_b . k_evicted - M_b), read back
+ *       through the landmark keys kt and the coefficients mu.
+ * The method is the one of "cortiq-engine 0.8.51 src/gpu_wgpu/o1_batch.rs"
+ * (module doc; kernels o1b_far_e, o1b_attend, o1b_far_commit,
+ * o1b_ring_commit, o1b_meta); the one-row variant is the one of
+ * "cortiq-engine 0.8.82 src/gpu_metal/o1c.rs" (encode_tok) and of
+ * "cortiq-engine 0.8.77 src/gpu_wgpu/dory.rs" (dory_os ... dory_ogate), whose
+ * rotation (dory_prep) and output gate (dory_gate1) it also applies.
+ *
+ * Conventions, for every entry point:
+ *  - Ownership: the caller allocates and frees every buffer. The library
+ *    never allocates device or host memory and keeps no global state; a
+ *    state buffer carries its own header.
+ *  - Pointers: "device" pointers are CUDA global memory of the current
+ *    device, "host" pointers are ordinary process memory. Device buffers must
+ *    be 16-byte aligned (a torch or cudaMalloc allocation always is); the
+ *    state and scratch buffers 256-byte aligned.
+ *  - Layouts are row-major fp32 unless stated; shapes are written [a][b][c]
+ *    with the last index fastest.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream). Calls are asynchronous on it except where stated. A
+ *    state must be used from one stream at a time.
+ *  - Errors: every call validates its arguments before launching anything
+ *    and returns O1_OK or a negative status; nothing falls back to another
+ *    implementation. O1_ERR_CUDA reports a failed launch or copy
+ *    (cudaPeekAtLastError / the copy's status).
+ */
+#ifndef O1_H
+#define O1_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define O1_API __attribute__((visibility("default")))
+#else
+#define O1_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    O1_OK = 0,
+    O1_ERR_ARG = -1,          /* null or misaligned pointer, bad size        */
+    O1_ERR_UNSUPPORTED = -2,  /* geometry outside the library's limits       */
+    O1_ERR_CUDA = -3,         /* a CUDA launch or copy failed                */
+    O1_ERR_STATE = -4         /* state header does not match the geometry    */
+};
+
+/* Geometry of one sealed layer ("cortiq-engine 0.8.51 src/gpu_wgpu/o1_batch.rs",
+ * struct Geom). Limits: groups >= 1, heads_per_group in [1, 16],
+ * d in [8, 256] with d % 8 == 0, dv in [4, 256] with dv % 4 == 0,
+ * sinks in [0, 255], window in [1, 1 << 20], landmarks in [1, 64]. */
+typedef struct o1_geom {
+    int32_t groups;           /* G: KV groups                                  */
+    int32_t heads_per_group;  /* hpg: query heads per KV group (nh = G * hpg)  */
+    int32_t d;                /* key / query width                             */
+    int32_t dv;               /* value width                                   */
+    int32_t sinks;            /* ns: sink keys per group                       */
+    int32_t window;           /* w: ring stride = the widest group window      */
+    int32_t landmarks;        /* m: landmark queries per head                  */
+    int32_t rect_far_mass;    /* 1: u_b = max(u_b, 0) (the pages' rect_fm)     */
+    float scale;              /* score scale, normally 1/sqrt(d)               */
+    float rope_base;          /* rotary base (e.g. 1e6); 0 = no rotation       */
+} o1_geom;
+
+/* Host-side view of a state, for o1_state_read / o1_state_write. Every
+ * pointer is host memory and may be NULL (that part is skipped). */
+typedef struct o1_state_host {
+    uint32_t *meta;    /* [G][4]: len, head, farl, group window                */
+    int64_t *pos;      /* [1]: absolute position of the next row               */
+    float *ring_k;     /* [G][window][d]: rotated keys by ring slot            */
+    float *ring_v;     /* [G][window][dv]                                      */
+    float *far_max;    /* M [G*hpg][m]; -inf while the far field is empty      */
+    float *far_mass;   /* Z [G*hpg][m]                                         */
+    float *far_val;    /* T [G*hpg][m][dv]                                     */
+} o1_state_host;
+
+/* Bytes of device memory a state of this geometry needs (0 if the geometry is
+ * outside the limits). Host-only; no CUDA call. */
+O1_API size_t o1_state_bytes(const o1_geom *geom);
+
+/* Bytes of device scratch that lets one o1_chunk_attend launch process up to
+ * `max_rows` rows in one pass (longer calls run in passes of that many rows).
+ * 0 if the geometry is unsupported or max_rows < 1. Host-only. */
+O1_API size_t o1_scratch_bytes(const o1_geom *geom, int32_t max_rows);
+
+/* Start a sealed layer from an empty ring and far field ("cortiq-engine
+ * 0.8.51 src/gpu_wgpu/o1_batch.rs", struct State and the meta layout of
+ * o1b_meta; an empty far field has M = -inf, Z = 0 as o1b_far_e's comment
+ * states).
+ *   state          device, o1_state_bytes(geom) bytes, 256-byte aligned; overwritten
+ *   group_windows  host [G] or NULL: each group's window (meta slot 3),
+ *                  0 = geom->window; every value <= geom->window
+ *   sink_k, sink_v device [G][ns][d], [G][ns][dv] (may be NULL if ns == 0)
+ *   k_tilde        device [G][m][d]      landmark keys, one set per group
+ *   q_tilde        device [G][hpg][m][d] landmark queries, per head
+ *   mu             device [G*hpg][m][m]  mu[a][b], a = landmark key, b = query
+ *   pos0           absolute position of the first row (rotation angle)
+ * Sinks and landmarks are used as given (already rotated). Asynchronous. */
+O1_API int o1_state_init(void *state, const o1_geom *geom, const int32_t *group_windows,
+                  const float *sink_k, const float *sink_v, const float *k_tilde,
+                  const float *q_tilde, const float *mu, int64_t pos0, void *stream);
+
+/* Attention of `rows` consecutive rows, and the state advanced past them
+ * ("cortiq-engine 0.8.51 src/gpu_wgpu/o1_batch.rs": encode and the kernels
+ * o1b_far_e, o1b_attend, o1b_far_commit, o1b_ring_commit, o1b_meta; gate as
+ * dory_gate1 of "cortiq-engine 0.8.77 src/gpu_wgpu/dory.rs").
+ *   q     device [rows][G*hpg][d]  queries, NOT rotated (rotated here at pos)
+ *   k     device [rows][G][d]      keys, not rotated
+ *   v     device [rows][G][dv]
+ *   gate  device [rows][G*hpg][dv] gate logits, or NULL for no gate
+ *   out   device [rows][G*hpg][dv] o / (1 + exp(-gate)); must not alias q/k/v/gate
+ *   scratch, scratch_bytes  device scratch, at least o1_scratch_bytes(geom, 1)
+ * The output equals the rows processed one at a time (rope, far insert, ring
+ * push, attend, gate), up to rounding. Asynchronous. */
+O1_API int o1_chunk_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                    const float *q, const float *k, const float *v, const float *gate,
+                    int32_t rows, float *out, void *stream);
+
+/* One row (a decode step): the same as o1_chunk_attend with rows = 1, by a
+ * path built for it ("cortiq-engine 0.8.82 src/gpu_metal/o1c.rs" encode_tok:
+ * near partials split across blocks, the far part, a merge, the commit).
+ *   q [G*hpg][d], k [G][d], v [G][dv], gate [G*hpg][dv] or NULL, out [G*hpg][dv]
+ *   scratch  device, at least o1_scratch_bytes(geom, 1) bytes
+ * Asynchronous. */
+O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                    const float *q, const float *k, const float *v, const float *gate,
+                    float *out, void *stream);
+
+/* Copy the state's mutable parts to host memory (NULL fields skipped).
+ * Synchronises `stream`. Returns O1_ERR_STATE if the state's header does not
+ * hold this geometry. */
+O1_API int o1_state_read(const void *state, const o1_geom *geom, o1_state_host *dst, void *stream);
+
+/* Overwrite the state's mutable parts from host memory (NULL fields kept):
+ * snapshots and test set-up. Synchronises `stream`. The caller keeps the
+ * state consistent (len <= group window, head < group window, M = -inf
+ * exactly where farl == 0, ...). */
+O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host *src, void *stream);
+
+/* A static, human-readable name for a status code. */
+O1_API const char *o1_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* O1_H */

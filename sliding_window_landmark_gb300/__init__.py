@@ -11,6 +11,6 @@ __all__ = ["synth", "o1"]
 
 def __getattr__(name):
     if name == "o1":
-        from . import o1 as mod
-        return mod
+        import importlib
+        return importlib.import_module(".o1", __name__)
     raise AttributeError(name)

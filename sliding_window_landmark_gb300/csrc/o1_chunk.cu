@@ -1,0 +1,669 @@
+// The chunk path of a sealed O(1) layer: one pass over R rows.
+//
+// The method is the one of "cortiq-engine 0.8.51 src/gpu_wgpu/o1_batch.rs":
+// per row, sinks + the row's ring window + the landmark far field; the state
+// moves by rope, far insert, ring push (module doc). The pages run it as five
+// dispatches per 64-row sub-chunk (o1b_far_e, o1b_attend, o1b_far_commit,
+// o1b_ring_commit, o1b_meta), each sub-chunk waiting for the last. Here the
+// whole pass is parallel, because only the far field is sequential and its
+// per-block partials compose associatively:
+//
+//  1. k_rope         rotate q and k of every row (dory.rs, dory_prep)
+//  2. k_far_logits   l = scale qt_b . k_e for every key the pass evicts
+//                    (o1b_far_e's dot, all blocks at once)
+//  3. k_far_scan     per (head, landmark): block max M_c, rescale R_c,
+//                    E = exp(l - M_c), far-mass prefix P per row (o1b_far_e's
+//                    max / rescale / prefix, as a scan over the blocks)
+//  4. k_far_dT       per block: sum_j E_bj v_ev(j)  (o1b_far_commit's sum)
+//  5. k_far_tscan    T entering each block, rescaled to its max
+//                    (o1b_far_commit's recurrence T <- R T + dT, as a scan)
+//  6. k_far_readout  per row: landmark scores, u = e^{f-F} mu, gains, the far
+//                    mass D and numerator (o1b_attend's far part)
+//  7. k_near         sinks + window, online softmax, merged with the far part
+//                    under one exponent, gate (o1b_attend's near part and
+//                    normalisation; dory_gate1)
+//  8. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
+//
+// Keys are indexed in X = [ring, oldest first] ++ [this pass's rows]: row r
+// sees X[max(0, len0 + r + 1 - wg) .. len0 + r] and evicts X[r - j0] once
+// r >= j0 = wg - len0 (o1b_far_e: "ring logical index j - j0"). That indexing
+// also covers a pass whose rows evict keys pushed earlier in the same pass
+// (window shorter than a block), which the pages' sub-chunking excludes.
+#include <math.h>
+
+#include "o1_common.cuh"
+
+// ------------------------------------------------------------------ rope
+
+// One block per row. Thread j < d/2 forms the angle of pair (j, j + d/2)
+// once and rotates every query head and every key group with it. The angle
+// p * inv[j] is formed in double (inv is f32, as the pages' table input),
+// reduced by 2 pi in two parts (Cody-Waite), and its sine and cosine are
+// taken in f32 with a first-order correction for the reduced angle's
+// rounding: within a few f32 ulp of the pages' f64-then-f32 table.
+__global__ void k_rope(O1Args a) {
+    const int r = blockIdx.x;
+    const int half = a.d >> 1;
+    const int64_t p = a.hdr->pos + r;
+    for (int j = threadIdx.x; j < half; j += blockDim.x) {
+        float c = 1.f, s = 0.f;
+        if (a.rotate) {
+            const double ang = (double)p * (double)a.hdr->inv_freq[j];
+            const double kq = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
+            double red = fma(-kq, 6.283185307179586, ang);        // 2 pi, high part
+            red = fma(-kq, 2.4492935982947064e-16, red);          // 2 pi, low part
+            const float rf = (float)red;
+            const float rl = (float)(red - (double)rf);
+            float sf, cf;
+            sincosf(rf, &sf, &cf);
+            c = cf - sf * rl;
+            s = sf + cf * rl;
+        }
+        for (int hh = 0; hh < a.nh; ++hh) {
+            const size_t o = ((size_t)r * a.nh + hh) * a.d;
+            const float x0 = a.q[o + j], x1 = a.q[o + j + half];
+            a.qr[o + j] = x0 * c - x1 * s;
+            a.qr[o + j + half] = x1 * c + x0 * s;
+        }
+        for (int g = 0; g < a.G; ++g) {
+            const size_t o = ((size_t)r * a.G + g) * a.d;
+            const float x0 = a.k[o + j], x1 = a.k[o + j + half];
+            a.kr[o + j] = x0 * c - x1 * s;
+            a.kr[o + j + half] = x1 * c + x0 * s;
+        }
+    }
+}
+
+// ------------------------------------------------------------- far field
+
+// Far logits of the evicted keys: E[gh][b][x] = scale qt[gh][b] . X[x] for
+// x < R - j0. Block = (64 evicted keys, head).
+__global__ __launch_bounds__(256) void k_far_logits(O1Args a) {
+    const int gh = blockIdx.y, g = gh / a.hpg;
+    const O1Meta mt = o1_meta(a, g);
+    const int j0 = mt.wg - mt.len0;
+    const int nev = a.R - j0;
+    const int x0 = blockIdx.x * 64;
+    if (x0 >= nev) return;
+    __shared__ float sA[64 * 33], sB[64 * 33];
+    float c[4][4];
+    blk_zero(c);
+    for (int kc = 0; kc < a.d; kc += 32) {
+        for (int idx = threadIdx.x; idx < 64 * 32; idx += 256) {
+            const int i = idx >> 5, kk = idx & 31;
+            const bool in = kc + kk < a.d;
+            sA[i * 33 + kk] = (i < a.m && in) ? a.qt[((size_t)gh * a.m + i) * a.d + kc + kk] : 0.f;
+            sB[i * 33 + kk] = (x0 + i < nev && in) ? o1_key(a, g, x0 + i, mt)[kc + kk] : 0.f;
+        }
+        __syncthreads();
+        blk_nt(c, sA, 33, sB, 33, 32);
+        __syncthreads();
+    }
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = ty + 16 * i, x = x0 + tx + 16 * j;
+            if (b < a.m && x < nev) a.E[((size_t)gh * a.m + b) * a.cap + x] = a.scale * c[i][j];
+        }
+}
+
+// One warp per (head, landmark query b), sequential over the pass's blocks of
+// O1_SUB rows: the far max after each block M_c, the rescale R_c of what came
+// before (1 if the max did not move, so an empty field stays empty), E =
+// exp(l - M_c) in place of l, and for every row the far mass P = R_c Z +
+// (prefix of E within the block).
+__global__ __launch_bounds__(256) void k_far_scan(O1Args a) {
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= a.nh * a.m) return;
+    const int gh = wid / a.m, g = gh / a.hpg;
+    const O1Meta mt = o1_meta(a, g);
+    const int j0 = mt.wg - mt.len0;
+    float Mo = a.M[wid], Zo = a.Z[wid];
+    float *E = a.E + (size_t)wid * a.cap;
+    float *P = a.P + (size_t)wid * a.cap;
+    for (int c = 0; c < a.nsub; ++c) {
+        const int r0 = c * O1_SUB;
+        float l[2];
+        bool ev[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = r0 + hf * 32 + lane;
+            ev[hf] = r < a.R && r >= j0;
+            l[hf] = ev[hf] ? E[r - j0] : -INFINITY;
+        }
+        const float Mn = fmaxf(Mo, warp_max(fmaxf(l[0], l[1])));
+        const float Rf = (Mn == Mo) ? 1.f : expf(Mo - Mn);
+        const float base = Rf * Zo;
+        float run = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = r0 + hf * 32 + lane;
+            const float e = ev[hf] ? expf(l[hf] - Mn) : 0.f;
+            if (ev[hf]) E[r - j0] = e;
+            float incl = e;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (r < a.R) P[r] = base + (run + incl);
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        Zo = base + run;
+        Mo = Mn;
+        if (lane == 0) {
+            a.Mc[(size_t)wid * a.nsub + c] = Mn;
+            a.Rc[(size_t)wid * a.nsub + c] = Rf;
+        }
+    }
+    if (lane == 0) {
+        a.M[wid] = Mo;
+        a.Z[wid] = Zo;
+    }
+}
+
+// Value-sum increment of each block: dT[c][gh][b][t] = sum over the block's
+// evicting rows j of E[b][j] v_ev(j)[t]. Block = (block c, head, 64 columns).
+__global__ __launch_bounds__(256) void k_far_dT(O1Args a) {
+    const int c = blockIdx.x, gh = blockIdx.y, tc = blockIdx.z * 64, g = gh / a.hpg;
+    const O1Meta mt = o1_meta(a, g);
+    const int j0 = mt.wg - mt.len0;
+    const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
+    float *dst = a.Tp + (size_t)(c * a.nh + gh) * a.m * a.dv;
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+    if (max(r0, j0) >= r0 + nr) {   // nothing evicted in this block
+        for (int idx = threadIdx.x; idx < a.m * 64; idx += 256) {
+            const int b = idx >> 6, t = tc + (idx & 63);
+            if (t < a.dv) dst[(size_t)b * a.dv + t] = 0.f;
+        }
+        return;
+    }
+    __shared__ float sA[64 * 65], sB[64 * 65];
+    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+        const int i = idx >> 6, jj = idx & 63;
+        const int r = r0 + jj;
+        const bool evj = jj < nr && r >= j0;
+        sA[i * 65 + jj] = (i < a.m && evj) ? a.E[((size_t)gh * a.m + i) * a.cap + (r - j0)] : 0.f;
+        // row i of B is evicting row r0 + i, column jj is value column tc + jj
+        const int ri = r0 + i;
+        const bool evi = i < nr && ri >= j0 && tc + jj < a.dv;
+        sB[i * 65 + jj] = evi ? o1_val(a, g, ri - j0, mt)[tc + jj] : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+    blk_zero(acc);
+    blk_nn(acc, sA, 65, sB, 65, 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = ty + 16 * i, t = tc + tx + 16 * j;
+            if (b < a.m && t < a.dv) dst[(size_t)b * a.dv + t] = acc[i][j];
+        }
+}
+
+// The value sum entering each block, rescaled to that block's max:
+// Tp[c] <- R_c T_{c-1} (what the block's rows read), T_c = R_c T_{c-1} + dT_c;
+// the last T is the new state. One thread per (head, landmark, column).
+__global__ void k_far_tscan(O1Args a) {
+    const size_t n = (size_t)a.nh * a.m * a.dv;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n) return;
+    const size_t wid = idx / a.dv;
+    float T = a.T[idx];
+    for (int c = 0; c < a.nsub; ++c) {
+        const float rf = a.Rc[wid * a.nsub + c];
+        float *tp = a.Tp + (size_t)c * n + idx;
+        const float dT = *tp;
+        const float Ts = rf * T;
+        *tp = Ts;
+        T = Ts + dT;
+    }
+    a.T[idx] = T;
+}
+
+// The far part of every row of block c for head gh (o1b_attend's far half,
+// referenced to the block's max as the pages do):
+//   f_a = scale q'.kt_a, F = max f, u_b = sum_a e^{f_a - F} mu[a][b] (rect),
+//   c_f = max_b (F + M_c[b]), gain_b = u_b e^{F + M_c[b] - c_f},
+//   D = sum_b gain_b P_b(row); the far part is dropped if D < 0;
+//   numerator = sum_b gain_b (R_c T_{c-1})_b + sum_{evicting j <= row} cf_j v_ev(j),
+//   cf_j = sum_b gain_b E_bj.
+// The numerator goes to `out` (the near kernel finishes the row there), and
+// (c_f, D, have) to the far header; c_f = -inf marks a row with no far field.
+__global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = tid >> 4, tx = tid & 15;
+    const O1Meta mt = o1_meta(a, g);
+    const int j0 = mt.wg - mt.len0;
+    const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
+    const int m = a.m, d = a.d, dv = a.dv, nh = a.nh;
+    const int farl_last = mt.farl0 + max(0, r0 + nr - j0);
+    if (farl_last == 0) {
+        for (int idx = tid; idx < nr * dv; idx += 256) {
+            const int i = idx / dv, t = idx % dv;
+            a.out[((size_t)(r0 + i) * nh + gh) * dv + t] = 0.f;
+        }
+        for (int i = tid; i < nr; i += 256)
+            *(float4 *)(a.fh + ((size_t)(r0 + i) * nh + gh) * 4) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        return;
+    }
+    float *sA = sm;                // 64 x 33  query chunk
+    float *sB = sA + 64 * 33;      // 64 x 33  landmark-key chunk
+    float *sF = sB + 64 * 33;      // 64 x 65  f, then e^{f - F}
+    float *sU = sF + 64 * 65;      // 64 x 65  u, then gains
+    float *sX = sU + 64 * 65;      // 64 x 65  mu, then E, then T chunk
+    float *sC = sX + 64 * 65;      // 64 x 65  cf
+    float *sV = sC + 64 * 65;      // 64 x 65  value chunk
+    float *sRow = sV + 64 * 65;    // 64       F per row
+    float *sMc = sRow + 64;        // 64       block max per landmark
+    float acc[4][4];
+
+    // 1. landmark scores
+    blk_zero(acc);
+    for (int kc = 0; kc < d; kc += 32) {
+        for (int idx = tid; idx < 64 * 32; idx += 256) {
+            const int i = idx >> 5, kk = idx & 31;
+            const bool in = kc + kk < d;
+            sA[i * 33 + kk] = (i < nr && in) ? a.qr[((size_t)(r0 + i) * nh + gh) * d + kc + kk] : 0.f;
+            sB[i * 33 + kk] = (i < m && in) ? a.kt[((size_t)g * m + i) * d + kc + kk] : 0.f;
+        }
+        __syncthreads();
+        blk_nt(acc, sA, 33, sB, 33, 32);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sF[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc[i][j];
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        const int aa = idx >> 6, b = idx & 63;
+        sX[aa * 65 + b] = (aa < m && b < m) ? a.mu[((size_t)gh * m + aa) * m + b] : 0.f;
+    }
+    for (int b = tid; b < 64; b += 256) sMc[b] = b < m ? a.Mc[((size_t)gh * m + b) * a.nsub + c] : 0.f;
+    __syncthreads();
+
+    // 2. F per row and e^{f - F}
+    for (int i = warp; i < 64; i += 8) {
+        const float v0 = lane < m ? sF[i * 65 + lane] : -INFINITY;
+        const float v1 = lane + 32 < m ? sF[i * 65 + lane + 32] : -INFINITY;
+        const float F = warp_max(fmaxf(v0, v1));
+        if (lane == 0) sRow[i] = F;
+        sF[i * 65 + lane] = lane < m ? expf(v0 - F) : 0.f;
+        sF[i * 65 + lane + 32] = lane + 32 < m ? expf(v1 - F) : 0.f;
+    }
+    __syncthreads();
+
+    // 3. u = e mu
+    blk_zero(acc);
+    blk_nn(acc, sF, 65, sX, 65, m);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sU[(ty + 16 * i) * 65 + tx + 16 * j] = acc[i][j];
+    __syncthreads();
+
+    // 4. gains, far mass, sign decision (one warp per row)
+    for (int i = warp; i < 64; i += 8) {
+        const int r = r0 + i;
+        const int farl = mt.farl0 + max(0, r - j0 + 1);
+        float g0 = 0.f, g1 = 0.f;
+        if (i < nr && farl > 0) {
+            float u0 = lane < m ? sU[i * 65 + lane] : 0.f;
+            float u1 = lane + 32 < m ? sU[i * 65 + lane + 32] : 0.f;
+            if (a.rect) {
+                u0 = fmaxf(u0, 0.f);
+                u1 = fmaxf(u1, 0.f);
+            }
+            const float F = sRow[i];
+            const float cb0 = lane < m ? F + sMc[lane] : -INFINITY;
+            const float cb1 = lane + 32 < m ? F + sMc[lane + 32] : -INFINITY;
+            const float cf = warp_max(fmaxf(cb0, cb1));
+            g0 = lane < m ? u0 * expf(cb0 - cf) : 0.f;
+            g1 = lane + 32 < m ? u1 * expf(cb1 - cf) : 0.f;
+            const float p0 = lane < m ? a.P[((size_t)gh * m + lane) * a.cap + r] : 0.f;
+            const float p1 = lane + 32 < m ? a.P[((size_t)gh * m + lane + 32) * a.cap + r] : 0.f;
+            const float D = warp_sum(g0 * p0 + g1 * p1);
+            const bool have = D >= 0.f;
+            if (!have) {
+                g0 = 0.f;
+                g1 = 0.f;
+            }
+            if (lane == 0)
+                *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) =
+                    make_float4(cf, have ? D : 0.f, have ? 1.f : 0.f, 0.f);
+        } else if (i < nr && lane == 0) {
+            *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        }
+        sU[i * 65 + lane] = g0;
+        sU[i * 65 + lane + 32] = g1;
+    }
+    // E of this block's evicting rows, referenced to M_c by k_far_scan
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        const int b = idx >> 6, jj = idx & 63;
+        const int r = r0 + jj;
+        sX[b * 65 + jj] = (b < m && jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
+    }
+    __syncthreads();
+
+    // 5. in-block far coefficients, causal: cf[i][jj] for jj <= i
+    blk_zero(acc);
+    blk_nn(acc, sU, 65, sX, 65, m);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int row = ty + 16 * i, jj = tx + 16 * j;
+            sC[row * 65 + jj] = jj <= row ? acc[i][j] : 0.f;
+        }
+    __syncthreads();
+
+    // 6. numerator, 64 value columns at a time
+    const float *Tp = a.Tp + (size_t)(c * nh + gh) * m * dv;
+    for (int tc = 0; tc < dv; tc += 64) {
+        for (int idx = tid; idx < 64 * 64; idx += 256) {
+            const int i = idx >> 6, t = idx & 63;
+            const bool in = tc + t < dv;
+            sX[i * 65 + t] = (i < m && in) ? Tp[(size_t)i * dv + tc + t] : 0.f;
+            const int r = r0 + i;
+            sV[i * 65 + t] = (i < nr && r >= j0 && in) ? o1_val(a, g, r - j0, mt)[tc + t] : 0.f;
+        }
+        __syncthreads();
+        blk_zero(acc);
+        blk_nn(acc, sU, 65, sX, 65, m);
+        blk_nn(acc, sC, 65, sV, 65, 64);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int row = ty + 16 * i, t = tc + tx + 16 * j;
+                if (row < nr && t < dv) a.out[((size_t)(r0 + row) * nh + gh) * dv + t] = acc[i][j];
+            }
+        __syncthreads();
+    }
+}
+
+// ----------------------------------------------------------- near + merge
+
+// Block = (rows, group): 32 query slots = floor(32 / hpg) rows x hpg heads,
+// so one staged key/value tile serves every head of the group. 8 warps, 4
+// slots each; within a key tile, lane = key. Keys: the group's sinks, then
+// X[lo(r0) .. hi(last row)]; each slot masks to its own row's window.
+// Online softmax (running max and sum), then the far part merged under the
+// common exponent c = max(near max, c_f) as o1b_attend's c_all, the
+// denominator floored at 1e-30 in those units, and the gate.
+template <int NV>
+__global__ __launch_bounds__(256) void k_near(O1Args a) {
+    extern __shared__ float sm[];
+    const int dq = a.d + 4, dvq = a.dv + 4;
+    float *sQ = sm;
+    float *sK = sQ + 32 * dq;
+    float *sV = sK + 32 * dq;
+    const int g = blockIdx.y;
+    const int hpg = a.hpg;
+    const int RB = 32 / hpg;
+    const int r0 = blockIdx.x * RB;
+    const int nr = min(RB, a.R - r0);
+    const int nq = nr * hpg;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const O1Meta mt = o1_meta(a, g);
+    const int d4 = a.d >> 2, dv4 = a.dv >> 2;
+
+    for (int idx = tid; idx < 32 * d4; idx += 256) {
+        const int s = idx / d4, c4 = idx % d4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < nq) {
+            const int r = r0 + s / hpg, hh = g * hpg + s % hpg;
+            val = ((const float4 *)(a.qr + ((size_t)r * a.nh + hh) * a.d))[c4];
+        }
+        ((float4 *)(sQ + s * dq))[c4] = val;
+    }
+
+    int lo[4], hi[4];
+    bool act[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int s = warp * 4 + i;
+        act[i] = s < nq;
+        const int r = r0 + (act[i] ? s / hpg : 0);
+        lo[i] = max(0, mt.len0 + r + 1 - mt.wg);
+        hi[i] = mt.len0 + r;
+    }
+    float mrow[4], lrow[4], acc[4][NV][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mrow[i] = -INFINITY;
+        lrow[i] = 0.f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[i][v][0] = acc[i][v][1] = acc[i][v][2] = acc[i][v][3] = 0.f;
+    }
+
+    const int xlo = max(0, mt.len0 + r0 + 1 - mt.wg);
+    const int xhi = mt.len0 + r0 + nr - 1;
+    const int nkeys = a.ns + (xhi - xlo + 1);
+    const float *sinks_k = a.sink_k + (size_t)g * a.ns * a.d;
+    const float *sinks_v = a.sink_v + (size_t)g * a.ns * a.dv;
+
+    for (int kb = 0; kb < nkeys; kb += 32) {
+        const int cnt = min(32, nkeys - kb);
+        __syncthreads();
+        for (int idx = tid; idx < 32 * d4; idx += 256) {
+            const int kk = idx / d4, c4 = idx % d4;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kk < cnt) {
+                const int key = kb + kk;
+                const float *src = key < a.ns ? sinks_k + (size_t)key * a.d : o1_key(a, g, xlo + key - a.ns, mt);
+                val = ((const float4 *)src)[c4];
+            }
+            ((float4 *)(sK + kk * dq))[c4] = val;
+        }
+        for (int idx = tid; idx < 32 * dv4; idx += 256) {
+            const int kk = idx / dv4, c4 = idx % dv4;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kk < cnt) {
+                const int key = kb + kk;
+                const float *src = key < a.ns ? sinks_v + (size_t)key * a.dv : o1_val(a, g, xlo + key - a.ns, mt);
+                val = ((const float4 *)src)[c4];
+            }
+            ((float4 *)(sV + kk * dvq))[c4] = val;
+        }
+        __syncthreads();
+
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4 *kp = (const float4 *)(sK + lane * dq);
+#pragma unroll 4
+        for (int c4 = 0; c4 < d4; ++c4) {
+            const float4 kv = kp[c4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 qv = ((const float4 *)(sQ + (warp * 4 + i) * dq))[c4];
+                sc[i] = fmaf(qv.x, kv.x, sc[i]);
+                sc[i] = fmaf(qv.y, kv.y, sc[i]);
+                sc[i] = fmaf(qv.z, kv.z, sc[i]);
+                sc[i] = fmaf(qv.w, kv.w, sc[i]);
+            }
+        }
+        const int key = kb + lane;
+        const int x = xlo + key - a.ns;
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool ok = act[i] && lane < cnt && (key < a.ns || (x >= lo[i] && x <= hi[i]));
+            const float s = ok ? sc[i] * a.scale : -INFINITY;
+            const float tm = warp_max(s);
+            p[i] = 0.f;
+            if (tm == -INFINITY) continue;
+            const float mn = fmaxf(mrow[i], tm);
+            const float al = expf(mrow[i] - mn);
+            p[i] = ok ? expf(s - mn) : 0.f;
+            lrow[i] = lrow[i] * al + warp_sum(p[i]);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                acc[i][v][0] *= al;
+                acc[i][v][1] *= al;
+                acc[i][v][2] *= al;
+                acc[i][v][3] *= al;
+            }
+            mrow[i] = mn;
+        }
+        for (int kk = 0; kk < cnt; ++kk) {
+            float pk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pk[i] = __shfl_sync(0xffffffffu, p[i], kk);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int col = lane * 4 + 128 * v;
+                if (col < a.dv) {
+                    const float4 vv = *(const float4 *)(sV + kk * dvq + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[i][v][0] = fmaf(pk[i], vv.x, acc[i][v][0]);
+                        acc[i][v][1] = fmaf(pk[i], vv.y, acc[i][v][1]);
+                        acc[i][v][2] = fmaf(pk[i], vv.z, acc[i][v][2]);
+                        acc[i][v][3] = fmaf(pk[i], vv.w, acc[i][v][3]);
+                    }
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (!act[i]) continue;
+        const int s = warp * 4 + i;
+        const int r = r0 + s / hpg, hh = g * hpg + s % hpg;
+        const float4 hd = *(const float4 *)(a.fh + ((size_t)r * a.nh + hh) * 4);
+        const bool have = hd.z > 0.5f;
+        const float cexp = hd.x > -INFINITY ? fmaxf(mrow[i], hd.x) : mrow[i];
+        const float al = expf(mrow[i] - cexp);
+        const float be = have ? expf(hd.x - cexp) : 0.f;
+        const float den = fmaxf(be * hd.y + al * lrow[i], 1e-30f);
+        float *o = a.out + ((size_t)r * a.nh + hh) * a.dv;
+        const float *gt = a.gate ? a.gate + ((size_t)r * a.nh + hh) * a.dv : nullptr;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int col = lane * 4 + 128 * v;
+            if (col >= a.dv) continue;
+            const float4 nf = *(const float4 *)(o + col);
+            float y[4] = {(be * nf.x + al * acc[i][v][0]) / den, (be * nf.y + al * acc[i][v][1]) / den,
+                          (be * nf.z + al * acc[i][v][2]) / den, (be * nf.w + al * acc[i][v][3]) / den};
+            if (gt) {
+                const float4 gv = *(const float4 *)(gt + col);
+                y[0] = y[0] / (1.f + expf(-gv.x));
+                y[1] = y[1] / (1.f + expf(-gv.y));
+                y[2] = y[2] / (1.f + expf(-gv.z));
+                y[3] = y[3] / (1.f + expf(-gv.w));
+            }
+            *(float4 *)(o + col) = make_float4(y[0], y[1], y[2], y[3]);
+        }
+    }
+}
+
+// --------------------------------------------------------------- commit
+
+// The pass's rotated keys and values into the ring (o1b_ring_commit: row j
+// to slot (head0 + len0 + j) % wg), only the last wg rows since earlier ones
+// would be overwritten within the pass; then, by the last block to arrive
+// (an atomic ticket, no waiting), every group's meta after R pushes
+// (o1b_meta) and the position.
+__global__ __launch_bounds__(256) void k_commit(O1Args a, int rows_per_block) {
+    const int g = blockIdx.y;
+    const O1Meta mt = o1_meta(a, g);
+    const int rstart = max(0, a.R - mt.wg);
+    const int d4 = a.d >> 2, dv4 = a.dv >> 2;
+    for (int i = 0; i < rows_per_block; ++i) {
+        const int r = rstart + blockIdx.x * rows_per_block + i;
+        if (r >= a.R) break;
+        const int slot = (int)(((long long)mt.head0 + mt.len0 + r) % mt.wg);
+        const float4 *ks = (const float4 *)(a.kr + ((size_t)r * a.G + g) * a.d);
+        const float4 *vs = (const float4 *)(a.v + ((size_t)r * a.G + g) * a.dv);
+        float4 *kd = (float4 *)(a.ring_k + ((size_t)g * a.w + slot) * a.d);
+        float4 *vd = (float4 *)(a.ring_v + ((size_t)g * a.w + slot) * a.dv);
+        for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) kd[c4] = ks[c4];
+        for (int c4 = threadIdx.x; c4 < dv4; c4 += blockDim.x) vd[c4] = vs[c4];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned total = gridDim.x * gridDim.y;
+        const unsigned t = atomicAdd(&a.hdr->ticket, 1u);
+        if (t == total - 1) {
+            __threadfence();
+            for (int gg = 0; gg < a.G; ++gg) {
+                const long long len0 = a.meta[gg * 4 + 0], head0 = a.meta[gg * 4 + 1];
+                const long long wg = a.meta[gg * 4 + 3];
+                const long long tot = len0 + a.R;
+                if (tot <= wg) {
+                    a.meta[gg * 4 + 0] = (uint32_t)tot;
+                } else {
+                    const long long ev = tot - wg;
+                    a.meta[gg * 4 + 0] = (uint32_t)wg;
+                    a.meta[gg * 4 + 1] = (uint32_t)((head0 + ev) % wg);
+                    a.meta[gg * 4 + 2] = a.meta[gg * 4 + 2] + (uint32_t)ev;
+                }
+            }
+            a.hdr->pos += a.R;
+            a.hdr->ticket = 0u;
+        }
+    }
+}
+
+// ------------------------------------------------------------- launchers
+
+static size_t readout_smem() { return (size_t)(2 * 64 * 33 + 5 * 64 * 65 + 128) * sizeof(float); }
+
+static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
+
+cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st) {
+    static bool attrs_set = false;
+    if (!attrs_set) {
+        cudaFuncSetAttribute(k_far_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
+        cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attrs_set = true;
+    }
+    const int R = a.R;
+    const int nblk = (R + O1_SUB - 1) / O1_SUB;
+    k_rope<<<R, 128, 0, st>>>(a);
+    k_far_logits<<<dim3(nblk, a.nh), 256, 0, st>>>(a);
+    k_far_scan<<<(a.nh * a.m * 32 + 255) / 256, 256, 0, st>>>(a);
+    k_far_dT<<<dim3(nblk, a.nh, (a.dv + 63) / 64), 256, 0, st>>>(a);
+    const size_t n = (size_t)a.nh * a.m * a.dv;
+    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    k_far_readout<<<dim3(nblk, a.nh), 256, readout_smem(), st>>>(a);
+    const int RB = 32 / a.hpg;
+    const dim3 gn((R + RB - 1) / RB, a.G);
+    if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
+    else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+    const int rpb = 4;
+    const int live = R < a.w ? R : a.w;
+    k_commit<<<dim3((live + rpb - 1) / rpb, a.G), 128, 0, st>>>(a, rpb);
+    return cudaPeekAtLastError();
+}
+
+// Fresh far field and ring: M = -inf, Z = 0, T = 0, ring zeros.
+__global__ void k_init_state(O1Args a) {
+    const size_t nM = (size_t)a.nh * a.m;
+    const size_t nT = nM * a.dv;
+    const size_t nK = (size_t)a.G * a.w * a.d, nV = (size_t)a.G * a.w * a.dv;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nT + nK + nV + nM; i += stride) {
+        if (i < nM) {
+            a.M[i] = -INFINITY;
+            a.Z[i] = 0.f;
+        }
+        if (i < nT) a.T[i] = 0.f;
+        else if (i < nT + nK) a.ring_k[i - nT] = 0.f;
+        else if (i < nT + nK + nV) a.ring_v[i - nT - nK] = 0.f;
+    }
+}
+
+cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st) {
+    k_init_state<<<304, 256, 0, st>>>(a);
+    return cudaPeekAtLastError();
+}

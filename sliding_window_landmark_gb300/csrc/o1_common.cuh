@@ -1,0 +1,203 @@
+// Internals shared by the library's translation units: the device layout of a
+// state and of a call's scratch, the kernel argument block, and block-level
+// helpers. Nothing here is part of the C ABI (include/o1.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "o1.h"
+
+#define O1_MAGIC 0x4C53314Fu   // "O1SL"
+#define O1_VERSION 1u
+#define O1_SUB 64              // rows of one far-field reference block
+#define O1_MAX_D 256
+#define O1_MAX_DV 256
+#define O1_MAX_M 64
+#define O1_MAX_HPG 16
+#define O1_MAX_NS 255
+#define O1_MAX_W (1 << 20)
+
+// First bytes of a state buffer.
+struct O1Header {
+    uint32_t magic;
+    uint32_t version;
+    o1_geom geom;
+    int64_t pos;                       // absolute position of the next row
+    uint32_t ticket;                   // arrival counter of last-block commits; 0 between calls
+    uint32_t flags;
+    float inv_freq[O1_MAX_D / 2];      // rotary inverse frequencies (f32)
+};
+
+static inline size_t o1_al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Byte offsets of a state's parts. Per group: meta, ring, sinks, landmark
+// keys; per head: landmark queries, mu and the far field (M, Z, T).
+struct O1Layout {
+    size_t hdr, meta, ring_k, ring_v, sink_k, sink_v, kt, qt, mu, M, Z, T, total;
+};
+
+static inline O1Layout o1_layout(const o1_geom &g) {
+    const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, d = g.d, dv = g.dv,
+                 ns = g.sinks, w = g.window, m = g.landmarks;
+    O1Layout L;
+    size_t off = 0;
+    L.hdr = off;    off += o1_al256(sizeof(O1Header));
+    L.meta = off;   off += o1_al256(G * 4 * sizeof(uint32_t));
+    L.ring_k = off; off += o1_al256(G * w * d * 4);
+    L.ring_v = off; off += o1_al256(G * w * dv * 4);
+    L.sink_k = off; off += o1_al256(G * ns * d * 4);
+    L.sink_v = off; off += o1_al256(G * ns * dv * 4);
+    L.kt = off;     off += o1_al256(G * m * d * 4);
+    L.qt = off;     off += o1_al256(nh * m * d * 4);
+    L.mu = off;     off += o1_al256(nh * m * m * 4);
+    L.M = off;      off += o1_al256(nh * m * 4);
+    L.Z = off;      off += o1_al256(nh * m * 4);
+    L.T = off;      off += o1_al256(nh * m * dv * 4);
+    L.total = off;
+    return L;
+}
+
+// A chunk call's scratch for up to `cap` rows per pass (nsub = reference
+// blocks of O1_SUB rows):
+//   qr [cap][nh][d]  rotated queries        kr [cap][G][d]  rotated keys
+//   E  [nh][m][cap]  far logits, then exp(l - M_block) per evicted key
+//   P  [nh][m][cap]  far mass prefix per row
+//   Mc, Rc [nh][m][nsub]  block max and rescale factor
+//   Tp [nsub][nh][m][dv]  far value sums: increments, then the value sum
+//                         entering each block, rescaled to its max
+//   fh [cap][nh] x 4      per row-head far header (c_f, D, have, -)
+struct O1Scratch {
+    size_t qr, kr, E, P, Mc, Rc, Tp, fh, total;
+    int cap, nsub;
+};
+
+static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
+    const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, d = g.d, dv = g.dv,
+                 m = g.landmarks;
+    O1Scratch S;
+    S.cap = cap;
+    S.nsub = (cap + O1_SUB - 1) / O1_SUB;
+    size_t c = (size_t)cap, ns = (size_t)S.nsub, off = 0;
+    S.qr = off; off += o1_al256(c * nh * d * 4);
+    S.kr = off; off += o1_al256(c * G * d * 4);
+    S.E = off;  off += o1_al256(nh * m * c * 4);
+    S.P = off;  off += o1_al256(nh * m * c * 4);
+    S.Mc = off; off += o1_al256(nh * m * ns * 4);
+    S.Rc = off; off += o1_al256(nh * m * ns * 4);
+    S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
+    S.fh = off; off += o1_al256(c * nh * 4 * 4);
+    S.total = off;
+    return S;
+}
+
+// Everything a kernel of one pass needs, by value.
+struct O1Args {
+    int G, hpg, nh, d, dv, ns, w, m, rect, rotate;
+    float scale;
+    // state
+    O1Header *hdr;
+    uint32_t *meta;
+    float *ring_k, *ring_v;
+    const float *sink_k, *sink_v, *kt, *qt, *mu;
+    float *M, *Z, *T;
+    // this pass's rows
+    const float *q, *k, *v, *gate;
+    float *out;
+    int R, nsub;
+    // scratch
+    float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh;
+    int cap;
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// The ring window of group g at the start of a pass: len0 keys in logical
+// order from slot head0; wg = the group's window (meta slot 3).
+struct O1Meta {
+    int len0, head0, farl0, wg;
+};
+
+__device__ __forceinline__ O1Meta o1_meta(const O1Args &a, int g) {
+    O1Meta mt;
+    mt.len0 = (int)a.meta[g * 4 + 0];
+    mt.head0 = (int)a.meta[g * 4 + 1];
+    mt.farl0 = (int)a.meta[g * 4 + 2];
+    mt.wg = (int)a.meta[g * 4 + 3];
+    return mt;
+}
+
+// Key x of the sequence X = [ring in logical order] ++ [this pass's rows]:
+// the rotated key and the value.
+__device__ __forceinline__ const float *o1_key(const O1Args &a, int g, int x, const O1Meta &mt) {
+    return x < mt.len0 ? a.ring_k + ((size_t)g * a.w + (mt.head0 + x) % mt.wg) * a.d
+                       : a.kr + ((size_t)(x - mt.len0) * a.G + g) * a.d;
+}
+
+__device__ __forceinline__ const float *o1_val(const O1Args &a, int g, int x, const O1Meta &mt) {
+    return x < mt.len0 ? a.ring_v + ((size_t)g * a.w + (mt.head0 + x) % mt.wg) * a.dv
+                       : a.v + ((size_t)(x - mt.len0) * a.G + g) * a.dv;
+}
+
+// Block-level fp32 products on shared-memory tiles, 256 threads, a 64 x 64
+// output held as 4 x 4 per thread (rows ty + 16 i, columns tx + 16 j).
+//   nt: c[i][j] += sum_k A[row_i][k] * B[col_j][k]   (both K-contiguous)
+//   nn: c[i][j] += sum_k A[row_i][k] * B[k][col_j]
+// Odd leading dimensions keep the column reads free of bank conflicts.
+__device__ __forceinline__ void blk_nt(float (&c)[4][4], const float *A, int lda, const float *B,
+                                       int ldb, int K) {
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = A[(ty + 16 * i) * lda + k];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = B[(tx + 16 * j) * ldb + k];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
+    }
+}
+
+__device__ __forceinline__ void blk_nn(float (&c)[4][4], const float *A, int lda, const float *B,
+                                       int ldb, int K) {
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = A[(ty + 16 * i) * lda + k];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = B[k * ldb + tx + 16 * j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
+    }
+}
+
+__device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
+}
+
+// Launchers (o1_chunk.cu). Each returns cudaPeekAtLastError() after its launches.
+cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st);
+cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);

@@ -141,6 +141,25 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
                     const float *q, const float *k, const float *v, const float *gate,
                     float *out, void *stream);
 
+/* Stages of one chunk pass, in launch order; o1_chunk_attend_timed records
+ * an event before each and one after the last. */
+#define O1_NUM_STAGES 8
+
+/* o1_chunk_attend that also records caller-created CUDA events (cudaEvent_t
+ * handles, passed as void*) on `stream`: events[i] just before stage i of a
+ * pass and events[O1_NUM_STAGES] after its last stage, so that
+ * cudaEventElapsedTime(events[i], events[i + 1]) is stage i's time. With
+ * several passes (rows above the scratch's capacity) the events end up
+ * holding the last pass. n_events must be at least O1_NUM_STAGES + 1.
+ * Same arguments, checks and result as o1_chunk_attend otherwise. */
+O1_API int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                                 const float *q, const float *k, const float *v, const float *gate,
+                                 int32_t rows, float *out, void *const *events, int32_t n_events,
+                                 void *stream);
+
+/* Name of stage i of a chunk pass (NULL outside [0, O1_NUM_STAGES)). */
+O1_API const char *o1_stage_name(int32_t stage);
+
 /* Copy the state's mutable parts to host memory (NULL fields skipped).
  * Synchronises `stream`. Returns O1_ERR_STATE if the state's header does not
  * hold this geometry. */

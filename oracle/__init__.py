@@ -58,7 +58,7 @@ class _State(ctypes.Structure):
 
 
 class _Diag(ctypes.Structure):
-    _fields_ = [("have", _P), ("far_den", _P), ("far_abs", _P)]
+    _fields_ = [("have", _P), ("far_den", _P), ("far_abs", _P), ("den", _P)]
 
 
 def load_library(path: str):
@@ -157,7 +157,7 @@ class OracleLayer:
 
     def rows(self, q, k, v, gate=None, threads: int = 1, diag: bool = False):
         """Advance by ``rows`` rows; returns out [rows][nh][dv] (float64), and
-        with ``diag`` also (have, far_den, far_abs) per (row, head)."""
+        with ``diag`` also (have, far_den, far_abs, den) per (row, head)."""
         g = self.geom
         q = np.ascontiguousarray(q, dtype=np.float32)
         rows = q.shape[0]
@@ -170,7 +170,8 @@ class OracleLayer:
         dg = None
         dgp = None
         if diag:
-            dg = (np.zeros((rows, g.nh), dtype=np.int8), np.zeros((rows, g.nh)), np.zeros((rows, g.nh)))
+            dg = (np.zeros((rows, g.nh), dtype=np.int8), np.zeros((rows, g.nh)), np.zeros((rows, g.nh)),
+                  np.zeros((rows, g.nh)))
             dgp = ctypes.byref(_Diag(*[_ptr(a) for a in dg]))
         if rows > 0:
             self.threads_used = self._lib.oo_rows(ctypes.byref(self._g), ctypes.byref(self._st),

@@ -73,11 +73,14 @@ typedef struct {
 
 /* Optional per-(row, head) diagnostics: the far-field sign decision and its
  * margin, so that rows whose decision sits within rounding of zero can be
- * told apart. Any pointer may be NULL. */
+ * told apart, and the denominator, whose size against sum_b |gain_b Z_b|
+ * says how much a relative error in the far terms grows in the output.
+ * Any pointer may be NULL. */
 typedef struct {
     int8_t *have;     /* [rows][nh] 1 if the far part was kept          */
     double *far_den;  /* [rows][nh] D before the sign test (e^-c units)  */
     double *far_abs;  /* [rows][nh] sum_b |gain_b Z_b| (e^-c units)      */
+    double *den;      /* [rows][nh] the row's denominator after the floor  */
 } oo_diag;
 
 /* Rotary table for one position: cs[j], sn[j], j < d/2, both rounded to f32
@@ -302,6 +305,7 @@ static void oo_group_rows(oo_job *jb)
                 for (int t = 0; t < dv; t++) num[t] += pw * vx[t];
             }
             if (den < 1e-30) den = 1e-30;
+            if (jb->diag && jb->diag->den) jb->diag->den[(size_t)r * nh + gh] = den;
 
             /* 5. gate, and the row's output */
             double *o = jb->out + ((size_t)r * nh + gh) * dv;

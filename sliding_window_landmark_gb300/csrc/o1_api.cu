@@ -6,6 +6,8 @@
 
 #include "o1_common.cuh"
 
+extern const char *const o1_stage_names[O1_NUM_STAGES];
+
 namespace {
 
 bool geom_ok(const o1_geom *g) {
@@ -82,7 +84,8 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
 }
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
-          const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream) {
+          const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream,
+          cudaEvent_t const *ev = nullptr) {
     if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
     if (rows < 0) return O1_ERR_ARG;
     if (rows == 0) return O1_OK;
@@ -117,7 +120,7 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
         a.out = out + (size_t)r0 * nh * g.dv;
         a.R = R;
         a.nsub = S.nsub;
-        if (o1_launch_pass(a, st) != cudaSuccess) return O1_ERR_CUDA;
+        if (o1_launch_pass(a, st, ev) != cudaSuccess) return O1_ERR_CUDA;
     }
     return O1_OK;
 }
@@ -201,6 +204,20 @@ int o1_state_init(void *state, const o1_geom *geom, const int32_t *group_windows
 int o1_chunk_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
                     const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream) {
     return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream);
+}
+
+int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                          const float *q, const float *k, const float *v, const float *gate, int32_t rows,
+                          float *out, void *const *events, int32_t n_events, void *stream) {
+    if (!events || n_events < O1_NUM_STAGES + 1) return O1_ERR_ARG;
+    for (int i = 0; i <= O1_NUM_STAGES; ++i)
+        if (!events[i]) return O1_ERR_ARG;
+    return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream,
+                 (cudaEvent_t const *)events);
+}
+
+const char *o1_stage_name(int32_t stage) {
+    return (stage >= 0 && stage < O1_NUM_STAGES) ? o1_stage_names[stage] : nullptr;
 }
 
 int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,

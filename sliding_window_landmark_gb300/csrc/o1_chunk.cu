@@ -615,11 +615,14 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a, int rows_per_block) {
 
 // ------------------------------------------------------------- launchers
 
+extern const char *const o1_stage_names[O1_NUM_STAGES] = {"rope", "far_logits", "far_scan", "far_dT",
+                                                   "far_tscan", "far_readout", "near", "commit"};
+
 static size_t readout_smem() { return (size_t)(2 * 64 * 33 + 5 * 64 * 65 + 128) * sizeof(float); }
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
-cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st) {
+cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
     static bool attrs_set = false;
     if (!attrs_set) {
         cudaFuncSetAttribute(k_far_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
@@ -629,20 +632,34 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st) {
     }
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
+    int stage = 0;
+    auto mark = [&]() {
+        if (ev) cudaEventRecord(ev[stage], st);
+        ++stage;
+    };
+    mark();
     k_rope<<<R, 128, 0, st>>>(a);
+    mark();
     k_far_logits<<<dim3(nblk, a.nh), 256, 0, st>>>(a);
+    mark();
     k_far_scan<<<(a.nh * a.m * 32 + 255) / 256, 256, 0, st>>>(a);
+    mark();
     k_far_dT<<<dim3(nblk, a.nh, (a.dv + 63) / 64), 256, 0, st>>>(a);
+    mark();
     const size_t n = (size_t)a.nh * a.m * a.dv;
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    mark();
     k_far_readout<<<dim3(nblk, a.nh), 256, readout_smem(), st>>>(a);
+    mark();
     const int RB = 32 / a.hpg;
     const dim3 gn((R + RB - 1) / RB, a.G);
     if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
     else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+    mark();
     const int rpb = 4;
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + rpb - 1) / rpb, a.G), 128, 0, st>>>(a, rpb);
+    mark();
     return cudaPeekAtLastError();
 }
 

@@ -199,5 +199,6 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 }
 
 // Launchers (o1_chunk.cu). Each returns cudaPeekAtLastError() after its launches.
-cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st);
+// `ev` may be null; otherwise O1_NUM_STAGES + 1 events recorded around the stages.
+cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);

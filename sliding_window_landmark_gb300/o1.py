@@ -65,6 +65,11 @@ def _load(path: str | None = None):
     lib.o1_state_init.restype = ctypes.c_int
     lib.o1_chunk_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP]
     lib.o1_chunk_attend.restype = ctypes.c_int
+    lib.o1_chunk_attend_timed.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, ctypes.c_int32,
+                                          _VP, ctypes.POINTER(_VP), ctypes.c_int32, _VP]
+    lib.o1_chunk_attend_timed.restype = ctypes.c_int
+    lib.o1_stage_name.argtypes = [ctypes.c_int32]
+    lib.o1_stage_name.restype = ctypes.c_char_p
     lib.o1_token_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.o1_token_attend.restype = ctypes.c_int
     lib.o1_state_read.argtypes = [_VP, _G, ctypes.POINTER(o1_state_host), _VP]
@@ -150,6 +155,27 @@ def o1_chunk_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, s
         scratch.numel() * scratch.element_size(),
         _dev(q, rows * nh * g.d, "q"), _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"),
         _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
+
+
+O1_NUM_STAGES = 8
+
+
+def o1_stage_name(stage: int):
+    n = LIB.o1_stage_name(int(stage))
+    return None if n is None else n.decode()
+
+
+def o1_chunk_attend_timed(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, events, stream=None) -> int:
+    """``events``: O1_NUM_STAGES + 1 torch.cuda.Event(enable_timing=True), each
+    already recorded once (so that its CUDA handle exists)."""
+    nh, G = g.nh, g.groups
+    arr = (_VP * len(events))(*[_VP(int(e.cuda_event)) for e in events])
+    return LIB.o1_chunk_attend_timed(
+        _dev(state, None, "state", dtype=None), ctypes.byref(g), _dev(scratch, None, "scratch", dtype=None),
+        scratch.numel() * scratch.element_size(),
+        _dev(q, rows * nh * g.d, "q"), _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"),
+        _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), arr, len(events),
+        _stream(stream))
 
 
 def o1_token_attend(state, g: o1_geom, scratch, q, k, v, gate, out, stream=None) -> int:

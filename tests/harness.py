@@ -8,6 +8,15 @@ formed differently on each side). Rows whose far-field sign decision sits
 within rounding of zero in the oracle (|D| <= 1e-5 sum_b |gain_b Z_b|) are
 counted and reported, not compared: there the output is discontinuous in
 the inputs and either side of the decision is a correct result.
+
+Conditioning. With signed mu the far terms can cancel, and the row's
+denominator den can be far smaller than A = sum_b |gain_b| Z_b. An fp32
+path carries a relative error of about EPS_FAR = 1e-6 on each far term (the
+logits are fp32 dots of f32-rounded rotated keys), which reaches the output
+as about EPS_FAR * kappa * (|o| + max|v|), kappa = A / den. Up to
+kappa = KAPPA_MAX = 100 that stays inside the tolerance above, so those rows
+get the strict check; rows above it are checked against the kappa-scaled
+bound instead, and counted.
 """
 from __future__ import annotations
 
@@ -18,6 +27,8 @@ from sliding_window_landmark_gb300 import synth
 
 ATOL, RTOL = 2e-4, 1e-4
 FLIP_MARGIN = 1e-5
+EPS_FAR = 1e-6
+KAPPA_MAX = 100.0
 
 
 def oracle_layer(shape: synth.Shape, consts, rect=False, scale=None, pos0=0):
@@ -80,23 +91,39 @@ class GpuLayer:
 
 
 def flip_rows(diag):
-    have, D, Dabs = diag
+    have, D, Dabs = diag[:3]
     return (Dabs > 0) & (np.abs(D) <= FLIP_MARGIN * Dabs)
 
 
-def assert_outputs(got, want, diag=None, what=""):
-    """Element-wise tolerance outside rows with a flip-prone far decision."""
+def kappa(diag):
+    return diag[2] / diag[3]
+
+
+def assert_outputs(got, want, diag=None, what="", vmax=5.0):
+    """Strict element-wise tolerance where kappa <= KAPPA_MAX, the
+    kappa-scaled bound above it, nothing at flip-prone rows."""
     got = np.asarray(got, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
-    skip = np.zeros(want.shape[:2], dtype=bool) if diag is None else flip_rows(diag)
+    rows = want.shape[:2]
+    skip = np.zeros(rows, dtype=bool) if diag is None else flip_rows(diag)
+    kap = np.zeros(rows) if diag is None else kappa(diag)
+    ill = (kap > KAPPA_MAX) & ~skip
     err = np.abs(got - want)
-    bad = (err > ATOL + RTOL * np.abs(want)) & ~skip[..., None]
+    tol = ATOL + RTOL * np.abs(want)
+    tol_ill = tol + EPS_FAR * kap[..., None] * (np.abs(want) + vmax)
+    bad = np.where(ill[..., None], err > tol_ill, err > tol) & ~skip[..., None]
     if bad.any():
         idx = np.argwhere(bad)[:5]
-        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance, first {idx.tolist()}, "
-                             f"max abs err {err[~skip].max():.3e}")
-    return {"max_abs": float(err[~skip].max()) if (~skip).any() else 0.0, "flip_rows": int(skip.sum()),
+        info = [(tuple(i), float(err[tuple(i)]), float(want[tuple(i)]), float(kap[tuple(i[:2])])) for i in idx]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; first (index, err, oracle, kappa) "
+                             f"{info}; max abs err {err[~skip].max():.3e}; rows with kappa > {KAPPA_MAX}: "
+                             f"{int(ill.sum())}, max kappa {kap.max():.3g}")
+    strict = ~skip & ~ill
+    return {"max_abs": float(err[strict].max()) if strict.any() else 0.0,
+            "max_rel_to_tol": float((err / tol)[strict].max()) if strict.any() else 0.0,
+            "flip_rows": int(skip.sum()), "ill_conditioned_rows": int(ill.sum()),
+            "max_kappa": float(kap.max()),
             "have_frac": float(diag[0].mean()) if diag is not None else None}
 
 

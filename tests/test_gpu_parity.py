@@ -173,3 +173,29 @@ def test_qwen_layer_decode_after_8192():
 def test_qwen_long_prompt_group_windows():
     st = _run(synth.QWEN_LONG, 3, [32768], check_state=True)
     print("32768-row prompt:", st)
+
+
+def test_qwen_long_prompt_nonnegative_mu():
+    """mu >= 0: the far mass cannot cancel (kappa <= 1), so every row gets the
+    strict tolerance."""
+    st = _run(synth.QWEN_LONG, 4, [32768], mu_abs=True)
+    assert st[0]["ill_conditioned_rows"] == 0 and st[0]["flip_rows"] == 0
+    print("32768-row prompt, mu >= 0:", st)
+
+
+@pytest.mark.parametrize("layer", [0, 23])
+def test_stack_layer_prompt(layer):
+    """A layer of the 24-layer stack (4 KV groups x 4 heads, d = dv = 128,
+    window 1024, 64 landmarks): the 65536-row prompt of its own seed."""
+    sh = synth.STACK_LAYER
+    seed = 1000 + layer
+    c = synth.layer_constants(sh, seed)
+    orc = harness.oracle_layer(sh, c)
+    gpu = harness.GpuLayer(sh, c, max_rows=16384)
+    stats = []
+    for r0 in range(0, 65536, 16384):
+        q, k, v, g = synth.layer_rows(sh, seed, r0, 16384)
+        want, diag = orc.rows(q, k, v, g, threads=sh.groups, diag=True)
+        stats.append(harness.assert_outputs(gpu.rows(q, k, v, g), want, diag, f"layer {layer} rows {r0}"))
+    harness.assert_state(gpu.read(), orc, f"layer {layer}")
+    print(f"stack layer {layer}:", stats)

@@ -183,7 +183,7 @@ def test_brute_force_far_algebra(case, lib=None):
     outs, haves = [], []
     r0 = 0
     for n in splits:
-        o, (hv, _, _) = lay.rows(q[r0:r0 + n], k[r0:r0 + n], v[r0:r0 + n], gate[r0:r0 + n], diag=True)
+        o, (hv, _, _, _) = lay.rows(q[r0:r0 + n], k[r0:r0 + n], v[r0:r0 + n], gate[r0:r0 + n], diag=True)
         outs.append(o)
         haves.append(hv)
         r0 += n
@@ -302,7 +302,7 @@ def test_forced_far_branches(lib=None):
         lay, _, g = _layer(sh, 9, rect=rect, consts=c, lib=lib)
         rows = 20
         q, k, v, gate = synth.layer_rows(sh, 9, 0, rows)
-        got, (have, D, _) = lay.rows(q, k, v, gate, diag=True)
+        got, (have, D, _, _) = lay.rows(q, k, v, gate, diag=True)
         scale = g.scale_f32()
         for r in range(rows):
             lo = max(0, r + 1 - 5)

@@ -160,6 +160,29 @@ O1_API int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch
 /* Name of stage i of a chunk pass (NULL outside [0, O1_NUM_STAGES)). */
 O1_API const char *o1_stage_name(int32_t stage);
 
+/* Size of the library's own device scratch used by o1_token_attend_noalloc:
+ * 4 MiB, held by every GPU that loads the library until the process exits. */
+#define O1_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* o1_token_attend for callers that cannot allocate device memory: no
+ * scratch argument, no cudaMalloc, cudaFree or allocating library call.
+ * For a plugin whose interface hands over no workspace, or a decode loop
+ * that must not call cudaMalloc (it can synchronise the device and stall
+ * other streams) nor keep a buffer of its own. The paper has no
+ * counterpart; this is a convenience of this library.
+ *   q, k, v, gate, out, state, stream: as o1_token_attend.
+ * The scratch is one static device array of O1_NOALLOC_SCRATCH_BYTES in
+ * this library, shared by every call on a device: calls that overlap on
+ * the GPU (other streams, other threads) race on it, so serialise them.
+ * Nothing in it needs to start at zero: a call writes every scratch value
+ * before reading it. The first call on each device looks the array's
+ * device address up (cudaGetSymbolAddress, that device current); make that
+ * first call before any stream capture. Returns O1_ERR_UNSUPPORTED when the
+ * geometry's one-row scratch exceeds O1_NOALLOC_SCRATCH_BYTES, else as
+ * o1_token_attend. */
+O1_API int o1_token_attend_noalloc(void *state, const o1_geom *geom, const float *q, const float *k,
+                                   const float *v, const float *gate, float *out, void *stream);
+
 /* Copy the state's mutable parts to host memory (NULL fields skipped).
  * Synchronises `stream`. Returns O1_ERR_STATE if the state's header does not
  * hold this geometry. */

@@ -4,7 +4,13 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "o1_common.cuh"
+
+// Scratch of o1_token_attend_noalloc: a file-scope device array, so that the
+// entry point allocates nothing. Every call on a device shares it.
+static __device__ __align__(256) unsigned char o1_noalloc_scratch[O1_NOALLOC_SCRATCH_BYTES];
 
 extern const char *const o1_stage_names[O1_NUM_STAGES];
 
@@ -134,6 +140,25 @@ int check_header(const void *state, const o1_geom &g, cudaStream_t st) {
     return O1_OK;
 }
 
+// Device address of o1_noalloc_scratch on the current device, looked up once
+// per device. In host code the array's name is only a host-side stand-in,
+// never a device address.
+int noalloc_scratch(void **out) {
+    static std::mutex mu;
+    static void *addr[256];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return O1_ERR_CUDA;
+    if (dev < 0 || dev >= 256) return O1_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, o1_noalloc_scratch) != cudaSuccess || !p) return O1_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return O1_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -223,6 +248,17 @@ const char *o1_stage_name(int32_t stage) {
 int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
                     const float *k, const float *v, const float *gate, float *out, void *stream) {
     return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, 1, out, stream);
+}
+
+int o1_token_attend_noalloc(void *state, const o1_geom *geom, const float *q, const float *k, const float *v,
+                            const float *gate, float *out, void *stream) {
+    if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
+    if (o1_scratch_layout(*geom, 1).total > (size_t)O1_NOALLOC_SCRATCH_BYTES) return O1_ERR_UNSUPPORTED;
+    if (!state || !q || !k || !v || !out) return O1_ERR_ARG;
+    void *scratch = nullptr;
+    const int st = noalloc_scratch(&scratch);
+    if (st != O1_OK) return st;
+    return chunk(state, geom, scratch, O1_NOALLOC_SCRATCH_BYTES, q, k, v, gate, 1, out, stream);
 }
 
 int o1_state_read(const void *state, const o1_geom *geom, o1_state_host *dst, void *stream) {

@@ -72,6 +72,8 @@ def _load(path: str | None = None):
     lib.o1_stage_name.restype = ctypes.c_char_p
     lib.o1_token_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.o1_token_attend.restype = ctypes.c_int
+    lib.o1_token_attend_noalloc.argtypes = [_VP, _G, _VP, _VP, _VP, _VP, _VP, _VP]
+    lib.o1_token_attend_noalloc.restype = ctypes.c_int
     lib.o1_state_read.argtypes = [_VP, _G, ctypes.POINTER(o1_state_host), _VP]
     lib.o1_state_read.restype = ctypes.c_int
     lib.o1_state_write.argtypes = [_VP, _G, ctypes.POINTER(o1_state_host), _VP]
@@ -183,6 +185,19 @@ def o1_token_attend(state, g: o1_geom, scratch, q, k, v, gate, out, stream=None)
     return LIB.o1_token_attend(
         _dev(state, None, "state", dtype=None), ctypes.byref(g), _dev(scratch, None, "scratch", dtype=None),
         scratch.numel() * scratch.element_size(),
+        _dev(q, nh * g.d, "q"), _dev(k, G * g.d, "k"), _dev(v, G * g.dv, "v"),
+        _dev(gate, nh * g.dv, "gate"), _dev(out, nh * g.dv, "out"), _stream(stream))
+
+
+O1_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def o1_token_attend_noalloc(state, g: o1_geom, q, k, v, gate, out, stream=None) -> int:
+    """o1_token_attend without a scratch argument: the library's own static
+    device scratch is used (see include/o1.h)."""
+    nh, G = g.nh, g.groups
+    return LIB.o1_token_attend_noalloc(
+        _dev(state, None, "state", dtype=None), ctypes.byref(g),
         _dev(q, nh * g.d, "q"), _dev(k, G * g.d, "k"), _dev(v, G * g.dv, "v"),
         _dev(gate, nh * g.dv, "gate"), _dev(out, nh * g.dv, "out"), _stream(stream))
 

@@ -112,11 +112,29 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
         overlaps(v, (size_t)rows * g.groups * g.dv * 4) || overlaps(gate, (size_t)rows * nh * g.dv * 4))
         return O1_ERR_ARG;
     const int cap = scratch_cap(g, scratch_bytes);
-    if (cap < 1) return O1_ERR_ARG;
+    if (cap < 1 || scratch_bytes < o1_tok_layout(g).total) return O1_ERR_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     O1Args a = state_args(state, g);
     for (int r0 = 0; r0 < rows; r0 += cap) {
         const int R = rows - r0 < cap ? rows - r0 : cap;
+        if (R == 1 && !ev) {
+            // one row: the decode path
+            const O1TokScratch T = o1_tok_layout(g);
+            char *sb = (char *)scratch;
+            a.part = (float *)(sb + T.part);
+            a.farp = (float *)(sb + T.farp);
+            a.kcur = (float *)(sb + T.kcur);
+            a.KC = T.KC;
+            a.NC = T.NC;
+            a.q = q + (size_t)r0 * nh * g.d;
+            a.k = k + (size_t)r0 * g.groups * g.d;
+            a.v = v + (size_t)r0 * g.groups * g.dv;
+            a.gate = gate ? gate + (size_t)r0 * nh * g.dv : nullptr;
+            a.out = out + (size_t)r0 * nh * g.dv;
+            a.R = 1;
+            if (o1_launch_token(a, st) != cudaSuccess) return O1_ERR_CUDA;
+            continue;
+        }
         const O1Scratch S = o1_scratch_layout(g, R);
         scratch_args(a, scratch, S);
         a.q = q + (size_t)r0 * nh * g.d;
@@ -170,7 +188,7 @@ size_t o1_state_bytes(const o1_geom *geom) {
 
 size_t o1_scratch_bytes(const o1_geom *geom, int32_t max_rows) {
     if (!geom_ok(geom) || max_rows < 1) return 0;
-    return o1_scratch_layout(*geom, max_rows).total;
+    return o1_scratch_need(*geom, max_rows);
 }
 
 int o1_state_init(void *state, const o1_geom *geom, const int32_t *group_windows, const float *sink_k,
@@ -253,7 +271,7 @@ int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size_t scra
 int o1_token_attend_noalloc(void *state, const o1_geom *geom, const float *q, const float *k, const float *v,
                             const float *gate, float *out, void *stream) {
     if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
-    if (o1_scratch_layout(*geom, 1).total > (size_t)O1_NOALLOC_SCRATCH_BYTES) return O1_ERR_UNSUPPORTED;
+    if (o1_scratch_need(*geom, 1) > (size_t)O1_NOALLOC_SCRATCH_BYTES) return O1_ERR_UNSUPPORTED;
     if (!state || !q || !k || !v || !out) return O1_ERR_ARG;
     void *scratch = nullptr;
     const int st = noalloc_scratch(&scratch);

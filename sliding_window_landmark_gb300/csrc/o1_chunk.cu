@@ -36,29 +36,15 @@
 // ------------------------------------------------------------------ rope
 
 // One block per row. Thread j < d/2 forms the angle of pair (j, j + d/2)
-// once and rotates every query head and every key group with it. The angle
-// p * inv[j] is formed in double (inv is f32, as the pages' table input),
-// reduced by 2 pi in two parts (Cody-Waite), and its sine and cosine are
-// taken in f32 with a first-order correction for the reduced angle's
-// rounding: within a few f32 ulp of the pages' f64-then-f32 table.
+// once (o1_rope_cs: within a few f32 ulp of the pages' f64-then-f32 table)
+// and rotates every query head and every key group with it.
 __global__ void k_rope(O1Args a) {
     const int r = blockIdx.x;
     const int half = a.d >> 1;
     const int64_t p = a.hdr->pos + r;
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
         float c = 1.f, s = 0.f;
-        if (a.rotate) {
-            const double ang = (double)p * (double)a.hdr->inv_freq[j];
-            const double kq = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
-            double red = fma(-kq, 6.283185307179586, ang);        // 2 pi, high part
-            red = fma(-kq, 2.4492935982947064e-16, red);          // 2 pi, low part
-            const float rf = (float)red;
-            const float rl = (float)(red - (double)rf);
-            float sf, cf;
-            sincosf(rf, &sf, &cf);
-            c = cf - sf * rl;
-            s = sf + cf * rl;
-        }
+        if (a.rotate) o1_rope_cs(a.hdr->inv_freq[j], p, c, s);
         for (int hh = 0; hh < a.nh; ++hh) {
             const size_t o = ((size_t)r * a.nh + hh) * a.d;
             const float x0 = a.q[o + j], x1 = a.q[o + j + half];

@@ -92,6 +92,40 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     return S;
 }
 
+// Scratch of the one-row path: near partials per (group, key slice, head)
+// = (max, sum, value sum [dv]); the far part per head = (c_f, D, have, -,
+// numerator [dv]); the row's rotated key per group. KC keys per slice, NC
+// slices per group, sized for the longest near set (sinks + window) so that
+// about two blocks per SM share the key reads.
+struct O1TokScratch {
+    size_t part, farp, kcur, total;
+    int KC, NC;
+};
+
+static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
+    const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, dv = g.dv, d = g.d;
+    const long long nmax = (long long)g.sinks + g.window;
+    long long kc = (G * nmax + 303) / 304;
+    kc = kc < 8 ? 8 : (kc + 7) / 8 * 8;
+    O1TokScratch S;
+    S.KC = (int)kc;
+    S.NC = (int)((nmax + kc - 1) / kc);
+    size_t off = 0;
+    S.part = off; off += o1_al256(G * S.NC * g.heads_per_group * (2 + dv) * 4);
+    S.farp = off; off += o1_al256(nh * (4 + dv) * 4);
+    S.kcur = off; off += o1_al256(G * d * 4);
+    S.total = off;
+    return S;
+}
+
+// Scratch that lets a call run passes of up to `rows` rows, a one-row pass
+// (the decode path) included.
+static inline size_t o1_scratch_need(const o1_geom &g, int rows) {
+    const size_t c = o1_scratch_layout(g, rows).total;
+    const size_t t = o1_tok_layout(g).total;
+    return c > t ? c : t;
+}
+
 // Everything a kernel of one pass needs, by value.
 struct O1Args {
     int G, hpg, nh, d, dv, ns, w, m, rect, rotate;
@@ -109,9 +143,29 @@ struct O1Args {
     // scratch
     float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh;
     int cap;
+    // one-row path scratch
+    float *part, *farp, *kcur;
+    int KC, NC;
 };
 
 // ---------------------------------------------------------------- helpers
+
+// Rotary cos/sin of pair j at position p: the angle p * inv[j] is formed in
+// double (inv is f32), reduced by 2 pi in two parts (Cody-Waite), and its
+// sine and cosine are taken in f32 with a first-order correction for the
+// reduced angle's rounding.
+__device__ __forceinline__ void o1_rope_cs(float inv, long long p, float &c, float &s) {
+    const double ang = (double)p * (double)inv;
+    const double kq = rint(ang * 0.15915494309189535);   // 1 / (2 pi)
+    double red = fma(-kq, 6.283185307179586, ang);        // 2 pi, high part
+    red = fma(-kq, 2.4492935982947064e-16, red);          // 2 pi, low part
+    const float rf = (float)red;
+    const float rl = (float)(red - (double)rf);
+    float sf, cf;
+    sincosf(rf, &sf, &cf);
+    c = cf - sf * rl;
+    s = sf + cf * rl;
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -202,3 +256,5 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 // `ev` may be null; otherwise O1_NUM_STAGES + 1 events recorded around the stages.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);
+// One row (o1_token.cu): main kernel + merge kernel.
+cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st);

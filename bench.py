@@ -48,16 +48,20 @@ FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12   # SMs x FP32 lanes x 2 flop 
 
 # ------------------------------------------------------------------ helpers
 
-def near_flops(shape: synth.Shape, rows: int, len0: int = 0) -> float:
-    """Algorithmic flops of the near part: 2 (ns + window_r) (d + dv) per
-    row-head, window_r = min(wg, len0 + r + 1)."""
+def window_flops(shape: synth.Shape, rows: int, len0: int = 0) -> float:
+    """Algorithmic flops of the window attention: 2 window_r (d + dv) per
+    row-head (q.k and p.v over the row's window keys),
+    window_r = min(wg, len0 + r + 1)."""
     wins = shape.group_windows or (shape.window,) * shape.groups
     r = np.arange(rows)
     tot = 0.0
     for wg in wins:
-        tot += shape.heads_per_group * float(np.sum(2.0 * (shape.sinks + np.minimum(wg, len0 + r + 1))
-                                                    * (shape.d + shape.dv)))
+        tot += shape.heads_per_group * float(np.sum(2.0 * np.minimum(wg, len0 + r + 1) * (shape.d + shape.dv)))
     return tot
+
+
+def tensor_core_window(shape: synth.Shape) -> bool:
+    return shape.d % 64 == 0 and shape.d <= 256 and shape.dv % 32 == 0 and shape.dv <= 256 and shape.window >= 512
 
 
 def decode_bytes(shape: synth.Shape) -> float:
@@ -367,17 +371,32 @@ def our_arm(args, rank, world, local_rank):
     dec_launches = 2
     dec_bytes = decode_bytes(sh)
 
-    # ---- roofline of the dominant kernel (near attention)
+    # ---- roofline of the dominant kernel (the window attention)
     pk_, src = peaks()
-    near_idx = 6
-    near_ms = float(stage_avg[near_idx])
-    flops = near_flops(sh, ROWS)
+    names = [o1.o1_stage_name(j) for j in range(nst)]
+    near_ms = float(stage_avg[names.index("near")])
+    flops = window_flops(sh, ROWS)
     ach = flops / (near_ms * 1e-3) / 1e12
-    traffic = traffic_record("k_near")
-    roof = {"kernel": "k_near (near attention, fp32 CUDA cores)", "bound": "alu", "achieved": ach,
-            "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": traffic,
-            "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz",
-            "algorithmic_flops_per_launch": flops, "launch_ms": near_ms}
+    if tensor_core_window(sh):
+        # fp16 tensor cores (same dense rate as bf16); each fp32 product costs
+        # three fp16 products (hi.hi + hi.lo + lo.hi), so peak / 3 is this
+        # formulation's own ceiling
+        peak = pk_["bf16_tflops"]
+        traffic = traffic_record("k_near_tc")
+        roof = {"kernel": "k_near_tc (window attention, tcgen05 kind::f16, 3-term fp16 split)",
+                "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": traffic,
+                "peak_source": f"{src} bf16 burst (dense fp16 runs at the bf16 rate)",
+                "issued_tensor_tflops": 3 * ach, "frac_of_split_ceiling": 3 * ach / peak,
+                "algorithmic_flops_per_launch": flops, "launch_ms": near_ms}
+        launches = nst
+    else:
+        traffic = traffic_record("k_near")
+        roof = {"kernel": "k_near (window attention, fp32 CUDA cores)", "bound": "alu", "achieved": ach,
+                "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": traffic,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz",
+                "algorithmic_flops_per_launch": flops, "launch_ms": near_ms}
+        launches = nst - 1   # no panel gather
 
     rows_total = ROWS * args.steps * world
     value = rows_total / (ms_max * 1e-3)
@@ -391,7 +410,7 @@ def our_arm(args, rank, world, local_rank):
                        "step": "device copy of the fresh state + o1_chunk_attend(rows=4096)"},
             "roofline": roof,
             "stages_ms": {o1.o1_stage_name(j): float(stage_avg[j]) for j in range(nst)},
-            "gpu_launches": nst * args.steps,
+            "gpu_launches": launches * args.steps,
             "e2e": {"value": ROWS * args.steps * world / (e2e_ms * 1e-3), "unit": "rows/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "decode": {"metric": "sealed-layer decode us/token", "value": dec_us, "unit": "us/token",

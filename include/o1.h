@@ -63,7 +63,7 @@ enum {
 /* Geometry of one sealed layer ("cortiq-engine 0.8.51 src/gpu_wgpu/o1_batch.rs",
  * struct Geom). Limits: groups >= 1, heads_per_group in [1, 16],
  * d in [8, 256] with d % 8 == 0, dv in [4, 256] with dv % 4 == 0,
- * sinks in [0, 255], window in [1, 1 << 20], landmarks in [1, 64]. */
+ * sinks in [0, 64], window in [1, 1 << 20], landmarks in [1, 64]. */
 typedef struct o1_geom {
     int32_t groups;           /* G: KV groups                                  */
     int32_t heads_per_group;  /* hpg: query heads per KV group (nh = G * hpg)  */
@@ -126,7 +126,14 @@ O1_API int o1_state_init(void *state, const o1_geom *geom, const int32_t *group_
  *   out   device [rows][G*hpg][dv] o / (1 + exp(-gate)); must not alias q/k/v/gate
  *   scratch, scratch_bytes  device scratch, at least o1_scratch_bytes(geom, 1)
  * The output equals the rows processed one at a time (rope, far insert, ring
- * push, attend, gate), up to rounding. Asynchronous. */
+ * push, attend, gate), up to rounding. Asynchronous.
+ * Window path: when d % 64 == 0, d <= 256, dv % 32 == 0, dv <= 256 and
+ * window >= 512, the window part of a pass with two or more rows runs on the
+ * tensor cores, each fp32 operand split into two fp16 halves (hi + lo, three
+ * products). It needs every rotated query, rotated key and value to lie
+ * inside the fp16 range (|x| < 65504); one outside it raises
+ * O1_FLAG_FP16_RANGE in the state's flags and that pass's output is not
+ * valid. Other geometries, and one-row passes, run in fp32 throughout. */
 O1_API int o1_chunk_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                     const float *q, const float *k, const float *v, const float *gate,
                     int32_t rows, float *out, void *stream);
@@ -142,8 +149,10 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
                     float *out, void *stream);
 
 /* Stages of one chunk pass, in launch order; o1_chunk_attend_timed records
- * an event before each and one after the last. */
-#define O1_NUM_STAGES 8
+ * an event before each and one after the last. A stage that does not apply
+ * to the geometry (the fp16 panel gather of the tensor-core window path)
+ * launches nothing and times as empty. */
+#define O1_NUM_STAGES 9
 
 /* o1_chunk_attend that also records caller-created CUDA events (cudaEvent_t
  * handles, passed as void*) on `stream`: events[i] just before stage i of a
@@ -193,6 +202,17 @@ O1_API int o1_state_read(const void *state, const o1_geom *geom, o1_state_host *
  * state consistent (len <= group window, head < group window, M = -inf
  * exactly where farl == 0, ...). */
 O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host *src, void *stream);
+
+/* Sticky conditions a kernel records in the state header (bits of the value
+ * o1_state_flags returns). */
+#define O1_FLAG_WAIT_EXPIRED 1u  /* a bounded in-kernel wait ran out (about 2 s);
+                                    that pass's output is incomplete      */
+#define O1_FLAG_FP16_RANGE 2u    /* an operand of the tensor-core window path
+                                    was outside the fp16 range             */
+
+/* Read the state's flags into *flags (host) and, if `clear` is non-zero,
+ * reset them to 0. Synchronises `stream`. */
+O1_API int o1_state_flags(void *state, const o1_geom *geom, uint32_t *flags, int32_t clear, void *stream);
 
 /* A static, human-readable name for a status code. */
 O1_API const char *o1_status_string(int status);

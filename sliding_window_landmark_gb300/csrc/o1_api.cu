@@ -87,6 +87,10 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.Tp = (float *)(b + S.Tp);
     a.fh = (float *)(b + S.fh);
     a.cap = S.cap;
+    a.Xk = (unsigned short *)(b + S.Xk);
+    a.XvT = (unsigned short *)(b + S.XvT);
+    a.nxp = S.nxp;
+    a.tc = S.nxp > 0;
 }
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
@@ -333,6 +337,19 @@ int o1_state_write(void *state, const o1_geom *geom, const o1_state_host *src, v
     cp(src->far_mass, L.Z, nh * m * 4);
     cp(src->far_val, L.T, nh * m * g.dv * 4);
     if (e != cudaSuccess) return O1_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return O1_ERR_CUDA;
+    return O1_OK;
+}
+
+int o1_state_flags(void *state, const o1_geom *geom, uint32_t *flags, int32_t clear, void *stream) {
+    if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
+    if (!state || !flags || !aligned(state, 256)) return O1_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int hs = check_header(state, *geom, st);
+    if (hs != O1_OK) return hs;
+    char *b = (char *)state + o1_layout(*geom).hdr + offsetof(O1Header, flags);
+    if (cudaMemcpyAsync(flags, b, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) return O1_ERR_CUDA;
+    if (clear && cudaMemsetAsync(b, 0, sizeof(uint32_t), st) != cudaSuccess) return O1_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return O1_ERR_CUDA;
     return O1_OK;
 }

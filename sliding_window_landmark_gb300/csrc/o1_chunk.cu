@@ -17,11 +17,12 @@
 //  4. k_far_dT       per block: sum_j E_bj v_ev(j)  (o1b_far_commit's sum)
 //  5. k_far_tscan    T entering each block, rescaled to its max
 //                    (o1b_far_commit's recurrence T <- R T + dT, as a scan)
-//  6. k_far_readout  per row: landmark scores, u = e^{f-F} mu, gains, the far
-//                    mass D and numerator (o1b_attend's far part)
-//  7. k_near         sinks + window, online softmax, merged with the far part
-//                    under one exponent, gate (o1b_attend's near part and
-//                    normalisation; dory_gate1)
+//  6. k_side_readout per row: the sinks and the far field (landmark scores,
+//                    u = e^{f-F} mu, gains, far mass and numerator) under one
+//                    exponent (o1b_attend's sink and far parts)
+//  7. k_near         the sliding window, online softmax, merged with the side
+//                    part under one exponent, gate (o1b_attend's window part
+//                    and normalisation; dory_gate1)
 //  8. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
 //
 // Keys are indexed in X = [ring, oldest first] ++ [this pass's rows]: row r
@@ -211,16 +212,21 @@ __global__ void k_far_tscan(O1Args a) {
     a.T[idx] = T;
 }
 
-// The far part of every row of block c for head gh (o1b_attend's far half,
-// referenced to the block's max as the pages do):
+// The side part of every row of block c for head gh: the sinks and the far
+// field, referenced to one exponent c_s = max(sink scores, c_f) (o1b_attend's
+// c_all restricted to these keys; the far half as the pages reference it to
+// the block's max):
 //   f_a = scale q'.kt_a, F = max f, u_b = sum_a e^{f_a - F} mu[a][b] (rect),
 //   c_f = max_b (F + M_c[b]), gain_b = u_b e^{F + M_c[b] - c_f},
-//   D = sum_b gain_b P_b(row); the far part is dropped if D < 0;
-//   numerator = sum_b gain_b (R_c T_{c-1})_b + sum_{evicting j <= row} cf_j v_ev(j),
-//   cf_j = sum_b gain_b E_bj.
-// The numerator goes to `out` (the near kernel finishes the row there), and
-// (c_f, D, have) to the far header; c_f = -inf marks a row with no far field.
-__global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
+//   D = sum_b gain_b P_b(row); the far part is dropped if D < 0 (c_f still
+//   enters c_s, as c_all keeps the far max);
+//   far numerator = sum_b gain_b (R_c T_{c-1})_b + sum_{evicting j <= row} cf_j v_ev(j),
+//   cf_j = sum_b gain_b E_bj;
+//   sinks: p_x = e^{scale q'.sink_x - c_s}.
+// The side numerator goes to `out` (the window kernel finishes the row
+// there) and (c_s, side mass) to the side header; c_s = -inf marks a row
+// with no sinks and no far field.
+__global__ __launch_bounds__(256) void k_side_readout(O1Args a) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -228,9 +234,9 @@ __global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
     const O1Meta mt = o1_meta(a, g);
     const int j0 = mt.wg - mt.len0;
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
-    const int m = a.m, d = a.d, dv = a.dv, nh = a.nh;
-    const int farl_last = mt.farl0 + max(0, r0 + nr - j0);
-    if (farl_last == 0) {
+    const int m = a.m, d = a.d, dv = a.dv, nh = a.nh, ns = a.ns;
+    const bool far_any = mt.farl0 + max(0, r0 + nr - j0) > 0;
+    if (!far_any && ns == 0) {
         for (int idx = tid; idx < nr * dv; idx += 256) {
             const int i = idx / dv, t = idx % dv;
             a.out[((size_t)(r0 + i) * nh + gh) * dv + t] = 0.f;
@@ -241,64 +247,74 @@ __global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
     }
     float *sA = sm;                // 64 x 33  query chunk
     float *sB = sA + 64 * 33;      // 64 x 33  landmark-key chunk
-    float *sF = sB + 64 * 33;      // 64 x 65  f, then e^{f - F}
-    float *sU = sF + 64 * 65;      // 64 x 65  u, then gains
+    float *sB2 = sB + 64 * 33;     // 64 x 33  sink-key chunk
+    float *sF = sB2 + 64 * 33;     // 64 x 65  f, then e^{f - F}, then sink weights
+    float *sU = sF + 64 * 65;      // 64 x 65  u, then gains (scaled to c_s)
     float *sX = sU + 64 * 65;      // 64 x 65  mu, then E, then T chunk
-    float *sC = sX + 64 * 65;      // 64 x 65  cf
-    float *sV = sC + 64 * 65;      // 64 x 65  value chunk
-    float *sRow = sV + 64 * 65;    // 64       F per row
+    float *sC = sX + 64 * 65;      // 64 x 65  sink scores, then cf
+    float *sV = sC + 64 * 65;      // 64 x 65  evicted-value chunk
+    float *sW = sV + 64 * 65;      // 64 x 65  sink-value chunk
+    float *sRow = sW + 64 * 65;    // 64       F per row
     float *sMc = sRow + 64;        // 64       block max per landmark
-    float acc[4][4];
+    float acc[4][4], acc2[4][4];
 
-    // 1. landmark scores
+    // 1. landmark scores and sink scores, one pass over d
     blk_zero(acc);
+    blk_zero(acc2);
     for (int kc = 0; kc < d; kc += 32) {
         for (int idx = tid; idx < 64 * 32; idx += 256) {
             const int i = idx >> 5, kk = idx & 31;
             const bool in = kc + kk < d;
             sA[i * 33 + kk] = (i < nr && in) ? a.qr[((size_t)(r0 + i) * nh + gh) * d + kc + kk] : 0.f;
-            sB[i * 33 + kk] = (i < m && in) ? a.kt[((size_t)g * m + i) * d + kc + kk] : 0.f;
+            sB[i * 33 + kk] = (far_any && i < m && in) ? a.kt[((size_t)g * m + i) * d + kc + kk] : 0.f;
+            sB2[i * 33 + kk] = (i < ns && in) ? a.sink_k[((size_t)g * ns + i) * d + kc + kk] : 0.f;
         }
         __syncthreads();
-        blk_nt(acc, sA, 33, sB, 33, 32);
+        if (far_any) blk_nt(acc, sA, 33, sB, 33, 32);
+        if (ns > 0) blk_nt(acc2, sA, 33, sB2, 33, 32);
         __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sF[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc[i][j];
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int aa = idx >> 6, b = idx & 63;
-        sX[aa * 65 + b] = (aa < m && b < m) ? a.mu[((size_t)gh * m + aa) * m + b] : 0.f;
-    }
-    for (int b = tid; b < 64; b += 256) sMc[b] = b < m ? a.Mc[((size_t)gh * m + b) * a.nsub + c] : 0.f;
-    __syncthreads();
-
-    // 2. F per row and e^{f - F}
-    for (int i = warp; i < 64; i += 8) {
-        const float v0 = lane < m ? sF[i * 65 + lane] : -INFINITY;
-        const float v1 = lane + 32 < m ? sF[i * 65 + lane + 32] : -INFINITY;
-        const float F = warp_max(fmaxf(v0, v1));
-        if (lane == 0) sRow[i] = F;
-        sF[i * 65 + lane] = lane < m ? expf(v0 - F) : 0.f;
-        sF[i * 65 + lane + 32] = lane + 32 < m ? expf(v1 - F) : 0.f;
-    }
-    __syncthreads();
-
-    // 3. u = e mu
-    blk_zero(acc);
-    blk_nn(acc, sF, 65, sX, 65, m);
+        for (int j = 0; j < 4; ++j) {
+            sF[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc[i][j];
+            sC[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc2[i][j];
+        }
+    if (far_any) {
+        for (int idx = tid; idx < 64 * 64; idx += 256) {
+            const int aa = idx >> 6, b = idx & 63;
+            sX[aa * 65 + b] = (aa < m && b < m) ? a.mu[((size_t)gh * m + aa) * m + b] : 0.f;
+        }
+        for (int b = tid; b < 64; b += 256) sMc[b] = b < m ? a.Mc[((size_t)gh * m + b) * a.nsub + c] : 0.f;
+        __syncthreads();
+        // 2. F per row and e^{f - F}
+        for (int i = warp; i < 64; i += 8) {
+            const float v0 = lane < m ? sF[i * 65 + lane] : -INFINITY;
+            const float v1 = lane + 32 < m ? sF[i * 65 + lane + 32] : -INFINITY;
+            const float F = warp_max(fmaxf(v0, v1));
+            if (lane == 0) sRow[i] = F;
+            sF[i * 65 + lane] = lane < m ? expf(v0 - F) : 0.f;
+            sF[i * 65 + lane + 32] = lane + 32 < m ? expf(v1 - F) : 0.f;
+        }
+        __syncthreads();
+        // 3. u = e mu
+        blk_zero(acc);
+        blk_nn(acc, sF, 65, sX, 65, m);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sU[(ty + 16 * i) * 65 + tx + 16 * j] = acc[i][j];
+            for (int j = 0; j < 4; ++j) sU[(ty + 16 * i) * 65 + tx + 16 * j] = acc[i][j];
+    }
     __syncthreads();
 
-    // 4. gains, far mass, sign decision (one warp per row)
+    // 4. per row (one warp each): far gains, mass and sign decision, the side
+    //    exponent c_s, sink weights, the side mass
     for (int i = warp; i < 64; i += 8) {
         const int r = r0 + i;
         const int farl = mt.farl0 + max(0, r - j0 + 1);
-        float g0 = 0.f, g1 = 0.f;
+        float g0 = 0.f, g1 = 0.f, cf = -INFINITY, D = 0.f;
+        bool have = false;
         if (i < nr && farl > 0) {
             float u0 = lane < m ? sU[i * 65 + lane] : 0.f;
             float u1 = lane + 32 < m ? sU[i * 65 + lane + 32] : 0.f;
@@ -309,37 +325,42 @@ __global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
             const float F = sRow[i];
             const float cb0 = lane < m ? F + sMc[lane] : -INFINITY;
             const float cb1 = lane + 32 < m ? F + sMc[lane + 32] : -INFINITY;
-            const float cf = warp_max(fmaxf(cb0, cb1));
+            cf = warp_max(fmaxf(cb0, cb1));
             g0 = lane < m ? u0 * expf(cb0 - cf) : 0.f;
             g1 = lane + 32 < m ? u1 * expf(cb1 - cf) : 0.f;
             const float p0 = lane < m ? a.P[((size_t)gh * m + lane) * a.cap + r] : 0.f;
             const float p1 = lane + 32 < m ? a.P[((size_t)gh * m + lane + 32) * a.cap + r] : 0.f;
-            const float D = warp_sum(g0 * p0 + g1 * p1);
-            const bool have = D >= 0.f;
-            if (!have) {
-                g0 = 0.f;
-                g1 = 0.f;
-            }
-            if (lane == 0)
-                *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) =
-                    make_float4(cf, have ? D : 0.f, have ? 1.f : 0.f, 0.f);
-        } else if (i < nr && lane == 0) {
-            *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            D = warp_sum(g0 * p0 + g1 * p1);
+            have = D >= 0.f;
         }
-        sU[i * 65 + lane] = g0;
-        sU[i * 65 + lane + 32] = g1;
+        // sink scores from step 1: lane x < ns holds s_x
+        const float sx0 = (i < nr && lane < ns) ? sC[i * 65 + lane] : -INFINITY;
+        const float sx1 = (i < nr && lane + 32 < ns) ? sC[i * 65 + lane + 32] : -INFINITY;
+        const float smax = warp_max(fmaxf(sx0, sx1));
+        const float cs = fmaxf(smax, cf);
+        const float w0 = sx0 > -INFINITY ? expf(sx0 - cs) : 0.f;
+        const float w1 = sx1 > -INFINITY ? expf(sx1 - cs) : 0.f;
+        const float fs = have ? expf(cf - cs) : 0.f;
+        const float side = warp_sum(w0 + w1) + fs * D;
+        sU[i * 65 + lane] = g0 * fs;
+        sU[i * 65 + lane + 32] = g1 * fs;
+        sF[i * 65 + lane] = w0;
+        sF[i * 65 + lane + 32] = w1;
+        if (i < nr && lane == 0)
+            *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) =
+                make_float4(cs, cs > -INFINITY ? side : 0.f, have ? 1.f : 0.f, 0.f);
     }
     // E of this block's evicting rows, referenced to M_c by k_far_scan
     for (int idx = tid; idx < 64 * 64; idx += 256) {
         const int b = idx >> 6, jj = idx & 63;
         const int r = r0 + jj;
-        sX[b * 65 + jj] = (b < m && jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
+        sX[b * 65 + jj] = (far_any && b < m && jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
     }
     __syncthreads();
 
     // 5. in-block far coefficients, causal: cf[i][jj] for jj <= i
     blk_zero(acc);
-    blk_nn(acc, sU, 65, sX, 65, m);
+    if (far_any) blk_nn(acc, sU, 65, sX, 65, m);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -349,20 +370,25 @@ __global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
         }
     __syncthreads();
 
-    // 6. numerator, 64 value columns at a time
+    // 6. side numerator, 64 value columns at a time
     const float *Tp = a.Tp + (size_t)(c * nh + gh) * m * dv;
+    const float *sinks_v = a.sink_v + (size_t)g * ns * dv;
     for (int tc = 0; tc < dv; tc += 64) {
         for (int idx = tid; idx < 64 * 64; idx += 256) {
             const int i = idx >> 6, t = idx & 63;
             const bool in = tc + t < dv;
-            sX[i * 65 + t] = (i < m && in) ? Tp[(size_t)i * dv + tc + t] : 0.f;
+            sX[i * 65 + t] = (far_any && i < m && in) ? Tp[(size_t)i * dv + tc + t] : 0.f;
             const int r = r0 + i;
-            sV[i * 65 + t] = (i < nr && r >= j0 && in) ? o1_val(a, g, r - j0, mt)[tc + t] : 0.f;
+            sV[i * 65 + t] = (far_any && i < nr && r >= j0 && in) ? o1_val(a, g, r - j0, mt)[tc + t] : 0.f;
+            sW[i * 65 + t] = (i < ns && in) ? sinks_v[(size_t)i * dv + tc + t] : 0.f;
         }
         __syncthreads();
         blk_zero(acc);
-        blk_nn(acc, sU, 65, sX, 65, m);
-        blk_nn(acc, sC, 65, sV, 65, 64);
+        if (far_any) {
+            blk_nn(acc, sU, 65, sX, 65, m);
+            blk_nn(acc, sC, 65, sV, 65, 64);
+        }
+        if (ns > 0) blk_nn(acc, sF, 65, sW, 65, ns);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -378,11 +404,12 @@ __global__ __launch_bounds__(256) void k_far_readout(O1Args a) {
 
 // Block = (rows, group): 32 query slots = floor(32 / hpg) rows x hpg heads,
 // so one staged key/value tile serves every head of the group. 8 warps, 4
-// slots each; within a key tile, lane = key. Keys: the group's sinks, then
+// slots each; within a key tile, lane = key. Keys: the window range
 // X[lo(r0) .. hi(last row)]; each slot masks to its own row's window.
-// Online softmax (running max and sum), then the far part merged under the
-// common exponent c = max(near max, c_f) as o1b_attend's c_all, the
-// denominator floored at 1e-30 in those units, and the gate.
+// Online softmax (running max and sum), then the side part (sinks + far
+// field) merged under the common exponent c = max(window max, c_s) — the
+// pages' c_all — the denominator floored at 1e-30 in those units, and the
+// gate.
 template <int NV>
 __global__ __launch_bounds__(256) void k_near(O1Args a) {
     extern __shared__ float sm[];
@@ -431,9 +458,7 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
 
     const int xlo = max(0, mt.len0 + r0 + 1 - mt.wg);
     const int xhi = mt.len0 + r0 + nr - 1;
-    const int nkeys = a.ns + (xhi - xlo + 1);
-    const float *sinks_k = a.sink_k + (size_t)g * a.ns * a.d;
-    const float *sinks_v = a.sink_v + (size_t)g * a.ns * a.dv;
+    const int nkeys = xhi - xlo + 1;
 
     for (int kb = 0; kb < nkeys; kb += 32) {
         const int cnt = min(32, nkeys - kb);
@@ -441,21 +466,13 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
         for (int idx = tid; idx < 32 * d4; idx += 256) {
             const int kk = idx / d4, c4 = idx % d4;
             float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (kk < cnt) {
-                const int key = kb + kk;
-                const float *src = key < a.ns ? sinks_k + (size_t)key * a.d : o1_key(a, g, xlo + key - a.ns, mt);
-                val = ((const float4 *)src)[c4];
-            }
+            if (kk < cnt) val = ((const float4 *)o1_key(a, g, xlo + kb + kk, mt))[c4];
             ((float4 *)(sK + kk * dq))[c4] = val;
         }
         for (int idx = tid; idx < 32 * dv4; idx += 256) {
             const int kk = idx / dv4, c4 = idx % dv4;
             float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (kk < cnt) {
-                const int key = kb + kk;
-                const float *src = key < a.ns ? sinks_v + (size_t)key * a.dv : o1_val(a, g, xlo + key - a.ns, mt);
-                val = ((const float4 *)src)[c4];
-            }
+            if (kk < cnt) val = ((const float4 *)o1_val(a, g, xlo + kb + kk, mt))[c4];
             ((float4 *)(sV + kk * dvq))[c4] = val;
         }
         __syncthreads();
@@ -474,12 +491,11 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
                 sc[i] = fmaf(qv.w, kv.w, sc[i]);
             }
         }
-        const int key = kb + lane;
-        const int x = xlo + key - a.ns;
+        const int x = xlo + kb + lane;
         float p[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const bool ok = act[i] && lane < cnt && (key < a.ns || (x >= lo[i] && x <= hi[i]));
+            const bool ok = act[i] && lane < cnt && x >= lo[i] && x <= hi[i];
             const float s = ok ? sc[i] * a.scale : -INFINITY;
             const float tm = warp_max(s);
             p[i] = 0.f;
@@ -524,10 +540,9 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
         const int s = warp * 4 + i;
         const int r = r0 + s / hpg, hh = g * hpg + s % hpg;
         const float4 hd = *(const float4 *)(a.fh + ((size_t)r * a.nh + hh) * 4);
-        const bool have = hd.z > 0.5f;
-        const float cexp = hd.x > -INFINITY ? fmaxf(mrow[i], hd.x) : mrow[i];
+        const float cexp = fmaxf(mrow[i], hd.x);
         const float al = expf(mrow[i] - cexp);
-        const float be = have ? expf(hd.x - cexp) : 0.f;
+        const float be = hd.x > -INFINITY ? expf(hd.x - cexp) : 0.f;
         const float den = fmaxf(be * hd.y + al * lrow[i], 1e-30f);
         float *o = a.out + ((size_t)r * a.nh + hh) * a.dv;
         const float *gt = a.gate ? a.gate + ((size_t)r * a.nh + hh) * a.dv : nullptr;
@@ -601,17 +616,17 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a, int rows_per_block) {
 
 // ------------------------------------------------------------- launchers
 
-extern const char *const o1_stage_names[O1_NUM_STAGES] = {"rope", "far_logits", "far_scan", "far_dT",
-                                                   "far_tscan", "far_readout", "near", "commit"};
+extern const char *const o1_stage_names[O1_NUM_STAGES] = {
+    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near", "commit"};
 
-static size_t readout_smem() { return (size_t)(2 * 64 * 33 + 5 * 64 * 65 + 128) * sizeof(float); }
+static size_t readout_smem() { return (size_t)(3 * 64 * 33 + 6 * 64 * 65 + 128) * sizeof(float); }
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
     static bool attrs_set = false;
     if (!attrs_set) {
-        cudaFuncSetAttribute(k_far_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
+        cudaFuncSetAttribute(k_side_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
         cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attrs_set = true;
@@ -635,12 +650,21 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     const size_t n = (size_t)a.nh * a.m * a.dv;
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
     mark();
-    k_far_readout<<<dim3(nblk, a.nh), 256, readout_smem(), st>>>(a);
+    k_side_readout<<<dim3(nblk, a.nh), 256, readout_smem(), st>>>(a);
     mark();
-    const int RB = 32 / a.hpg;
-    const dim3 gn((R + RB - 1) / RB, a.G);
-    if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
-    else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+    if (a.tc) {
+        cudaError_t e = o1_launch_gather_tc(a, st);
+        if (e != cudaSuccess) return e;
+        mark();
+        e = o1_launch_near_tc(a, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        mark();   // no panels to gather
+        const int RB = 32 / a.hpg;
+        const dim3 gn((R + RB - 1) / RB, a.G);
+        if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
+        else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+    }
     mark();
     const int rpb = 4;
     const int live = R < a.w ? R : a.w;

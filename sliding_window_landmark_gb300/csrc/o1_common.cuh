@@ -16,8 +16,10 @@
 #define O1_MAX_DV 256
 #define O1_MAX_M 64
 #define O1_MAX_HPG 16
-#define O1_MAX_NS 255
+#define O1_MAX_NS 64
 #define O1_MAX_W (1 << 20)
+#define O1_TC_BN 64            // keys per tile of the tensor-core window path
+#define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
 
 // First bytes of a state buffer.
 struct O1Header {
@@ -67,11 +69,26 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   Mc, Rc [nh][m][nsub]  block max and rescale factor
 //   Tp [nsub][nh][m][dv]  far value sums: increments, then the value sum
 //                         entering each block, rescaled to its max
-//   fh [cap][nh] x 4      per row-head far header (c_f, D, have, -)
+//   fh [cap][nh] x 4      per row-head side header (c_s, side mass, have, -)
+// and, when the tensor-core window path serves the geometry, the window key
+// sequence as fp16 hi / lo panels (nxp keys per group, zero past the end):
+//   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]
 struct O1Scratch {
-    size_t qr, kr, E, P, Mc, Rc, Tp, fh, total;
-    int cap, nsub;
+    size_t qr, kr, E, P, Mc, Rc, Tp, fh, Xk, XvT, total;
+    int cap, nsub, nxp;
 };
+
+// The tensor-core window path: d in 64-wide chunks (one 128-byte swizzle row
+// of fp16), at most 256 (Q_lo fills TMEM columns 384..511), dv a multiple of
+// 32 (TMEM load width) up to 256, and a window wide enough to pay for the
+// panel gather.
+static inline bool o1_tc_supported(const o1_geom &g) {
+    return g.d % 64 == 0 && g.d <= 256 && g.dv % 32 == 0 && g.dv <= 256 && g.window >= O1_TC_MIN_WINDOW;
+}
+
+// Keys per group in the fp16 panels: the ring, the pass's rows, one tile of
+// slack for the last tile's overhang, rounded to 8 (16-byte rows of XvT).
+static inline int o1_tc_nxp(const o1_geom &g, int cap) { return (g.window + cap + O1_TC_BN + 7) & ~7; }
 
 static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, d = g.d, dv = g.dv,
@@ -88,6 +105,10 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     S.Rc = off; off += o1_al256(nh * m * ns * 4);
     S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
     S.fh = off; off += o1_al256(c * nh * 4 * 4);
+    S.nxp = o1_tc_supported(g) ? o1_tc_nxp(g, cap) : 0;
+    const size_t nx = (size_t)S.nxp;
+    S.Xk = off;  off += o1_al256(2 * G * nx * d * 2);
+    S.XvT = off; off += o1_al256(2 * G * dv * nx * 2);
     S.total = off;
     return S;
 }
@@ -96,7 +117,8 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
 // = (max, sum, value sum [dv]); the far part per head = (c_f, D, have, -,
 // numerator [dv]); the row's rotated key per group. KC keys per slice, NC
 // slices per group, sized for the longest near set (sinks + window) so that
-// about two blocks per SM share the key reads.
+// about two blocks per SM share the key reads, and capped so that a slice
+// fits in shared memory.
 struct O1TokScratch {
     size_t part, farp, kcur, total;
     int KC, NC;
@@ -107,6 +129,10 @@ static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     const long long nmax = (long long)g.sinks + g.window;
     long long kc = (G * nmax + 303) / 304;
     kc = kc < 8 ? 8 : (kc + 7) / 8 * 8;
+    // a slice's keys, values and scores stay within 227 KB of shared memory
+    const long long kmax = ((227 * 1024 / 4) - (long long)(g.heads_per_group + 1) * g.d - 2 * g.heads_per_group) /
+                           ((long long)g.d + g.dv + g.heads_per_group) / 8 * 8;
+    if (kc > kmax) kc = kmax;
     O1TokScratch S;
     S.KC = (int)kc;
     S.NC = (int)((nmax + kc - 1) / kc);
@@ -143,6 +169,9 @@ struct O1Args {
     // scratch
     float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh;
     int cap;
+    // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
+    unsigned short *Xk, *XvT;
+    int nxp, tc;
     // one-row path scratch
     float *part, *farp, *kcur;
     int KC, NC;
@@ -256,5 +285,9 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 // `ev` may be null; otherwise O1_NUM_STAGES + 1 events recorded around the stages.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);
+// Tensor-core window path (o1_near_tc.cu): panel gather, then the window
+// attention with the side merge and the gate.
+cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st);
+cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st);
 // One row (o1_token.cu): main kernel + merge kernel.
 cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st);

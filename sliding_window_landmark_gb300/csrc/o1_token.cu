@@ -262,16 +262,28 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
     const float cf = sRed[1], D = sRed[2];
     const bool have = D >= 0.f;
     // value sums: insert the evicted value and read the far numerator
+    // (16 loads issued before the first store: the stores may alias later
+    // loads as far as the compiler knows, which would serialise them)
     for (int t = tid; t < dv; t += blockDim.x) {
         float *T = a.T + (size_t)h * m * dv + t;
+        const float vt = evict ? sve[t] : 0.f;
         float acc = 0.f;
-        for (int b = 0; b < m; ++b) {
-            float Tv = T[(size_t)b * dv];
-            if (evict) {
-                Tv = sRho[b] * Tv + sE[b] * sve[t];
-                T[(size_t)b * dv] = Tv;
+        for (int b0 = 0; b0 < m; b0 += 16) {
+            float Tv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tv[i] = b0 + i < m ? T[(size_t)(b0 + i) * dv] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int b = b0 + i;
+                if (b < m) {
+                    float x = Tv[i];
+                    if (evict) {
+                        x = sRho[b] * x + sE[b] * vt;
+                        T[(size_t)b * dv] = x;
+                    }
+                    acc = fmaf(sG[b], x, acc);
+                }
             }
-            acc = fmaf(sG[b], Tv, acc);
         }
         fp[4 + t] = have ? acc : 0.f;
     }
@@ -293,27 +305,62 @@ __global__ __launch_bounds__(256) void k_tok_main(O1Args a) {
     else tok_far(a, g, r - a.NC, mt, sm);
 }
 
-// Merge per (head, 64 value columns); block (0, 0) also commits the row.
-__global__ __launch_bounds__(64) void k_tok_merge(O1Args a) {
+// Merge per (head, 64 value columns), 256 threads: the slices' common max
+// and mass by block reductions, then four slice groups of 64 columns each
+// accumulate with independent loads; block (0, 0) also commits the row.
+__global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
+    __shared__ float sred[8];
+    __shared__ float sacc[4][64];
     o1_wait_primary();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, g = h / a.hpg, hl = h % a.hpg;
-    const int t = blockIdx.y * 64 + threadIdx.x;
     const size_t cs = (size_t)a.hpg * (2 + a.dv);
     const float *part = a.part + (size_t)g * a.NC * cs + (size_t)hl * (2 + a.dv);
     float mx = -INFINITY;
-    for (int c = 0; c < a.NC; ++c) mx = fmaxf(mx, __ldcg(part + c * cs));
-    float l = 0.f, acc = 0.f;
-    for (int c = 0; c < a.NC; ++c) {
+    for (int c = tid; c < a.NC; c += 256) mx = fmaxf(mx, __ldcg(part + c * cs));
+    mx = warp_max(mx);
+    if (lane == 0) sred[warp] = mx;
+    __syncthreads();
+    mx = sred[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sred[i]);
+    __syncthreads();
+    float l = 0.f;
+    for (int c = tid; c < a.NC; c += 256) {
         const float mc = __ldcg(part + c * cs);
-        if (mc == -INFINITY) continue;
-        const float w = expf(mc - mx);
-        l = fmaf(w, __ldcg(part + c * cs + 1), l);
-        if (t < a.dv) acc = fmaf(w, __ldcg(part + c * cs + 2 + t), acc);
+        if (mc > -INFINITY) l = fmaf(expf(mc - mx), __ldcg(part + c * cs + 1), l);
     }
-    const float *fp = a.farp + (size_t)h * (4 + a.dv);
-    const float cf = __ldcg(fp), Df = __ldcg(fp + 1);
-    const bool have = __ldcg(fp + 2) > 0.5f;
+    l = warp_sum(l);
+    if (lane == 0) sred[warp] = l;
+    __syncthreads();
+    l = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l += sred[i];
+    const int cg = tid >> 6, col = tid & 63, t = blockIdx.y * 64 + col;
+    float acc = 0.f;
     if (t < a.dv) {
+        float ac[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c0 = cg; c0 < a.NC; c0 += 16) {
+            float mc[4], vc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + 4 * u;
+                mc[u] = c < a.NC ? __ldcg(part + c * cs) : -INFINITY;
+                vc[u] = c < a.NC ? __ldcg(part + c * cs + 2 + t) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (mc[u] > -INFINITY) ac[u] = fmaf(expf(mc[u] - mx), vc[u], ac[u]);
+        }
+        acc = (ac[0] + ac[1]) + (ac[2] + ac[3]);
+    }
+    sacc[cg][col] = acc;
+    __syncthreads();
+    if (cg == 0 && t < a.dv) {
+        acc = (sacc[0][col] + sacc[1][col]) + (sacc[2][col] + sacc[3][col]);
+        const float *fp = a.farp + (size_t)h * (4 + a.dv);
+        const float cf = __ldcg(fp), Df = __ldcg(fp + 1);
+        const bool have = __ldcg(fp + 2) > 0.5f;
         const float c = cf > -INFINITY ? fmaxf(mx, cf) : mx;
         const float al = expf(mx - c);
         const float be = have ? expf(cf - c) : 0.f;
@@ -357,7 +404,7 @@ cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
     k_tok_main<<<a.G * (a.NC + a.hpg), 256, tok_main_smem(a), st>>>(a);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.nh, (a.dv + 63) / 64, 1);
-    cfg.blockDim = dim3(64, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -78,6 +78,8 @@ def _load(path: str | None = None):
     lib.o1_state_read.restype = ctypes.c_int
     lib.o1_state_write.argtypes = [_VP, _G, ctypes.POINTER(o1_state_host), _VP]
     lib.o1_state_write.restype = ctypes.c_int
+    lib.o1_state_flags.argtypes = [_VP, _G, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, _VP]
+    lib.o1_state_flags.restype = ctypes.c_int
     lib.o1_status_string.argtypes = [ctypes.c_int]
     lib.o1_status_string.restype = ctypes.c_char_p
     return lib
@@ -159,7 +161,7 @@ def o1_chunk_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, s
         _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
 
 
-O1_NUM_STAGES = 8
+O1_NUM_STAGES = 9
 
 
 def o1_stage_name(stage: int):
@@ -232,6 +234,18 @@ def o1_state_write(state, g: o1_geom, src: dict, stream=None) -> int:
     hv = _host_view(g, src)
     return LIB.o1_state_write(_dev(state, o1_state_bytes(g), "state", dtype=None), ctypes.byref(g),
                               ctypes.byref(hv), _stream(stream))
+
+
+O1_FLAG_WAIT_EXPIRED = 1
+O1_FLAG_FP16_RANGE = 2
+
+
+def o1_state_flags(state, g: o1_geom, clear: bool = False, stream=None) -> int:
+    """The state's sticky flags (O1_FLAG_*); raises O1Error on a bad status."""
+    f = ctypes.c_uint32(0)
+    check(LIB.o1_state_flags(_dev(state, o1_state_bytes(g), "state", dtype=None), ctypes.byref(g),
+                             ctypes.byref(f), int(bool(clear)), _stream(stream)), "flags")
+    return int(f.value)
 
 
 def empty_state_arrays(g: o1_geom) -> dict:

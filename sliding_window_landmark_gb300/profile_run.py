@@ -1,0 +1,63 @@
+"""A fixed launch sequence for profilers: one sealed layer, `--calls` chunk
+calls of `--rows` rows each from a fresh state (the state restored between
+calls), or `--tokens` one-row calls after a prompt of `--rows` rows.
+
+  python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 4096 --calls 3
+  python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 8192 --tokens 16
+
+Launches per chunk call, in order: rope, far_logits, far_scan, far_dT,
+far_tscan, side_readout, [gather_tc], near, commit; per one-row call:
+k_tok_main, k_tok_merge. The library must already be built.
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+import torch
+
+from . import o1, synth
+
+SHAPES = {"tiny": synth.TINY, "qwen": synth.QWEN_LAYER, "qwen_long": synth.QWEN_LONG,
+          "stack": synth.STACK_LAYER}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--shape", choices=sorted(SHAPES), default="qwen")
+    ap.add_argument("--rows", type=int, default=4096)
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=1)
+    args = ap.parse_args()
+    sh = SHAPES[args.shape]
+    dev = torch.device("cuda")
+    g = o1.geom(sh.groups, sh.heads_per_group, sh.d, sh.dv, sh.sinks, sh.window, sh.landmarks,
+                rope_base=sh.rope_base)
+    c = synth.layer_constants(sh, args.seed)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    consts = [up(c.sink_k), up(c.sink_v), up(c.k_tilde), up(c.q_tilde), up(c.mu)]
+    state = torch.empty(o1.o1_state_bytes(g), dtype=torch.uint8, device=dev)
+    o1.check(o1.o1_state_init(state, g, sh.group_windows, *consts, 0), "init")
+    fresh = state.clone()
+    scratch = torch.empty(o1.o1_scratch_bytes(g, args.rows), dtype=torch.uint8, device=dev)
+    q, k, v, gt = (up(x) for x in synth.layer_rows(sh, args.seed, 0, args.rows))
+    out = torch.empty((args.rows, sh.nh, sh.dv), dtype=torch.float32, device=dev)
+    if args.tokens:
+        o1.check(o1.o1_chunk_attend(state, g, scratch, q, k, v, gt, args.rows, out), "prompt")
+        tq, tk, tv, tg = (up(x) for x in synth.layer_rows(sh, args.seed, args.rows, args.tokens))
+        tout = torch.empty((args.tokens, sh.nh, sh.dv), dtype=torch.float32, device=dev)
+        for i in range(args.tokens):
+            o1.check(o1.o1_token_attend(state, g, scratch, tq[i], tk[i], tv[i], tg[i], tout[i]), "token")
+    else:
+        for _ in range(args.calls):
+            state.copy_(fresh)
+            o1.check(o1.o1_chunk_attend(state, g, scratch, q, k, v, gt, args.rows, out), "chunk")
+    torch.cuda.synchronize()
+    assert o1.o1_state_flags(state, g) == 0, "state flags raised"
+    assert torch.isfinite(out).all().item()
+    print("done", args.shape, args.rows, args.calls, args.tokens)
+
+
+if __name__ == "__main__":
+    main()

@@ -45,7 +45,7 @@ def test_sizes(o1):
     assert o1.o1_scratch_bytes(g, 0) == 0
     for bad in (o1.geom(0, 4, 256, 256, 4, 2048, 32), o1.geom(2, 4, 260, 256, 4, 2048, 32),
                 o1.geom(2, 4, 256, 256, 4, 2048, 65), o1.geom(2, 17, 256, 256, 4, 2048, 32),
-                o1.geom(2, 4, 12, 12, 4, 2048, 32), o1.geom(2, 4, 256, 256, 256, 2048, 32)):
+                o1.geom(2, 4, 12, 12, 4, 2048, 32), o1.geom(2, 4, 256, 256, 65, 2048, 32)):
         assert o1.o1_state_bytes(bad) == 0
 
 

@@ -104,6 +104,46 @@ def test_small_shapes(case):
     _run(sh, 100 + d, list(calls), rect=rect, mu_abs=mu_abs, scratch_rows=srows)
 
 
+# The tensor-core window path (d % 64 == 0, dv % 32 == 0, window >= 512):
+# every d chunk count (1, 2, 4), dv from 32 to 256, ragged 128-row tiles,
+# tile starts not on a 64-key boundary, one-row passes between chunks, a
+# group window shorter than the ring stride, rectified mass, no sinks.
+TC = [
+    # (G, hpg, d, dv, ns, w, group windows, m, calls, rect, mu_abs, rope)
+    (2, 2, 128, 128, 4, 512, (512, 130), 16, (1500, 77), False, False, 1e6),
+    (1, 4, 64, 64, 0, 600, None, 8, (130, 900, 1), False, True, 1e6),
+    (2, 3, 256, 256, 2, 520, (520, 515), 32, (700,), True, False, 1e4),
+    (1, 1, 64, 32, 1, 512, None, 4, (1, 63, 600), False, False, 0.0),
+    (1, 2, 192, 96, 3, 700, None, 8, (333, 1000), False, False, 1e6),
+]
+
+
+@pytest.mark.parametrize("case", TC, ids=[f"tc{i}" for i in range(len(TC))])
+def test_tensor_core_window_shapes(case):
+    G, hpg, d, dv, ns, w, gw, m, calls, rect, mu_abs, rope = case
+    sh = synth.Shape(groups=G, heads_per_group=hpg, d=d, dv=dv, sinks=ns, window=w, landmarks=m,
+                     rope_base=rope, group_windows=gw)
+    st = _run(sh, 300 + d, list(calls), rect=rect, mu_abs=mu_abs)
+    print("tensor-core window:", st)
+
+
+def test_tensor_core_flags():
+    """The tensor-core path leaves the state's flags clear on ordinary inputs
+    and raises O1_FLAG_FP16_RANGE for a value outside the fp16 range."""
+    from sliding_window_landmark_gb300 import o1
+    sh = synth.Shape(groups=1, heads_per_group=2, d=64, dv=64, sinks=1, window=512, landmarks=4)
+    c = synth.layer_constants(sh, 5)
+    gpu = harness.GpuLayer(sh, c, max_rows=256)
+    q, k, v, g = synth.layer_rows(sh, 5, 0, 256)
+    gpu.rows(q, k, v, g)
+    assert o1.o1_state_flags(gpu.state, gpu.g) == 0
+    v = v.copy()
+    v[100, 0, 3] = 1e5
+    gpu.rows(q, k, v, g)
+    assert o1.o1_state_flags(gpu.state, gpu.g, clear=True) == o1.O1_FLAG_FP16_RANGE
+    assert o1.o1_state_flags(gpu.state, gpu.g) == 0
+
+
 def test_no_gate_and_empty_call():
     sh = synth.Shape(groups=2, heads_per_group=2, d=16, dv=8, sinks=1, window=10, landmarks=3)
     c = synth.layer_constants(sh, 7)

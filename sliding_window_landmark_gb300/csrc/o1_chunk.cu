@@ -226,8 +226,46 @@ __global__ void k_far_tscan(O1Args a) {
 // The side numerator goes to `out` (the window kernel finishes the row
 // there) and (c_s, side mass) to the side header; c_s = -inf marks a row
 // with no sinks and no far field.
-__global__ __launch_bounds__(256) void k_side_readout(O1Args a) {
-    extern __shared__ float sm[];
+//
+// Layout (256 threads, 8 warps). The products are register-tiled with
+// float4 shared-memory reads:
+//   scores  [64 rows] x [landmarks | sinks] over d, 4 x 4 per thread,
+//           k in float4 steps (both operands k-contiguous);
+//   side numerator = A6 . B6 in one product of depth K6 = m + 64 + ns:
+//           A6 = [gains | in-block coefficients | sink weights] (stored
+//           k-major, so a warp's 8 rows are one broadcast float4 pair),
+//           B6 = [T entering the block | evicted values | sink values],
+//           8 rows x 4 NV columns per thread (warp = 8 rows).
+constexpr int SR_LDQ = 36;   // 32-wide k chunk + 4
+constexpr int SR_LDA = 68;   // A6 row stride (64 rows + 4)
+
+__host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
+    const int nbt = (a.m + a.ns + 63) / 64;
+    const int K6 = a.m + 64 + a.ns;
+    const size_t r1a = (size_t)64 * SR_LDQ * (1 + nbt), r1b = (size_t)32 * (a.dv + 4);
+    off[0] = 0;                                              // A6 [K6][SR_LDA]
+    off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks
+    off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
+    off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
+    off[4] = off[3] + 64 * 65;                               // F per row [64], M_c [64]
+    off[5] = off[4] + 128;                                   // total (floats)
+}
+
+__device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
+            c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
+            c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
+            c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
+        }
+}
+
+template <int NV>
+__global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
+    extern __shared__ __align__(16) float sm[];
     const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ty = tid >> 4, tx = tid & 15;
@@ -245,79 +283,119 @@ __global__ __launch_bounds__(256) void k_side_readout(O1Args a) {
             *(float4 *)(a.fh + ((size_t)(r0 + i) * nh + gh) * 4) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
         return;
     }
-    float *sA = sm;                // 64 x 33  query chunk
-    float *sB = sA + 64 * 33;      // 64 x 33  landmark-key chunk
-    float *sB2 = sB + 64 * 33;     // 64 x 33  sink-key chunk
-    float *sF = sB2 + 64 * 33;     // 64 x 65  f, then e^{f - F}, then sink weights
-    float *sU = sF + 64 * 65;      // 64 x 65  u, then gains (scaled to c_s)
-    float *sX = sU + 64 * 65;      // 64 x 65  mu, then E, then T chunk
-    float *sC = sX + 64 * 65;      // 64 x 65  sink scores, then cf
-    float *sV = sC + 64 * 65;      // 64 x 65  evicted-value chunk
-    float *sW = sV + 64 * 65;      // 64 x 65  sink-value chunk
-    float *sRow = sW + 64 * 65;    // 64       F per row
-    float *sMc = sRow + 64;        // 64       block max per landmark
-    float acc[4][4], acc2[4][4];
+    size_t off[6];
+    side_layout(a, off);
+    const int nbt = (m + ns + 63) / 64;
+    const int ldS = 64 * nbt + 1;
+    const int K6 = m + 64 + ns;
+    float *sA6 = sm + off[0];
+    float *sR1 = sm + off[1];
+    float *sS = sm + off[2];
+    float *sR3 = sm + off[3];
+    float *sRow = sm + off[4];
+    float *sMc = sRow + 64;
 
-    // 1. landmark scores and sink scores, one pass over d
-    blk_zero(acc);
-    blk_zero(acc2);
-    for (int kc = 0; kc < d; kc += 32) {
-        for (int idx = tid; idx < 64 * 32; idx += 256) {
-            const int i = idx >> 5, kk = idx & 31;
-            const bool in = kc + kk < d;
-            sA[i * 33 + kk] = (i < nr && in) ? a.qr[((size_t)(r0 + i) * nh + gh) * d + kc + kk] : 0.f;
-            sB[i * 33 + kk] = (far_any && i < m && in) ? a.kt[((size_t)g * m + i) * d + kc + kk] : 0.f;
-            sB2[i * 33 + kk] = (i < ns && in) ? a.sink_k[((size_t)g * ns + i) * d + kc + kk] : 0.f;
+    // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks
+    {
+        float *sQc = sR1;                    // [64][SR_LDQ]
+        float *sBc = sR1 + 64 * SR_LDQ;      // [64 nbt][SR_LDQ]
+        float acc[2][4][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) blk_zero(acc[t]);
+        const int nrow = 64 * (1 + nbt);
+        for (int kc = 0; kc < d; kc += 32) {
+            for (int idx = tid; idx < nrow * 8; idx += 256) {
+                const int row = idx >> 3, k = kc + 4 * (idx & 7);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (k < d) {
+                    if (row < 64) {
+                        if (row < nr) v = *(const float4 *)(a.qr + ((size_t)(r0 + row) * nh + gh) * d + k);
+                    } else {
+                        const int col = row - 64;
+                        if (col < m) {
+                            if (far_any) v = *(const float4 *)(a.kt + ((size_t)g * m + col) * d + k);
+                        } else if (col < m + ns) {
+                            v = *(const float4 *)(a.sink_k + ((size_t)g * ns + col - m) * d + k);
+                        }
+                    }
+                }
+                *(float4 *)(sR1 + row * SR_LDQ + 4 * (idx & 7)) = v;
+            }
+            __syncthreads();
+#pragma unroll 2
+            for (int k4 = 0; k4 < 8; ++k4) {
+                float4 av[4], bv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) av[i] = *(const float4 *)(sQc + (ty + 16 * i) * SR_LDQ + 4 * k4);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (t < nbt) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
+                        fma4x4_k4(acc[t], av, bv);
+                    }
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        if (far_any) blk_nt(acc, sA, 33, sB, 33, 32);
-        if (ns > 0) blk_nt(acc2, sA, 33, sB2, 33, 32);
-        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (t < nbt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sS[(ty + 16 * i) * ldS + 64 * t + tx + 16 * j] = a.scale * acc[t][i][j];
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            sF[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc[i][j];
-            sC[(ty + 16 * i) * 65 + tx + 16 * j] = a.scale * acc2[i][j];
-        }
     if (far_any) {
-        for (int idx = tid; idx < 64 * 64; idx += 256) {
-            const int aa = idx >> 6, b = idx & 63;
-            sX[aa * 65 + b] = (aa < m && b < m) ? a.mu[((size_t)gh * m + aa) * m + b] : 0.f;
+        float *sMu = sR3;   // [m][65]
+        for (int idx = tid; idx < m * m; idx += 256) {
+            const int aa = idx / m, b = idx % m;
+            sMu[aa * 65 + b] = a.mu[((size_t)gh * m + aa) * m + b];
         }
         for (int b = tid; b < 64; b += 256) sMc[b] = b < m ? a.Mc[((size_t)gh * m + b) * a.nsub + c] : 0.f;
         __syncthreads();
-        // 2. F per row and e^{f - F}
+        // 2. F per row and e^{f - F} (columns [0, m))
         for (int i = warp; i < 64; i += 8) {
-            const float v0 = lane < m ? sF[i * 65 + lane] : -INFINITY;
-            const float v1 = lane + 32 < m ? sF[i * 65 + lane + 32] : -INFINITY;
+            const float v0 = lane < m ? sS[i * ldS + lane] : -INFINITY;
+            const float v1 = lane + 32 < m ? sS[i * ldS + lane + 32] : -INFINITY;
             const float F = warp_max(fmaxf(v0, v1));
             if (lane == 0) sRow[i] = F;
-            sF[i * 65 + lane] = lane < m ? expf(v0 - F) : 0.f;
-            sF[i * 65 + lane + 32] = lane + 32 < m ? expf(v1 - F) : 0.f;
+            if (lane < m) sS[i * ldS + lane] = expf(v0 - F);
+            if (lane + 32 < m) sS[i * ldS + lane + 32] = expf(v1 - F);
         }
         __syncthreads();
-        // 3. u = e mu
+        // 3. u = e mu, written back over columns [0, m)
+        float acc[4][4];
         blk_zero(acc);
-        blk_nn(acc, sF, 65, sX, 65, m);
+        blk_nn(acc, sS, ldS, sMu, 65, m);
+        __syncthreads();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sU[(ty + 16 * i) * 65 + tx + 16 * j] = acc[i][j];
+            for (int j = 0; j < 4; ++j)
+                if (tx + 16 * j < m) sS[(ty + 16 * i) * ldS + tx + 16 * j] = acc[i][j];
+        __syncthreads();
+        // E of this block's evicting rows, referenced to M_c by k_far_scan
+        float *sE = sR3;   // [m][65]
+        for (int idx = tid; idx < m * 64; idx += 256) {
+            const int b = idx >> 6, jj = idx & 63;
+            const int r = r0 + jj;
+            sE[b * 65 + jj] = (jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
+        }
     }
-    __syncthreads();
 
     // 4. per row (one warp each): far gains, mass and sign decision, the side
-    //    exponent c_s, sink weights, the side mass
+    //    exponent c_s, sink weights, the side mass; gains and sink weights
+    //    into A6 (k-major)
     for (int i = warp; i < 64; i += 8) {
         const int r = r0 + i;
         const int farl = mt.farl0 + max(0, r - j0 + 1);
         float g0 = 0.f, g1 = 0.f, cf = -INFINITY, D = 0.f;
         bool have = false;
-        if (i < nr && farl > 0) {
-            float u0 = lane < m ? sU[i * 65 + lane] : 0.f;
-            float u1 = lane + 32 < m ? sU[i * 65 + lane + 32] : 0.f;
+        if (far_any && i < nr && farl > 0) {
+            float u0 = lane < m ? sS[i * ldS + lane] : 0.f;
+            float u1 = lane + 32 < m ? sS[i * ldS + lane + 32] : 0.f;
             if (a.rect) {
                 u0 = fmaxf(u0, 0.f);
                 u1 = fmaxf(u1, 0.f);
@@ -333,70 +411,110 @@ __global__ __launch_bounds__(256) void k_side_readout(O1Args a) {
             D = warp_sum(g0 * p0 + g1 * p1);
             have = D >= 0.f;
         }
-        // sink scores from step 1: lane x < ns holds s_x
-        const float sx0 = (i < nr && lane < ns) ? sC[i * 65 + lane] : -INFINITY;
-        const float sx1 = (i < nr && lane + 32 < ns) ? sC[i * 65 + lane + 32] : -INFINITY;
+        const float sx0 = (i < nr && lane < ns) ? sS[i * ldS + m + lane] : -INFINITY;
+        const float sx1 = (i < nr && lane + 32 < ns) ? sS[i * ldS + m + lane + 32] : -INFINITY;
         const float smax = warp_max(fmaxf(sx0, sx1));
         const float cs = fmaxf(smax, cf);
         const float w0 = sx0 > -INFINITY ? expf(sx0 - cs) : 0.f;
         const float w1 = sx1 > -INFINITY ? expf(sx1 - cs) : 0.f;
         const float fs = have ? expf(cf - cs) : 0.f;
         const float side = warp_sum(w0 + w1) + fs * D;
-        sU[i * 65 + lane] = g0 * fs;
-        sU[i * 65 + lane + 32] = g1 * fs;
-        sF[i * 65 + lane] = w0;
-        sF[i * 65 + lane + 32] = w1;
+        if (lane < m) sA6[lane * SR_LDA + i] = g0 * fs;
+        if (lane + 32 < m) sA6[(lane + 32) * SR_LDA + i] = g1 * fs;
+        if (lane < ns) sA6[(m + 64 + lane) * SR_LDA + i] = w0;
+        if (lane + 32 < ns) sA6[(m + 64 + lane + 32) * SR_LDA + i] = w1;
         if (i < nr && lane == 0)
             *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) =
                 make_float4(cs, cs > -INFINITY ? side : 0.f, have ? 1.f : 0.f, 0.f);
     }
-    // E of this block's evicting rows, referenced to M_c by k_far_scan
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int b = idx >> 6, jj = idx & 63;
-        const int r = r0 + jj;
-        sX[b * 65 + jj] = (far_any && b < m && jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
-    }
     __syncthreads();
 
-    // 5. in-block far coefficients, causal: cf[i][jj] for jj <= i
-    blk_zero(acc);
-    if (far_any) blk_nn(acc, sU, 65, sX, 65, m);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int row = ty + 16 * i, jj = tx + 16 * j;
-            sC[row * 65 + jj] = jj <= row ? acc[i][j] : 0.f;
-        }
-    __syncthreads();
-
-    // 6. side numerator, 64 value columns at a time
-    const float *Tp = a.Tp + (size_t)(c * nh + gh) * m * dv;
-    const float *sinks_v = a.sink_v + (size_t)g * ns * dv;
-    for (int tc = 0; tc < dv; tc += 64) {
-        for (int idx = tid; idx < 64 * 64; idx += 256) {
-            const int i = idx >> 6, t = idx & 63;
-            const bool in = tc + t < dv;
-            sX[i * 65 + t] = (far_any && i < m && in) ? Tp[(size_t)i * dv + tc + t] : 0.f;
-            const int r = r0 + i;
-            sV[i * 65 + t] = (far_any && i < nr && r >= j0 && in) ? o1_val(a, g, r - j0, mt)[tc + t] : 0.f;
-            sW[i * 65 + t] = (i < ns && in) ? sinks_v[(size_t)i * dv + tc + t] : 0.f;
-        }
-        __syncthreads();
+    // 5. in-block far coefficients, causal: W[row][jj] = sum_b gain_b(row) E_b(jj)
+    //    for jj <= row, into A6 rows m + jj
+    if (far_any) {
+        const float *sE = sR3;
+        float acc[4][4];
         blk_zero(acc);
-        if (far_any) {
-            blk_nn(acc, sU, 65, sX, 65, m);
-            blk_nn(acc, sC, 65, sV, 65, 64);
+#pragma unroll 4
+        for (int b = 0; b < m; ++b) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) av[i] = sA6[b * SR_LDA + ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bv[j] = sE[b * 65 + tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        if (ns > 0) blk_nn(acc, sF, 65, sW, 65, ns);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int row = ty + 16 * i, t = tc + tx + 16 * j;
-                if (row < nr && t < dv) a.out[((size_t)(r0 + row) * nh + gh) * dv + t] = acc[i][j];
+                const int row = ty + 16 * i, jj = tx + 16 * j;
+                sA6[(m + jj) * SR_LDA + row] = jj <= row ? acc[i][j] : 0.f;
             }
+    }
+    __syncthreads();
+
+    // 6. side numerator = A6 . B6, B6 rows: T entering the block (b < m), the
+    //    evicted values (m + jj), the sink values (m + 64 + x)
+    const float *Tp = a.Tp + (size_t)(c * nh + gh) * m * dv;
+    const float *sinks_v = a.sink_v + (size_t)g * ns * dv;
+    const int kbeg = far_any ? 0 : m + 64;
+    const int ldB = dv + 4, dv4 = dv >> 2;
+    float acc6[8][NV][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc6[i][v][0] = acc6[i][v][1] = acc6[i][v][2] = acc6[i][v][3] = 0.f;
+    for (int k0 = kbeg; k0 < K6; k0 += 32) {
+        const int kn = min(32, K6 - k0);
+        for (int idx = tid; idx < kn * dv4; idx += 256) {
+            const int kk = idx / dv4, c4 = idx % dv4, k = k0 + kk;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < m) {
+                v = *(const float4 *)(Tp + (size_t)k * dv + 4 * c4);
+            } else if (k < m + 64) {
+                const int jj = k - m, r = r0 + jj;
+                if (jj < nr && r >= j0) v = ((const float4 *)o1_val(a, g, r - j0, mt))[c4];
+            } else {
+                v = *(const float4 *)(sinks_v + (size_t)(k - m - 64) * dv + 4 * c4);
+            }
+            *(float4 *)(sR1 + kk * ldB + 4 * c4) = v;
+        }
         __syncthreads();
+#pragma unroll 2
+        for (int kk = 0; kk < kn; ++kk) {
+            const float4 a0 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp);
+            const float4 a1 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp + 4);
+            const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int col = 4 * lane + 128 * v;
+                const float4 bv = col < dv ? *(const float4 *)(sR1 + kk * ldB + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc6[i][v][0] = fmaf(ar[i], bv.x, acc6[i][v][0]);
+                    acc6[i][v][1] = fmaf(ar[i], bv.y, acc6[i][v][1]);
+                    acc6[i][v][2] = fmaf(ar[i], bv.z, acc6[i][v][2]);
+                    acc6[i][v][3] = fmaf(ar[i], bv.w, acc6[i][v][3]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = 8 * warp + i;
+        if (row >= nr) continue;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int col = 4 * lane + 128 * v;
+            if (col < dv)
+                *(float4 *)(a.out + ((size_t)(r0 + row) * nh + gh) * dv + col) =
+                    make_float4(acc6[i][v][0], acc6[i][v][1], acc6[i][v][2], acc6[i][v][3]);
+        }
     }
 }
 
@@ -619,14 +737,19 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a, int rows_per_block) {
 extern const char *const o1_stage_names[O1_NUM_STAGES] = {
     "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near", "commit"};
 
-static size_t readout_smem() { return (size_t)(3 * 64 * 33 + 6 * 64 * 65 + 128) * sizeof(float); }
+static size_t readout_smem(const O1Args &a) {
+    size_t off[6];
+    side_layout(a, off);
+    return off[5] * sizeof(float);
+}
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
     static bool attrs_set = false;
     if (!attrs_set) {
-        cudaFuncSetAttribute(k_side_readout, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)readout_smem());
+        cudaFuncSetAttribute(k_side_readout<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attrs_set = true;
@@ -650,7 +773,8 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     const size_t n = (size_t)a.nh * a.m * a.dv;
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
     mark();
-    k_side_readout<<<dim3(nblk, a.nh), 256, readout_smem(), st>>>(a);
+    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
+    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
     mark();
     if (a.tc) {
         cudaError_t e = o1_launch_gather_tc(a, st);

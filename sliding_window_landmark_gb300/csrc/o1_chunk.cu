@@ -46,11 +46,22 @@ __global__ void k_rope(O1Args a) {
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
         float c = 1.f, s = 0.f;
         if (a.rotate) o1_rope_cs(a.hdr->inv_freq[j], p, c, s);
-        for (int hh = 0; hh < a.nh; ++hh) {
-            const size_t o = ((size_t)r * a.nh + hh) * a.d;
-            const float x0 = a.q[o + j], x1 = a.q[o + j + half];
-            a.qr[o + j] = x0 * c - x1 * s;
-            a.qr[o + j + half] = x1 * c + x0 * s;
+        // 8 heads' loads ahead of their stores
+        for (int h0 = 0; h0 < a.nh; h0 += 8) {
+            float x0[8], x1[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const size_t o = ((size_t)r * a.nh + h0 + u) * a.d;
+                x0[u] = h0 + u < a.nh ? a.q[o + j] : 0.f;
+                x1[u] = h0 + u < a.nh ? a.q[o + j + half] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (h0 + u >= a.nh) break;
+                const size_t o = ((size_t)r * a.nh + h0 + u) * a.d;
+                a.qr[o + j] = x0[u] * c - x1[u] * s;
+                a.qr[o + j + half] = x1[u] * c + x0[u] * s;
+            }
         }
         for (int g = 0; g < a.G; ++g) {
             const size_t o = ((size_t)r * a.G + g) * a.d;
@@ -111,15 +122,28 @@ __global__ __launch_bounds__(256) void k_far_scan(O1Args a) {
     float Mo = a.M[wid], Zo = a.Z[wid];
     float *E = a.E + (size_t)wid * a.cap;
     float *P = a.P + (size_t)wid * a.cap;
+    constexpr int NB = 4;   // blocks whose logits are loaded ahead of their stores
+    float lq[NB][2];
     for (int c = 0; c < a.nsub; ++c) {
         const int r0 = c * O1_SUB;
+        if (c % NB == 0) {
+#pragma unroll
+            for (int q = 0; q < NB; ++q)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r = (c + q) * O1_SUB + hf * 32 + lane;
+                    lq[q][hf] = (r < a.R && r >= j0) ? E[r - j0] : -INFINITY;
+                }
+        }
         float l[2];
         bool ev[2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int r = r0 + hf * 32 + lane;
             ev[hf] = r < a.R && r >= j0;
-            l[hf] = ev[hf] ? E[r - j0] : -INFINITY;
+#pragma unroll
+            for (int q = 0; q < NB; ++q)
+                if (q == c % NB) l[hf] = lq[q][hf];
         }
         const float Mn = fmaxf(Mo, warp_max(fmaxf(l[0], l[1])));
         const float Rf = (Mn == Mo) ? 1.f : expf(Mo - Mn);
@@ -201,13 +225,25 @@ __global__ void k_far_tscan(O1Args a) {
     if (idx >= n) return;
     const size_t wid = idx / a.dv;
     float T = a.T[idx];
-    for (int c = 0; c < a.nsub; ++c) {
-        const float rf = a.Rc[wid * a.nsub + c];
-        float *tp = a.Tp + (size_t)c * n + idx;
-        const float dT = *tp;
-        const float Ts = rf * T;
-        *tp = Ts;
-        T = Ts + dT;
+    // 16 blocks' loads issued before their stores (the compiler cannot
+    // reorder them itself: the stores may alias later loads for all it knows)
+    for (int c0 = 0; c0 < a.nsub; c0 += 16) {
+        float rf[16], dT[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            rf[i] = c < a.nsub ? a.Rc[wid * a.nsub + c] : 1.f;
+            dT[i] = c < a.nsub ? a.Tp[(size_t)c * n + idx] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            if (c < a.nsub) {
+                const float Ts = rf[i] * T;
+                a.Tp[(size_t)c * n + idx] = Ts;
+                T = Ts + dT[i];
+            }
+        }
     }
     a.T[idx] = T;
 }
@@ -347,6 +383,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) sS[(ty + 16 * i) * ldS + 64 * t + tx + 16 * j] = a.scale * acc[t][i][j];
     }
+    __syncthreads();   // scores complete before any row reads them (step 2 or 4)
     if (far_any) {
         float *sMu = sR3;   // [m][65]
         for (int idx = tid; idx < m * m; idx += 256) {
@@ -690,21 +727,32 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
 // would be overwritten within the pass; then, by the last block to arrive
 // (an atomic ticket, no waiting), every group's meta after R pushes
 // (o1b_meta) and the position.
-__global__ __launch_bounds__(256) void k_commit(O1Args a, int rows_per_block) {
+__global__ __launch_bounds__(256) void k_commit(O1Args a) {
     const int g = blockIdx.y;
     const O1Meta mt = o1_meta(a, g);
     const int rstart = max(0, a.R - mt.wg);
     const int d4 = a.d >> 2, dv4 = a.dv >> 2;
-    for (int i = 0; i < rows_per_block; ++i) {
-        const int r = rstart + blockIdx.x * rows_per_block + i;
-        if (r >= a.R) break;
-        const int slot = (int)(((long long)mt.head0 + mt.len0 + r) % mt.wg);
-        const float4 *ks = (const float4 *)(a.kr + ((size_t)r * a.G + g) * a.d);
-        const float4 *vs = (const float4 *)(a.v + ((size_t)r * a.G + g) * a.dv);
-        float4 *kd = (float4 *)(a.ring_k + ((size_t)g * a.w + slot) * a.d);
-        float4 *vd = (float4 *)(a.ring_v + ((size_t)g * a.w + slot) * a.dv);
-        for (int c4 = threadIdx.x; c4 < d4; c4 += blockDim.x) kd[c4] = ks[c4];
-        for (int c4 = threadIdx.x; c4 < dv4; c4 += blockDim.x) vd[c4] = vs[c4];
+    constexpr int RPB = 4;   // rows per block, all loaded before any store
+    const int rb = rstart + blockIdx.x * RPB;
+    for (int c4 = threadIdx.x; c4 < max(d4, dv4); c4 += blockDim.x) {
+        float4 kv[RPB], vv[RPB];
+#pragma unroll
+        for (int i = 0; i < RPB; ++i) {
+            const int r = rb + i;
+            const bool in = r < a.R;
+            kv[i] = (in && c4 < d4) ? ((const float4 *)(a.kr + ((size_t)r * a.G + g) * a.d))[c4]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            vv[i] = (in && c4 < dv4) ? ((const float4 *)(a.v + ((size_t)r * a.G + g) * a.dv))[c4]
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < RPB; ++i) {
+            const int r = rb + i;
+            if (r >= a.R) break;
+            const int slot = (int)(((long long)mt.head0 + mt.len0 + r) % mt.wg);
+            if (c4 < d4) ((float4 *)(a.ring_k + ((size_t)g * a.w + slot) * a.d))[c4] = kv[i];
+            if (c4 < dv4) ((float4 *)(a.ring_v + ((size_t)g * a.w + slot) * a.dv))[c4] = vv[i];
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -790,9 +838,8 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
         else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
     }
     mark();
-    const int rpb = 4;
     const int live = R < a.w ? R : a.w;
-    k_commit<<<dim3((live + rpb - 1) / rpb, a.G), 128, 0, st>>>(a, rpb);
+    k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
     mark();
     return cudaPeekAtLastError();
 }

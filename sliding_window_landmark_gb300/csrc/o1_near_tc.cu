@@ -171,7 +171,9 @@ struct TcPlan {
 
 __device__ __forceinline__ TcPlan tc_plan(const O1Args &a) {
     TcPlan p;
-    p.r0 = blockIdx.x * TC_BM;
+    // row blocks in reverse: the late blocks see full windows and are the
+    // longest, so they start first and the short early ones fill the tail
+    p.r0 = (gridDim.x - 1 - blockIdx.x) * TC_BM;
     p.h = blockIdx.y;
     p.g = p.h / a.hpg;
     p.mt = o1_meta(a, p.g);
@@ -203,32 +205,44 @@ __global__ __launch_bounds__(256) void k_gather_tc(O1Args a, unsigned short *Xk,
     const size_t kpanel = (size_t)a.G * NXp * a.d, vpanel = (size_t)a.G * a.dv * NXp;
     bool range_ok = true;
     const int d2 = a.d >> 1;
-    for (int idx = threadIdx.x; idx < 32 * d2; idx += blockDim.x) {
-        const int i = idx / d2, j2 = idx % d2, x = x0 + i;
-        if (x >= NXp) continue;
-        uint32_t hi = 0, lo = 0;
-        if (x < NX) {
-            const float2 v = ((const float2 *)o1_key(a, g, x, mt))[j2];
-            split_pair(v.x, v.y, hi, lo);
-            range_ok &= fabsf(v.x) < 65504.f && fabsf(v.y) < 65504.f;
+    // loads in batches of 8 ahead of their stores (the stores could alias
+    // later loads as far as the compiler knows, which would serialise them)
+    for (int base = threadIdx.x; base < 32 * d2; base += 8 * 256) {
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + 256 * u, i = idx / d2, j2 = idx % d2, x = x0 + i;
+            v[u] = (idx < 32 * d2 && x < NX) ? ((const float2 *)o1_key(a, g, x, mt))[j2] : make_float2(0.f, 0.f);
         }
-        const size_t o = ((size_t)g * NXp + x) * a.d + 2 * j2;
-        *(uint32_t *)(Xk + o) = hi;
-        *(uint32_t *)(Xk + kpanel + o) = lo;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + 256 * u, i = idx / d2, j2 = idx % d2, x = x0 + i;
+            if (idx >= 32 * d2 || x >= NXp) continue;
+            uint32_t hi, lo;
+            split_pair(v[u].x, v[u].y, hi, lo);
+            range_ok &= fabsf(v[u].x) < 65504.f && fabsf(v[u].y) < 65504.f;
+            const size_t o = ((size_t)g * NXp + x) * a.d + 2 * j2;
+            *(uint32_t *)(Xk + o) = hi;
+            *(uint32_t *)(Xk + kpanel + o) = lo;
+        }
     }
-    for (int idx = threadIdx.x; idx < 32 * a.dv; idx += blockDim.x) {
-        const int i = idx / a.dv, t = idx % a.dv, x = x0 + i;
-        unsigned short hi = 0, lo = 0;
-        if (x < NX) {
-            const float v = o1_val(a, g, x, mt)[t];
-            const __half h = __float2half_rn(v);
-            const __half l = __float2half_rn(v - __half2float(h));
-            hi = __half_as_ushort(h);
-            lo = __half_as_ushort(l);
-            range_ok &= fabsf(v) < 65504.f;
+    for (int base = threadIdx.x; base < 32 * a.dv; base += 8 * 256) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + 256 * u, i = idx / a.dv, t = idx % a.dv, x = x0 + i;
+            v[u] = (idx < 32 * a.dv && x < NX) ? o1_val(a, g, x, mt)[t] : 0.f;
         }
-        ((unsigned short *)sv[i])[t] = hi;
-        svl[i][t] = lo;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = base + 256 * u, i = idx / a.dv, t = idx % a.dv;
+            if (idx >= 32 * a.dv) continue;
+            const __half h = __float2half_rn(v[u]);
+            const __half l = __float2half_rn(v[u] - __half2float(h));
+            range_ok &= fabsf(v[u]) < 65504.f;
+            ((unsigned short *)sv[i])[t] = __half_as_ushort(h);
+            svl[i][t] = __half_as_ushort(l);
+        }
     }
     if (!range_ok) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_FP16_RANGE);
     __syncthreads();

@@ -20,10 +20,13 @@
 //  6. k_side_readout per row: the sinks and the far field (landmark scores,
 //                    u = e^{f-F} mu, gains, far mass and numerator) under one
 //                    exponent (o1b_attend's sink and far parts)
-//  7. k_near         the sliding window, online softmax, merged with the side
-//                    part under one exponent, gate (o1b_attend's window part
-//                    and normalisation; dory_gate1)
-//  8. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
+//  7. k_gather_tc    (tensor-core geometries) the window key sequence as
+//                    fp16 hi / lo panels (o1_near_tc.cu)
+//  8. k_near_tc      the sliding window on the tensor cores, merged with the
+//     or k_near      side part under one exponent, gate (o1b_attend's window
+//                    part and normalisation; dory_gate1); k_near is the fp32
+//                    version for the other geometries
+//  9. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
 //
 // Keys are indexed in X = [ring, oldest first] ++ [this pass's rows]: row r
 // sees X[max(0, len0 + r + 1 - wg) .. len0 + r] and evicts X[r - j0] once

@@ -262,9 +262,10 @@ __global__ void k_far_tscan(O1Args a) {
 //   far numerator = sum_b gain_b (R_c T_{c-1})_b + sum_{evicting j <= row} cf_j v_ev(j),
 //   cf_j = sum_b gain_b E_bj;
 //   sinks: p_x = e^{scale q'.sink_x - c_s}.
-// The side numerator goes to `out` (the window kernel finishes the row
-// there) and (c_s, side mass) to the side header; c_s = -inf marks a row
-// with no sinks and no far field.
+// Then the merge with the row's window part, which the window kernel left
+// in `out` (numerator) and in the row's window header (reference, mass,
+// true max): one exponent for all three parts, the 1e-30 floor, the gate.
+// c_s = -inf marks a row with no sinks and no far field.
 //
 // Layout (256 threads, 8 warps). The products are register-tiled with
 // float4 shared-memory reads:
@@ -286,8 +287,8 @@ __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
     off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks
     off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
     off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
-    off[4] = off[3] + 64 * 65;                               // F per row [64], M_c [64]
-    off[5] = off[4] + 128;                                   // total (floats)
+    off[4] = off[3] + 64 * 65;                               // F, M_c, c_s, side mass, merge factors [64] each
+    off[5] = off[4] + 6 * 64;                                // total (floats)
 }
 
 __device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
@@ -313,15 +314,6 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
     const int m = a.m, d = a.d, dv = a.dv, nh = a.nh, ns = a.ns;
     const bool far_any = mt.farl0 + max(0, r0 + nr - j0) > 0;
-    if (!far_any && ns == 0) {
-        for (int idx = tid; idx < nr * dv; idx += 256) {
-            const int i = idx / dv, t = idx % dv;
-            a.out[((size_t)(r0 + i) * nh + gh) * dv + t] = 0.f;
-        }
-        for (int i = tid; i < nr; i += 256)
-            *(float4 *)(a.fh + ((size_t)(r0 + i) * nh + gh) * 4) = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        return;
-    }
     size_t off[6];
     side_layout(a, off);
     const int nbt = (m + ns + 63) / 64;
@@ -333,6 +325,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     float *sR3 = sm + off[3];
     float *sRow = sm + off[4];
     float *sMc = sRow + 64;
+    float *sCs = sMc + 64, *sSm = sCs + 64, *sFa = sSm + 64, *sFb = sFa + 64;
 
     // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks
     {
@@ -463,11 +456,30 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         if (lane + 32 < m) sA6[(lane + 32) * SR_LDA + i] = g1 * fs;
         if (lane < ns) sA6[(m + 64 + lane) * SR_LDA + i] = w0;
         if (lane + 32 < ns) sA6[(m + 64 + lane + 32) * SR_LDA + i] = w1;
-        if (i < nr && lane == 0)
-            *(float4 *)(a.fh + ((size_t)r * nh + gh) * 4) =
-                make_float4(cs, cs > -INFINITY ? side : 0.f, have ? 1.f : 0.f, 0.f);
+        if (lane == 0) {
+            sCs[i] = cs;
+            sSm[i] = cs > -INFINITY ? side : 0.f;
+        }
     }
     __syncthreads();
+    // merge factors with the window part of each row (its header from the
+    // window kernel): c = max(window max, c_s) (the pages' c_all), the
+    // denominator floored at 1e-30 in those units
+    if (tid < 64) {
+        float fa = 0.f, fb = 0.f;
+        if (tid < nr) {
+            const float4 wh = *(const float4 *)(a.fh + ((size_t)(r0 + tid) * nh + gh) * 4);
+            const float cs = sCs[tid];
+            const float cc = fmaxf(wh.z, cs);
+            const float al = expf(wh.x - cc);
+            const float be = cs > -INFINITY ? expf(cs - cc) : 0.f;
+            const float den = fmaxf(al * wh.y + be * sSm[tid], 1e-30f);
+            fa = al / den;
+            fb = be / den;
+        }
+        sFa[tid] = fa;
+        sFb[tid] = fb;
+    }
 
     // 5. in-block far coefficients, causal: W[row][jj] = sum_b gain_b(row) E_b(jj)
     //    for jj <= row, into A6 rows m + jj
@@ -501,7 +513,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     //    evicted values (m + jj), the sink values (m + 64 + x)
     const float *Tp = a.Tp + (size_t)(c * nh + gh) * m * dv;
     const float *sinks_v = a.sink_v + (size_t)g * ns * dv;
-    const int kbeg = far_any ? 0 : m + 64;
+    const int kbeg = far_any ? 0 : (ns > 0 ? m + 64 : K6);
     const int ldB = dv + 4, dv4 = dv >> 2;
     float acc6[8][NV][4];
 #pragma unroll
@@ -544,16 +556,30 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         }
         __syncthreads();
     }
+    // 7. out = fa * (window numerator, already in out) + fb * side numerator,
+    //    then the gate (dory_gate1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = 8 * warp + i;
         if (row >= nr) continue;
+        const float fa = sFa[row], fb = sFb[row];
+        const size_t ro = ((size_t)(r0 + row) * nh + gh) * dv;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int col = 4 * lane + 128 * v;
-            if (col < dv)
-                *(float4 *)(a.out + ((size_t)(r0 + row) * nh + gh) * dv + col) =
-                    make_float4(acc6[i][v][0], acc6[i][v][1], acc6[i][v][2], acc6[i][v][3]);
+            if (col < dv) {
+                const float4 ow = *(const float4 *)(a.out + ro + col);
+                float y0 = fa * ow.x + fb * acc6[i][v][0], y1 = fa * ow.y + fb * acc6[i][v][1];
+                float y2 = fa * ow.z + fb * acc6[i][v][2], y3 = fa * ow.w + fb * acc6[i][v][3];
+                if (a.gate) {
+                    const float4 gv = *(const float4 *)(a.gate + ro + col);
+                    y0 = y0 / (1.f + expf(-gv.x));
+                    y1 = y1 / (1.f + expf(-gv.y));
+                    y2 = y2 / (1.f + expf(-gv.z));
+                    y3 = y3 / (1.f + expf(-gv.w));
+                }
+                *(float4 *)(a.out + ro + col) = make_float4(y0, y1, y2, y3);
+            }
         }
     }
 }
@@ -564,10 +590,9 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // so one staged key/value tile serves every head of the group. 8 warps, 4
 // slots each; within a key tile, lane = key. Keys: the window range
 // X[lo(r0) .. hi(last row)]; each slot masks to its own row's window.
-// Online softmax (running max and sum), then the side part (sinks + far
-// field) merged under the common exponent c = max(window max, c_s) — the
-// pages' c_all — the denominator floored at 1e-30 in those units, and the
-// gate.
+// Online softmax (running max and sum); the row's window numerator goes to
+// `out` and (max, mass, max) to its window header, for the side readout to
+// merge.
 template <int NV>
 __global__ __launch_bounds__(256) void k_near(O1Args a) {
     extern __shared__ float sm[];
@@ -692,34 +717,21 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
         }
     }
 
+    // the window part of the row: numerator into `out`, (reference, mass,
+    // max) into the row's window header; the side readout merges
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (!act[i]) continue;
         const int s = warp * 4 + i;
         const int r = r0 + s / hpg, hh = g * hpg + s % hpg;
-        const float4 hd = *(const float4 *)(a.fh + ((size_t)r * a.nh + hh) * 4);
-        const float cexp = fmaxf(mrow[i], hd.x);
-        const float al = expf(mrow[i] - cexp);
-        const float be = hd.x > -INFINITY ? expf(hd.x - cexp) : 0.f;
-        const float den = fmaxf(be * hd.y + al * lrow[i], 1e-30f);
         float *o = a.out + ((size_t)r * a.nh + hh) * a.dv;
-        const float *gt = a.gate ? a.gate + ((size_t)r * a.nh + hh) * a.dv : nullptr;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int col = lane * 4 + 128 * v;
-            if (col >= a.dv) continue;
-            const float4 nf = *(const float4 *)(o + col);
-            float y[4] = {(be * nf.x + al * acc[i][v][0]) / den, (be * nf.y + al * acc[i][v][1]) / den,
-                          (be * nf.z + al * acc[i][v][2]) / den, (be * nf.w + al * acc[i][v][3]) / den};
-            if (gt) {
-                const float4 gv = *(const float4 *)(gt + col);
-                y[0] = y[0] / (1.f + expf(-gv.x));
-                y[1] = y[1] / (1.f + expf(-gv.y));
-                y[2] = y[2] / (1.f + expf(-gv.z));
-                y[3] = y[3] / (1.f + expf(-gv.w));
-            }
-            *(float4 *)(o + col) = make_float4(y[0], y[1], y[2], y[3]);
+            if (col < a.dv) *(float4 *)(o + col) = make_float4(acc[i][v][0], acc[i][v][1], acc[i][v][2], acc[i][v][3]);
         }
+        if (lane == 0)
+            *(float4 *)(a.fh + ((size_t)r * a.nh + hh) * 4) = make_float4(mrow[i], lrow[i], mrow[i], 0.f);
     }
 }
 
@@ -786,7 +798,7 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a) {
 // ------------------------------------------------------------- launchers
 
 extern const char *const o1_stage_names[O1_NUM_STAGES] = {
-    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near", "commit"};
+    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "gather_tc", "near", "side_readout", "commit"};
 
 static size_t readout_smem(const O1Args &a) {
     size_t off[6];
@@ -824,9 +836,6 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     const size_t n = (size_t)a.nh * a.m * a.dv;
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
     mark();
-    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
-    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
-    mark();
     if (a.tc) {
         cudaError_t e = o1_launch_gather_tc(a, st);
         if (e != cudaSuccess) return e;
@@ -840,6 +849,9 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
         if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
         else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
     }
+    mark();
+    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
+    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
     mark();
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);

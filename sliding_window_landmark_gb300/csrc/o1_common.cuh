@@ -18,7 +18,7 @@
 #define O1_MAX_HPG 16
 #define O1_MAX_NS 64
 #define O1_MAX_W (1 << 20)
-#define O1_TC_BN 64            // keys per tile of the tensor-core window path
+#define O1_TC_BN 128           // keys per tile of the tensor-core window path
 #define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
 
 // First bytes of a state buffer.
@@ -69,7 +69,9 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   Mc, Rc [nh][m][nsub]  block max and rescale factor
 //   Tp [nsub][nh][m][dv]  far value sums: increments, then the value sum
 //                         entering each block, rescaled to its max
-//   fh [cap][nh] x 4      per row-head side header (c_s, side mass, have, -)
+//   fh [cap][nh] x 4      per row-head window header, written by the window
+//                         kernel: (reference c_w, mass l, true max, -), the
+//                         window numerator being in `out` relative to c_w
 // and, when the tensor-core window path serves the geometry, the window key
 // sequence as fp16 hi / lo panels (nxp keys per group, zero past the end):
 //   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]
@@ -79,9 +81,10 @@ struct O1Scratch {
 };
 
 // The tensor-core window path: d in 64-wide chunks (one 128-byte swizzle row
-// of fp16), at most 256 (Q_lo fills TMEM columns 384..511), dv a multiple of
-// 32 (TMEM load width) up to 256, and a window wide enough to pay for the
-// panel gather.
+// of fp16), at most 256 (Q_hi and Q_lo take 2 x 64 KB of shared memory at
+// d = 256 and leave three 32 KB ring slots), dv a multiple of 32 (TMEM load
+// width) up to 256 (O fills TMEM columns 0..255, the two S buffers
+// 256..511), and a window wide enough to pay for the panel gather.
 static inline bool o1_tc_supported(const o1_geom &g) {
     return g.d % 64 == 0 && g.d <= 256 && g.dv % 32 == 0 && g.dv <= 256 && g.window >= O1_TC_MIN_WINDOW;
 }

@@ -18,15 +18,22 @@
 //               ++ [this pass's rotated keys] as dense fp16 panels
 //               Xk[hi|lo][g][x][d] and, transposed, XvT[hi|lo][g][t][x],
 //               zero past the end.
-//  k_near_tc    one CTA per (128 query rows, head): Q_hi resident in smem
-//               (128-byte swizzle) and Q_lo in TMEM; key tiles of 64 stream
-//               through a TMA ring; S = Q.K^T into one of two TMEM buffers;
-//               softmax threads (one per row) mask to the row's window, keep
-//               a running max, write P (hi and lo, fp16) back over S in
-//               TMEM; O += P.V with P read from TMEM. The epilogue merges
-//               the side part (sinks + far field) under the common
-//               exponent, with the 1e-30 floor, applies the gate, and writes
-//               the tile through shared memory with coalesced stores.
+//  k_near_tc    one CTA per (128 query rows, head): Q_hi and Q_lo resident in
+//               smem (128-byte swizzle); key tiles of 128 stream through a
+//               TMA ring (a key d-chunk or a value half-tile per 32 KB slot);
+//               S = Q.K^T (N = 128) into one of two TMEM buffers; softmax
+//               threads (one per row) mask to the row's window, keep a
+//               running max, write P (hi and lo, fp16) back over S in TMEM;
+//               O += P.V with P read from TMEM. The epilogue writes the
+//               window numerator O to `out` through shared memory with
+//               coalesced stores, and each row's (reference, mass, true max)
+//               to its window header; the side readout merges and gates.
+//
+// Tile width: a 128 x N x 16 MMA costs about the same time on the tensor
+// pipe for N = 64 and N = 128, so S is issued with N = 128 (48 MMAs per
+// 128 keys at d = 256 instead of 96); that needs both S buffers at 128
+// columns, so with O at up to 256 columns the TMEM is full and Q_lo stays
+// in smem (an SS MMA for lo.hi costs the same as the TS form).
 //
 // Roles: warps 0-3 softmax / epilogue (thread = TMEM lane = query row),
 // warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner). Every wait is
@@ -46,8 +53,7 @@ constexpr int TC_BN = O1_TC_BN;    // keys per tile
 constexpr int TC_SLOT = 32768;     // bytes per ring slot
 constexpr int TC_THREADS = 192;
 constexpr int TC_O_COL = 0;        // O accumulator: TMEM columns [0, dv)
-constexpr int TC_S_COL = 256;      // S / P buffers: [256, 320) and [320, 384)
-constexpr int TC_QLO_COL = 384;    // Q_lo as fp16 pairs: [384, 384 + d/2)
+constexpr int TC_S_COL = 256;      // S / P buffers: [256, 384) and [384, 512)
 constexpr float TC_RESCALE = 8.f;  // log2-units headroom before O is rescaled
 constexpr long long TC_WAIT_CYCLES = 4000000000LL;
 
@@ -165,7 +171,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // The CTA's tile schedule; every role derives the same one.
 struct TcPlan {
-    int r0, nr, h, g, kt0, nt, nkc, nks;
+    int r0, nr, h, g, kt0, nt, nkc;
     O1Meta mt;
 };
 
@@ -182,8 +188,7 @@ __device__ __forceinline__ TcPlan tc_plan(const O1Args &a) {
     const int hi_last = p.mt.len0 + p.r0 + p.nr - 1;
     p.kt0 = lo_first & ~7;   // TMA x coordinates of the fp16 value panel: 16-byte aligned
     p.nt = (hi_last - p.kt0) / TC_BN + 1;
-    p.nkc = a.d / 64;        // 64 fp16 = one 128-byte swizzle row
-    p.nks = (p.nkc + 1) / 2; // a K slot holds two d-chunks, hi and lo each
+    p.nkc = a.d / 64;        // 64 fp16 = one 128-byte swizzle row; one ring slot per d-chunk (hi, lo)
     return p;
 }
 
@@ -258,6 +263,11 @@ __global__ __launch_bounds__(256) void k_gather_tc(O1Args a, unsigned short *Xk,
 
 // --------------------------------------------------------------- attention
 
+// Shared memory: Q_hi [nkc][128 rows][128 B], Q_lo the same, then nslot ring
+// slots of 32 KB, then barriers. A key item is one d-chunk of a 128-key tile
+// (hi 16 KB, lo 16 KB); a value item is the hi or lo half of V^T for 64 keys
+// (dv rows x 128 B). Per tile j the ring carries K(j) chunks 0..nkc-1, later
+// V(j) as hi(keys 0-63), lo(0-63), hi(64-127), lo(64-127).
 __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __grid_constant__ CUtensorMap mk,
                                                             const __grid_constant__ CUtensorMap mv, int NXp, int nslot) {
     extern __shared__ __align__(1024) unsigned char smraw[];
@@ -265,15 +275,15 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
     const TcPlan pl = tc_plan(a);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = a.d, dv = a.dv;
-    unsigned char *sQ = sm;                                  // Q_hi: nkc x 16 KB
-    unsigned char *sR = sQ + (size_t)pl.nkc * 16384;         // nslot x 32 KB
+    unsigned char *sQh = sm;                                 // nkc x 16 KB
+    unsigned char *sQl = sQh + (size_t)pl.nkc * 16384;       // nkc x 16 KB
+    unsigned char *sR = sQl + (size_t)pl.nkc * 16384;        // nslot x 32 KB
     uint64_t *bars = (uint64_t *)(sR + (size_t)nslot * TC_SLOT);
     uint64_t *full = bars, *empty = bars + nslot;
     uint64_t *s_full = bars + 2 * nslot, *p_full = s_full + 2, *pv_done = p_full + 2, *o_done = pv_done + 1,
              *q_ready = o_done + 1;
     uint32_t *tslot = (uint32_t *)(q_ready + 1);
     volatile int *abort = (volatile int *)(tslot + 1);
-    float *srow = (float *)(tslot + 2);                     // [128][2]: the rows' merge factors
 
     if (tid == 0) {
         for (int i = 0; i < nslot; ++i) {
@@ -302,11 +312,10 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
 
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer
+        // (starts at once: the Q tile has its own smem)
         if (lane == 0) {
             int it = 0;
             const int ybase = pl.g * NXp;
-            // the ring carries Q_lo into TMEM first
-            if (!mbar_wait(q_ready, 0, abort)) it = -1;
             auto next = [&](uint32_t bytes) -> int {
                 const int s = it % nslot;
                 if (!mbar_wait(&empty[s], ((it / nslot) & 1) ^ 1, abort)) return -1;
@@ -314,33 +323,31 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 ++it;
                 return s;
             };
-            // K slot ks: d-chunks 2ks and 2ks + 1, each as [64 keys x 64] hi then lo (8 KB boxes)
-            auto load_s = [&](int j) -> bool {
-                for (int ks = 0; ks < pl.nks; ++ks) {
-                    const int nb = min(2, pl.nkc - 2 * ks);
-                    const int s = next(nb * 16384);
+            auto load_k = [&](int j) -> bool {
+                for (int c = 0; c < pl.nkc; ++c) {
+                    const int s = next(2 * TC_BN * 128);
                     if (s < 0) return false;
-                    for (int b = 0; b < nb; ++b)
-                        for (int hl = 0; hl < 2; ++hl)
-                            tma_3d(sR + (size_t)s * TC_SLOT + b * 16384 + hl * 8192, &mk, 64 * (2 * ks + b),
-                                   ybase + pl.kt0 + TC_BN * j, hl, &full[s]);
+                    for (int hl = 0; hl < 2; ++hl)
+                        tma_3d(sR + (size_t)s * TC_SLOT + hl * (TC_BN * 128), &mk, 64 * c, ybase + pl.kt0 + TC_BN * j, hl,
+                               &full[s]);
                 }
                 return true;
             };
-            // V slots: [dv x 64 keys] hi, then lo
             auto load_v = [&](int j) -> bool {
-                for (int hl = 0; hl < 2; ++hl) {
-                    const int s = next(dv * 128);
-                    if (s < 0) return false;
-                    tma_3d(sR + (size_t)s * TC_SLOT, &mv, pl.kt0 + TC_BN * j, pl.g * dv, hl, &full[s]);
-                }
+                for (int kh = 0; kh < 2; ++kh)
+                    for (int hl = 0; hl < 2; ++hl) {
+                        const int s = next(dv * 128);
+                        if (s < 0) return false;
+                        tma_3d(sR + (size_t)s * TC_SLOT, &mv, pl.kt0 + TC_BN * j + 64 * kh, pl.g * dv, hl, &full[s]);
+                    }
                 return true;
             };
-            bool ok = it == 0 && load_s(0);
+            bool ok = load_k(0);
             for (int j = 0; ok && j < pl.nt; ++j) {
-                if (j + 1 < pl.nt) ok = load_s(j + 1);
+                if (j + 1 < pl.nt) ok = load_k(j + 1);
                 if (ok) ok = load_v(j);
             }
+
             if (!ok && it > 0) {
                 // drain: wait (bounded) for this thread's copies still in flight
                 for (int i = max(0, it - nslot); i < it; ++i) {
@@ -354,26 +361,23 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t id_s = idesc_f16(TC_BM, TC_BN), id_o = idesc_f16(TC_BM, dv);
-            const uint32_t qa = su32(sQ), ra = su32(sR);
+            const uint32_t qh0 = su32(sQh), ql0 = su32(sQl), ra = su32(sR);
             int it = 0;
             bool ok = mbar_wait(q_ready, 0, abort);
             tc_after();
-            // S = Q_hi.K_hi + Q_hi.K_lo + Q_lo.K_hi (Q_lo read from TMEM)
+            // S = Q_hi.K_hi + Q_hi.K_lo + Q_lo.K_hi, one ring slot per d-chunk
             auto issue_s = [&](int j) -> bool {
                 const uint32_t dcol = tmem + TC_S_COL + TC_BN * (j & 1);
-                for (int ks = 0; ks < pl.nks; ++ks) {
+                for (int c = 0; c < pl.nkc; ++c) {
                     const int s = it % nslot;
                     if (!mbar_wait(&full[s], (it / nslot) & 1, abort)) return false;
                     tc_after();
-                    const int nb = min(2, pl.nkc - 2 * ks);
-                    for (int b = 0; b < nb; ++b) {
-                        const int ch = 2 * ks + b;
-                        const uint32_t kh = ra + s * TC_SLOT + b * 16384, kl = kh + 8192, qh = qa + ch * 16384;
-                        for (int k = 0; k < 4; ++k) {
-                            mma_ss(dcol, desc_sw128(qh + 32 * k), desc_sw128(kh + 32 * k), id_s, (ch | k) ? 1u : 0u);
-                            mma_ss(dcol, desc_sw128(qh + 32 * k), desc_sw128(kl + 32 * k), id_s, 1u);
-                            mma_ts(dcol, tmem + TC_QLO_COL + 32 * ch + 8 * k, desc_sw128(kh + 32 * k), id_s, 1u);
-                        }
+                    const uint32_t kh = ra + s * TC_SLOT, kl = kh + TC_BN * 128, qh = qh0 + c * 16384,
+                                   ql = ql0 + c * 16384;
+                    for (int k = 0; k < 4; ++k) {
+                        mma_ss(dcol, desc_sw128(qh + 32 * k), desc_sw128(kh + 32 * k), id_s, (c | k) ? 1u : 0u);
+                        mma_ss(dcol, desc_sw128(qh + 32 * k), desc_sw128(kl + 32 * k), id_s, 1u);
+                        mma_ss(dcol, desc_sw128(ql + 32 * k), desc_sw128(kh + 32 * k), id_s, 1u);
                     }
                     mma_commit(&empty[s]);
                     ++it;
@@ -381,23 +385,25 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 mma_commit(&s_full[j & 1]);
                 return true;
             };
-            // O += P_hi.V_hi + P_hi.V_lo + P_lo.V_hi
+            // O += P_hi.V_hi + P_hi.V_lo + P_lo.V_hi, per 64-key half
             auto issue_pv = [&](int j) -> bool {
                 const uint32_t pcol = tmem + TC_S_COL + TC_BN * (j & 1);
-                const int sh = it % nslot, sl = (it + 1) % nslot;
-                if (!mbar_wait(&full[sh], (it / nslot) & 1, abort)) return false;
-                if (!mbar_wait(&full[sl], ((it + 1) / nslot) & 1, abort)) return false;
-                tc_after();
-                const uint32_t vh = ra + sh * TC_SLOT, vl = ra + sl * TC_SLOT;
-                for (int k = 0; k < TC_BN / 16; ++k) {
-                    const uint32_t ph = pcol + 16 * k, plo = ph + 8;   // keys 16k .. 16k + 15
-                    mma_ts(tmem + TC_O_COL, ph, desc_sw128(vh + 32 * k), id_o, (j | k) ? 1u : 0u);
-                    mma_ts(tmem + TC_O_COL, ph, desc_sw128(vl + 32 * k), id_o, 1u);
-                    mma_ts(tmem + TC_O_COL, plo, desc_sw128(vh + 32 * k), id_o, 1u);
+                for (int kh = 0; kh < 2; ++kh) {
+                    const int sh = it % nslot, sl = (it + 1) % nslot;
+                    if (!mbar_wait(&full[sh], (it / nslot) & 1, abort)) return false;
+                    if (!mbar_wait(&full[sl], ((it + 1) / nslot) & 1, abort)) return false;
+                    tc_after();
+                    const uint32_t vh = ra + sh * TC_SLOT, vl = ra + sl * TC_SLOT;
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t ph = pcol + 64 * kh + 16 * k, plo = ph + 8;   // keys 64kh + 16k .. + 15
+                        mma_ts(tmem + TC_O_COL, ph, desc_sw128(vh + 32 * k), id_o, (j | kh | k) ? 1u : 0u);
+                        mma_ts(tmem + TC_O_COL, ph, desc_sw128(vl + 32 * k), id_o, 1u);
+                        mma_ts(tmem + TC_O_COL, plo, desc_sw128(vh + 32 * k), id_o, 1u);
+                    }
+                    mma_commit(&empty[sh]);
+                    mma_commit(&empty[sl]);
+                    it += 2;
                 }
-                mma_commit(&empty[sh]);
-                mma_commit(&empty[sl]);
-                it += 2;
                 mma_commit(pv_done);
                 return true;
             };
@@ -420,13 +426,10 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         const bool valid = row < pl.nr;
         const int lo = max(0, pl.mt.len0 + r + 1 - pl.mt.wg), hi = pl.mt.len0 + r;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        // Q tile: hi -> smem (128-byte swizzle: 16-byte unit u of row i stored
-        // at unit u ^ (i & 7)); lo -> staged in the ring, then each thread
-        // moves its own row into TMEM lanes as fp16 pairs
+        // Q tile -> smem as fp16 hi and lo (128-byte swizzle: 16-byte unit u
+        // of row i stored at unit u ^ (i & 7))
         {
             const int d4 = d >> 2;
-            const int lstride = (d >> 1) + 1;   // words per staged lo row (padded)
-            uint32_t *stage = (uint32_t *)sR;
             bool q_ok = true;
             for (int base = tid; base < TC_BM * d4; base += 16 * TC_BM) {
                 float4 vv[16];
@@ -448,22 +451,12 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                     split_pair(vv[k].x, vv[k].y, h01, l01);
                     split_pair(vv[k].z, vv[k].w, h23, l23);
                     const int e = 4 * u4, ch = e >> 6, u = (e & 63) >> 3, half8 = (e & 7) * 2;
-                    *(uint2 *)(sQ + (size_t)ch * 16384 + i * 128 + ((u ^ (i & 7)) << 4) + half8) =
-                        make_uint2(h01, h23);
-                    stage[i * lstride + 2 * u4] = l01;
-                    stage[i * lstride + 2 * u4 + 1] = l23;
+                    const size_t off = (size_t)ch * 16384 + i * 128 + ((u ^ (i & 7)) << 4) + half8;
+                    *(uint2 *)(sQh + off) = make_uint2(h01, h23);
+                    *(uint2 *)(sQl + off) = make_uint2(l01, l23);
                 }
             }
             if (!q_ok) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_FP16_RANGE);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            uint32_t w[32];
-            for (int c = 0; c < d / 64; ++c) {
-#pragma unroll
-                for (int t = 0; t < 32; ++t) w[t] = stage[tid * lstride + 32 * c + t];
-                TMEM_ST32(lane_base + TC_QLO_COL + 32 * c, w);
-            }
-            tmem_st_wait();
-            tc_before();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(q_ready);
         }
@@ -471,34 +464,35 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         const float sc2 = a.scale * 1.4426950408889634f;   // scores in log2 units
         float mref = -INFINITY, mtrue = -INFINITY, l = 0.f;
         bool ok = true;
-        uint32_t v[TC_BN];
+        uint32_t v[64];
         for (int j = 0; j < pl.nt && ok; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort));
             if (!ok) break;
             tc_after();
             const uint32_t scol = lane_base + TC_S_COL + TC_BN * (j & 1);
-#pragma unroll
-            for (int c = 0; c < TC_BN / 32; ++c) TMEM_LD32(scol + 32 * c, (&v[32 * c]));
-            tmem_ld_wait();
             const int x0 = pl.kt0 + TC_BN * j;
             const bool all_in = valid && x0 >= lo && x0 + TC_BN - 1 <= hi;
-            // scale to log2 units, mask to the row's window, row max (4 chains)
+            const int a0 = lo - x0, a1 = hi - x0;   // valid columns [a0, a1]
+            // pass 1: the tile's row max (scores scaled to log2 units, masked).
+            // A tile inside the row's window takes a path without per-column
+            // predicates (64 selects on a handful of predicate registers
+            // serialise); tiles that cross a window edge take the masked one.
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (all_in) {
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                TMEM_LD32(scol + 64 * hf, (&v[0]));
+                TMEM_LD32(scol + 64 * hf + 32, (&v[32]));
+                tmem_ld_wait();
+                if (all_in) {
 #pragma unroll
-                for (int c = 0; c < TC_BN; ++c) {
-                    const float s = __uint_as_float(v[c]) * sc2;
-                    v[c] = __float_as_uint(s);
-                    m4[c & 3] = fmaxf(m4[c & 3], s);
-                }
-            } else {
-                const int a0 = lo - x0, a1 = hi - x0;   // valid columns [a0, a1]
+                    for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(v[c]) * sc2);
+                } else {
+                    const int b0 = a0 - 64 * hf, b1 = a1 - 64 * hf;   // valid columns of this half
 #pragma unroll
-                for (int c = 0; c < TC_BN; ++c) {
-                    const bool in = valid && c >= a0 && c <= a1;
-                    const float s = in ? __uint_as_float(v[c]) * sc2 : -INFINITY;
-                    v[c] = __float_as_uint(s);
-                    m4[c & 3] = fmaxf(m4[c & 3], s);
+                    for (int c = 0; c < 64; ++c) {
+                        const bool in = valid && c >= b0 && c <= b1;
+                        m4[c & 3] = fmaxf(m4[c & 3], in ? __uint_as_float(v[c]) * sc2 : -INFINITY);
+                    }
                 }
             }
             const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -525,30 +519,50 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 }
                 mref = mnew;
             }
-            // P = 2^(s - mref) as fp16 pairs (two keys per column, the lower key
-            // in the low half), per 16-key group q: hi in columns 16q..16q+7, lo
-            // in 16q+8..16q+15. A group's scores are read before its words are
-            // written. No key is valid in this row yet iff mref is -inf.
+            // pass 2: P = 2^(s - mref) as fp16 pairs (two keys per column, the
+            // lower key in the low half), per 16-key group q: hi in columns
+            // 16q..16q+7, lo in 16q+8..16q+15, written over the scores of the
+            // same 64-key half after they are read. No key is valid in this
+            // row yet iff mref is -inf.
             const float mr = mref > -INFINITY ? mref : 0.f;
             float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                TMEM_LD32(scol + 64 * hf, (&v[0]));
+                TMEM_LD32(scol + 64 * hf + 32, (&v[32]));
+                tmem_ld_wait();
+                // exponent arguments s - mref in place; masked columns -inf
+                // (2^-inf = 0), with predicates only on tiles that cross an edge
+                if (all_in) {
 #pragma unroll
-            for (int q = 0; q < TC_BN / 16; ++q) {
-                float pq[16];
+                    for (int c = 0; c < 64; ++c) v[c] = __float_as_uint(fmaf(__uint_as_float(v[c]), sc2, -mr));
+                } else {
+                    const int b0 = a0 - 64 * hf, b1 = a1 - 64 * hf;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) pq[t] = ex2(__uint_as_float(v[16 * q + t]) - mr);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    uint32_t hw, lw;
-                    split_pair(pq[2 * t], pq[2 * t + 1], hw, lw);
-                    ls0 += pq[2 * t];
-                    ls1 += pq[2 * t + 1];
-                    v[16 * q + t] = hw;
-                    v[16 * q + 8 + t] = lw;
+                    for (int c = 0; c < 64; ++c) {
+                        const bool in = valid && c >= b0 && c <= b1;
+                        v[c] = __float_as_uint(in ? fmaf(__uint_as_float(v[c]), sc2, -mr) : -INFINITY);
+                    }
                 }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float pq[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) pq[t] = ex2(__uint_as_float(v[16 * q + t]));
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        uint32_t hw, lw;
+                        split_pair(pq[2 * t], pq[2 * t + 1], hw, lw);
+                        ls0 += pq[2 * t];
+                        ls1 += pq[2 * t + 1];
+                        v[16 * q + t] = hw;
+                        v[16 * q + 8 + t] = lw;
+                    }
+                }
+                TMEM_ST32(scol + 64 * hf, (&v[0]));
+                TMEM_ST32(scol + 64 * hf + 32, (&v[32]));
             }
             l += ls0 + ls1;
-#pragma unroll
-            for (int c = 0; c < TC_BN / 32; ++c) TMEM_ST32(scol + 32 * c, (&v[32 * c]));
             tmem_st_wait();
             tc_before();
             mbar_arrive(&p_full[j & 1]);
@@ -556,21 +570,14 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, 0, abort));
         tc_after();
         if (ok) {
-            // merge factors of this row with the side part (sinks + far field):
-            // out = (al O + be side_num) / den, then the gate
-            float al = 0.f, be = 0.f, den = 1.f;
-            if (valid) {
-                const float4 hd = *(const float4 *)(a.fh + ((size_t)r * a.nh + pl.h) * 4);
-                const float cw = mref * 0.6931471805599453f;   // reference of l and O, natural units
-                const float c = fmaxf(mtrue * 0.6931471805599453f, hd.x);
-                al = expf(cw - c);
-                be = hd.x > -INFINITY ? expf(hd.x - c) : 0.f;
-                den = fmaxf(al * l + be * hd.y, 1e-30f);
-            }
-            srow[2 * row] = al / den;
-            srow[2 * row + 1] = be / den;
-            // the O row -> smem (the ring is free: every load was consumed)
-            float *so = (float *)sR;
+            // the window part of each row: its header (reference, mass, true
+            // max, natural units) and its numerator O, which goes to `out`
+            // through shared memory with coalesced stores; the side readout
+            // merges it with the sinks and the far field and applies the gate
+            if (valid)
+                *(float4 *)(a.fh + ((size_t)r * a.nh + pl.h) * 4) = make_float4(
+                    mref * 0.6931471805599453f, l, mtrue * 0.6931471805599453f, 0.f);
+            float *so = (float *)sm;   // Q and the ring are free: every MMA has completed
             const int ostride = dv + 4;
             uint32_t o[32];
             for (int c = 0; c < dv / 32; ++c) {
@@ -583,39 +590,12 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                                     __uint_as_float(o[4 * t4 + 2]), __uint_as_float(o[4 * t4 + 3]));
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            // coalesced: consecutive threads take consecutive float4s of a row
             const int dv4 = dv >> 2;
             const int n4 = pl.nr * dv4;
-            for (int base = tid; base < n4; base += 4 * TC_BM) {
-                float4 ns[4], gv[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int idx = base + k * TC_BM;
-                    if (idx < n4) {
-                        const int i = idx / dv4, c4 = idx % dv4;
-                        const size_t go = ((size_t)(pl.r0 + i) * a.nh + pl.h) * dv + 4 * c4;
-                        ns[k] = *(const float4 *)(a.out + go);
-                        gv[k] = a.gate ? *(const float4 *)(a.gate + go) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int idx = base + k * TC_BM;
-                    if (idx >= n4) break;
-                    const int i = idx / dv4, c4 = idx % dv4;
-                    const float fa = srow[2 * i], fb = srow[2 * i + 1];
-                    const float4 ow = *(const float4 *)(so + i * ostride + 4 * c4);
-                    float y0 = fa * ow.x + fb * ns[k].x, y1 = fa * ow.y + fb * ns[k].y;
-                    float y2 = fa * ow.z + fb * ns[k].z, y3 = fa * ow.w + fb * ns[k].w;
-                    if (a.gate) {
-                        y0 = y0 / (1.f + expf(-gv[k].x));
-                        y1 = y1 / (1.f + expf(-gv[k].y));
-                        y2 = y2 / (1.f + expf(-gv[k].z));
-                        y3 = y3 / (1.f + expf(-gv[k].w));
-                    }
-                    const size_t go = ((size_t)(pl.r0 + i) * a.nh + pl.h) * dv + 4 * c4;
-                    *(float4 *)(a.out + go) = make_float4(y0, y1, y2, y3);
-                }
+            for (int idx = tid; idx < n4; idx += TC_BM) {
+                const int i = idx / dv4, c4 = idx % dv4;
+                *(float4 *)(a.out + ((size_t)(pl.r0 + i) * a.nh + pl.h) * dv + 4 * c4) =
+                    *(const float4 *)(so + i * ostride + 4 * c4);
             }
         }
     }
@@ -666,10 +646,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 }
 
 size_t tc_smem(int d, int *nslot) {
-    const size_t fixed = 1024 + (size_t)(d / 64) * 16384 + 2048;   // alignment slack, Q_hi, barriers + row factors
+    // alignment slack, Q_hi and Q_lo, barriers + row factors
+    const size_t fixed = 1024 + 2 * (size_t)(d / 64) * 16384 + 2048;
     const size_t limit = 227 * 1024;
     int ns = (int)((limit - fixed) / TC_SLOT);
-    if (ns > 6) ns = 6;
+    if (ns > 8) ns = 8;
     *nslot = ns;
     return fixed + (size_t)ns * TC_SLOT;
 }
@@ -693,6 +674,7 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
     CUtensorMap mk, mv;
     if (!make_map(&mk, a.Xk, (uint64_t)a.d, (uint64_t)a.G * NXp, 64, TC_BN)) return cudaErrorInvalidValue;
     if (!make_map(&mv, a.XvT, (uint64_t)NXp, (uint64_t)a.G * a.dv, 64, (uint32_t)a.dv)) return cudaErrorInvalidValue;
+    if (nslot < 3) return cudaErrorInvalidValue;   // a value half-tile needs two slots, plus one in flight
     k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh), TC_THREADS, smem, st>>>(a, mk, mv, NXp, nslot);
     return cudaPeekAtLastError();
 }

@@ -89,6 +89,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.cap = S.cap;
     a.Xk = (unsigned short *)(b + S.Xk);
     a.XvT = (unsigned short *)(b + S.XvT);
+    a.Qs = (unsigned short *)(b + S.Qs);
     a.nxp = S.nxp;
     a.tc = S.nxp > 0;
 }

@@ -33,6 +33,7 @@
 // r >= j0 = wg - len0 (o1b_far_e: "ring logical index j - j0"). That indexing
 // also covers a pass whose rows evict keys pushed earlier in the same pass
 // (window shorter than a block), which the pages' sub-chunking excludes.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "o1_common.cuh"
@@ -62,8 +63,19 @@ __global__ void k_rope(O1Args a) {
             for (int u = 0; u < 8; ++u) {
                 if (h0 + u >= a.nh) break;
                 const size_t o = ((size_t)r * a.nh + h0 + u) * a.d;
-                a.qr[o + j] = x0[u] * c - x1[u] * s;
-                a.qr[o + j + half] = x1[u] * c + x0[u] * s;
+                const float y0 = x0[u] * c - x1[u] * s, y1 = x1[u] * c + x0[u] * s;
+                a.qr[o + j] = y0;
+                a.qr[o + j + half] = y1;
+                if (a.tc) {
+                    // fp16 hi / lo of the rotated query for the tensor-core window path
+                    const size_t lo_off = (size_t)a.R * a.nh * a.d;
+                    const __half h0v = __float2half_rn(y0), h1v = __float2half_rn(y1);
+                    a.Qs[o + j] = __half_as_ushort(h0v);
+                    a.Qs[o + j + half] = __half_as_ushort(h1v);
+                    a.Qs[lo_off + o + j] = __half_as_ushort(__float2half_rn(y0 - __half2float(h0v)));
+                    a.Qs[lo_off + o + j + half] = __half_as_ushort(__float2half_rn(y1 - __half2float(h1v)));
+                    if (!(fabsf(y0) < 65504.f && fabsf(y1) < 65504.f)) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_FP16_RANGE);
+                }
             }
         }
         for (int g = 0; g < a.G; ++g) {
@@ -314,6 +326,11 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
     const int m = a.m, d = a.d, dv = a.dv, nh = a.nh, ns = a.ns;
     const bool far_any = mt.farl0 + max(0, r0 + nr - j0) > 0;
+    // the gate rows this block merges with at the end: into L2 now
+    if (a.gate && tid < nr)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)(a.gate + ((size_t)(r0 + tid) * nh + gh) * dv)),
+                     "r"((uint32_t)dv * 4u)
+                     : "memory");
     size_t off[6];
     side_layout(a, off);
     const int nbt = (m + ns + 63) / 64;

@@ -73,10 +73,11 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //                         kernel: (reference c_w, mass l, true max, -), the
 //                         window numerator being in `out` relative to c_w
 // and, when the tensor-core window path serves the geometry, the window key
-// sequence as fp16 hi / lo panels (nxp keys per group, zero past the end):
-//   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]
+// sequence as fp16 hi / lo panels (nxp keys per group, zero past the end)
+// and the rotated queries as fp16 hi / lo:
+//   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]    Qs [2][cap][nh][d]
 struct O1Scratch {
-    size_t qr, kr, E, P, Mc, Rc, Tp, fh, Xk, XvT, total;
+    size_t qr, kr, E, P, Mc, Rc, Tp, fh, Xk, XvT, Qs, total;
     int cap, nsub, nxp;
 };
 
@@ -112,6 +113,7 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     const size_t nx = (size_t)S.nxp;
     S.Xk = off;  off += o1_al256(2 * G * nx * d * 2);
     S.XvT = off; off += o1_al256(2 * G * dv * nx * 2);
+    S.Qs = off;  off += o1_al256(S.nxp ? 2 * c * nh * d * 2 : 0);
     S.total = off;
     return S;
 }
@@ -119,9 +121,8 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
 // Scratch of the one-row path: near partials per (group, key slice, head)
 // = (max, sum, value sum [dv]); the far part per head = (c_f, D, have, -,
 // numerator [dv]); the row's rotated key per group. KC keys per slice, NC
-// slices per group, sized for the longest near set (sinks + window) so that
-// about two blocks per SM share the key reads, and capped so that a slice
-// fits in shared memory.
+// slices per group, sized for the longest near set (sinks + window), about
+// 64 per group, and capped so that a slice fits in shared memory.
 struct O1TokScratch {
     size_t part, farp, kcur, total;
     int KC, NC;
@@ -130,11 +131,14 @@ struct O1TokScratch {
 static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, dv = g.dv, d = g.d;
     const long long nmax = (long long)g.sinks + g.window;
-    long long kc = (G * nmax + 303) / 304;
+    // about 64 slices per group: one wave of blocks on the GPU for a couple
+    // of groups, few partials for the merge
+    long long kc = (nmax + 63) / 64;
     kc = kc < 8 ? 8 : (kc + 7) / 8 * 8;
     // a slice's keys, values and scores stay within 227 KB of shared memory
-    const long long kmax = ((227 * 1024 / 4) - (long long)(g.heads_per_group + 1) * g.d - 2 * g.heads_per_group) /
-                           ((long long)g.d + g.dv + g.heads_per_group) / 8 * 8;
+    // (rows padded by 4 floats)
+    const long long kmax = ((227 * 1024 / 4) - (long long)(g.heads_per_group + 1) * (g.d + 4) - 2 * g.heads_per_group) /
+                           ((long long)g.d + 4 + g.dv + g.heads_per_group) / 8 * 8;
     if (kc > kmax) kc = kmax;
     O1TokScratch S;
     S.KC = (int)kc;
@@ -173,7 +177,7 @@ struct O1Args {
     float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh;
     int cap;
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
-    unsigned short *Xk, *XvT;
+    unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;
     // one-row path scratch
     float *part, *farp, *kcur;

@@ -100,6 +100,13 @@ __device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x,
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
+            su32(dst)),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(su32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -269,19 +276,20 @@ __global__ __launch_bounds__(256) void k_gather_tc(O1Args a, unsigned short *Xk,
 // (dv rows x 128 B). Per tile j the ring carries K(j) chunks 0..nkc-1, later
 // V(j) as hi(keys 0-63), lo(0-63), hi(64-127), lo(64-127).
 __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __grid_constant__ CUtensorMap mk,
-                                                            const __grid_constant__ CUtensorMap mv, int NXp, int nslot) {
+                                                            const __grid_constant__ CUtensorMap mv,
+                                                            const __grid_constant__ CUtensorMap mq, int NXp, int nslot) {
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     const TcPlan pl = tc_plan(a);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = a.d, dv = a.dv;
+    const int dv = a.dv;
     unsigned char *sQh = sm;                                 // nkc x 16 KB
     unsigned char *sQl = sQh + (size_t)pl.nkc * 16384;       // nkc x 16 KB
     unsigned char *sR = sQl + (size_t)pl.nkc * 16384;        // nslot x 32 KB
     uint64_t *bars = (uint64_t *)(sR + (size_t)nslot * TC_SLOT);
     uint64_t *full = bars, *empty = bars + nslot;
     uint64_t *s_full = bars + 2 * nslot, *p_full = s_full + 2, *pv_done = p_full + 2, *o_done = pv_done + 1,
-             *q_ready = o_done + 1;
+             *q_ready = o_done + 1;   // the Q tile's TMA
     uint32_t *tslot = (uint32_t *)(q_ready + 1);
     volatile int *abort = (volatile int *)(tslot + 1);
 
@@ -296,7 +304,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         mbar_init(&p_full[1], TC_BM);
         mbar_init(pv_done, 1);
         mbar_init(o_done, 1);
-        mbar_init(q_ready, TC_BM);
+        mbar_init(q_ready, 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -314,6 +322,12 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         // ---------------------------------------------------- TMA producer
         // (starts at once: the Q tile has its own smem)
         if (lane == 0) {
+            // the Q tile, fp16 hi and lo, straight into its swizzled slots
+            // (rows past R read as zeros)
+            mbar_expect_tx(q_ready, 2 * pl.nkc * 16384);
+            for (int hl = 0; hl < 2; ++hl)
+                for (int c = 0; c < pl.nkc; ++c)
+                    tma_4d((hl ? sQl : sQh) + (size_t)c * 16384, &mq, 64 * c, pl.h, pl.r0, hl, q_ready);
             int it = 0;
             const int ybase = pl.g * NXp;
             auto next = [&](uint32_t bytes) -> int {
@@ -426,41 +440,6 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         const bool valid = row < pl.nr;
         const int lo = max(0, pl.mt.len0 + r + 1 - pl.mt.wg), hi = pl.mt.len0 + r;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        // Q tile -> smem as fp16 hi and lo (128-byte swizzle: 16-byte unit u
-        // of row i stored at unit u ^ (i & 7))
-        {
-            const int d4 = d >> 2;
-            bool q_ok = true;
-            for (int base = tid; base < TC_BM * d4; base += 16 * TC_BM) {
-                float4 vv[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int idx = base + k * TC_BM, i = idx / d4, u4 = idx % d4;
-                    vv[k] = (idx < TC_BM * d4 && i < pl.nr)
-                                ? ((const float4 *)(a.qr + ((size_t)(pl.r0 + i) * a.nh + pl.h) * d))[u4]
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int idx = base + k * TC_BM;
-                    if (idx >= TC_BM * d4) break;
-                    const int i = idx / d4, u4 = idx % d4;
-                    uint32_t h01, l01, h23, l23;
-                    q_ok &= fmaxf(fmaxf(fabsf(vv[k].x), fabsf(vv[k].y)), fmaxf(fabsf(vv[k].z), fabsf(vv[k].w))) <
-                            65504.f;
-                    split_pair(vv[k].x, vv[k].y, h01, l01);
-                    split_pair(vv[k].z, vv[k].w, h23, l23);
-                    const int e = 4 * u4, ch = e >> 6, u = (e & 63) >> 3, half8 = (e & 7) * 2;
-                    const size_t off = (size_t)ch * 16384 + i * 128 + ((u ^ (i & 7)) << 4) + half8;
-                    *(uint2 *)(sQh + off) = make_uint2(h01, h23);
-                    *(uint2 *)(sQl + off) = make_uint2(l01, l23);
-                }
-            }
-            if (!q_ok) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_FP16_RANGE);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(q_ready);
-        }
-
         const float sc2 = a.scale * 1.4426950408889634f;   // scores in log2 units
         float mref = -INFINITY, mtrue = -INFINITY, l = 0.f;
         bool ok = true;
@@ -675,6 +654,20 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
     if (!make_map(&mk, a.Xk, (uint64_t)a.d, (uint64_t)a.G * NXp, 64, TC_BN)) return cudaErrorInvalidValue;
     if (!make_map(&mv, a.XvT, (uint64_t)NXp, (uint64_t)a.G * a.dv, 64, (uint32_t)a.dv)) return cudaErrorInvalidValue;
     if (nslot < 3) return cudaErrorInvalidValue;   // a value half-tile needs two slots, plus one in flight
-    k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh), TC_THREADS, smem, st>>>(a, mk, mv, NXp, nslot);
+    CUtensorMap mq;
+    {
+        // Qs [2][R][nh][d] fp16, boxes of 64 x 1 head x 128 rows
+        auto enc = tensor_map_encoder();
+        if (!enc) return cudaErrorInvalidValue;
+        cuuint64_t dims[4] = {(cuuint64_t)a.d, (cuuint64_t)a.nh, (cuuint64_t)a.R, 2};
+        cuuint64_t strides[3] = {(cuuint64_t)a.d * 2, (cuuint64_t)a.nh * a.d * 2, (cuuint64_t)a.R * a.nh * a.d * 2};
+        cuuint32_t box[4] = {64, 1, TC_BM, 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, (void *)a.Qs, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh), TC_THREADS, smem, st>>>(a, mk, mv, mq, NXp, nslot);
     return cudaPeekAtLastError();
 }

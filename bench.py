@@ -272,7 +272,7 @@ def our_arm(args, rank, world, local_rank):
 
     nst = o1.O1_NUM_STAGES
     total_steps = args.warmup + args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(total_steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(total_steps)]
     for row in evs:
         for e in row:
             e.record(stream)   # create the CUDA events before they are handed to the library
@@ -303,7 +303,7 @@ def our_arm(args, rank, world, local_rank):
         torch.cuda.synchronize()
     barrier()
     ms = t_start.elapsed_time(t_end)
-    stage_ms = [[evs[args.warmup + i][j].elapsed_time(evs[args.warmup + i][j + 1]) for j in range(nst)]
+    stage_ms = [[evs[args.warmup + i][2 * j].elapsed_time(evs[args.warmup + i][2 * j + 1]) for j in range(nst)]
                 for i in range(args.steps)]
     stage_avg = np.mean(np.array(stage_ms), axis=0)
     ms_max = ms

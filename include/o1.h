@@ -148,19 +148,26 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
                     const float *q, const float *k, const float *v, const float *gate,
                     float *out, void *stream);
 
-/* Stages of one chunk pass, in launch order; o1_chunk_attend_timed records
- * an event before each and one after the last. A stage that does not apply
- * to the geometry (the fp16 panel gather of the tensor-core window path)
- * launches nothing and times as empty. */
-#define O1_NUM_STAGES 9
+/* Stages of one chunk pass, in launch order: rope, far_logits, far_scan,
+ * far_dT, far_tscan, side_readout, gather_tc, near, merge, commit. The
+ * far-field stages (far_logits .. side_readout) run on a second stream of the
+ * library's, concurrently with gather_tc and near; it is forked from and
+ * joined back into the caller's stream by events, so a stream capture of a
+ * call captures both branches. The stream and its two events are created by
+ * the first call on each host thread and device (make that call before a
+ * stream capture) and live until the process exits. A stage that does not apply to the geometry
+ * (the fp16 panel gather outside the tensor-core window path) launches
+ * nothing and times as empty. */
+#define O1_NUM_STAGES 10
 
 /* o1_chunk_attend that also records caller-created CUDA events (cudaEvent_t
- * handles, passed as void*) on `stream`: events[i] just before stage i of a
- * pass and events[O1_NUM_STAGES] after its last stage, so that
- * cudaEventElapsedTime(events[i], events[i + 1]) is stage i's time. With
- * several passes (rows above the scratch's capacity) the events end up
- * holding the last pass. n_events must be at least O1_NUM_STAGES + 1.
- * Same arguments, checks and result as o1_chunk_attend otherwise. */
+ * handles, passed as void*): events[2i] just before and events[2i + 1] just
+ * after stage i of a pass, on the stream that stage runs on, so that
+ * cudaEventElapsedTime(events[2i], events[2i + 1]) is stage i's time (with
+ * the other branch running concurrently). With several passes (rows above
+ * the scratch's capacity) the events end up holding the last pass. n_events
+ * must be at least 2 * O1_NUM_STAGES. Same arguments, checks and result as
+ * o1_chunk_attend otherwise. */
 O1_API int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                                  const float *q, const float *k, const float *v, const float *gate,
                                  int32_t rows, float *out, void *const *events, int32_t n_events,

@@ -86,6 +86,8 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.Rc = (float *)(b + S.Rc);
     a.Tp = (float *)(b + S.Tp);
     a.fh = (float *)(b + S.fh);
+    a.sh = (float *)(b + S.sh);
+    a.sn = (float *)(b + S.sn);
     a.cap = S.cap;
     a.Xk = (unsigned short *)(b + S.Xk);
     a.XvT = (unsigned short *)(b + S.XvT);
@@ -257,8 +259,8 @@ int o1_chunk_attend(void *state, const o1_geom *geom, void *scratch, size_t scra
 int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                           const float *q, const float *k, const float *v, const float *gate, int32_t rows,
                           float *out, void *const *events, int32_t n_events, void *stream) {
-    if (!events || n_events < O1_NUM_STAGES + 1) return O1_ERR_ARG;
-    for (int i = 0; i <= O1_NUM_STAGES; ++i)
+    if (!events || n_events < 2 * O1_NUM_STAGES) return O1_ERR_ARG;
+    for (int i = 0; i < 2 * O1_NUM_STAGES; ++i)
         if (!events[i]) return O1_ERR_ARG;
     return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream,
                  (cudaEvent_t const *)events);

@@ -22,11 +22,13 @@
 //                    exponent (o1b_attend's sink and far parts)
 //  7. k_gather_tc    (tensor-core geometries) the window key sequence as
 //                    fp16 hi / lo panels (o1_near_tc.cu)
-//  8. k_near_tc      the sliding window on the tensor cores, merged with the
-//     or k_near      side part under one exponent, gate (o1b_attend's window
-//                    part and normalisation; dory_gate1); k_near is the fp32
-//                    version for the other geometries
-//  9. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
+//  8. k_near_tc      the sliding window on the tensor cores (o1b_attend's
+//     or k_near      window part); k_near is the fp32 version for the other
+//                    geometries
+//  9. k_merge        window and side parts under one exponent, the 1e-30
+//                    floor, the gate (o1b_attend's normalisation; dory_gate1)
+// 10. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
+// Stages 2-6 and 7-8 share no data; they run on two streams.
 //
 // Keys are indexed in X = [ring, oldest first] ++ [this pass's rows]: row r
 // sees X[max(0, len0 + r + 1 - wg) .. len0 + r] and evicts X[r - j0] once
@@ -274,10 +276,8 @@ __global__ void k_far_tscan(O1Args a) {
 //   far numerator = sum_b gain_b (R_c T_{c-1})_b + sum_{evicting j <= row} cf_j v_ev(j),
 //   cf_j = sum_b gain_b E_bj;
 //   sinks: p_x = e^{scale q'.sink_x - c_s}.
-// Then the merge with the row's window part, which the window kernel left
-// in `out` (numerator) and in the row's window header (reference, mass,
-// true max): one exponent for all three parts, the 1e-30 floor, the gate.
-// c_s = -inf marks a row with no sinks and no far field.
+// The side numerator goes to the side buffer sn and (c_s, side mass) to the
+// row's side header; c_s = -inf marks a row with no sinks and no far field.
 //
 // Layout (256 threads, 8 warps). The products are register-tiled with
 // float4 shared-memory reads:
@@ -299,8 +299,8 @@ __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
     off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks
     off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
     off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
-    off[4] = off[3] + 64 * 65;                               // F, M_c, c_s, side mass, merge factors [64] each
-    off[5] = off[4] + 6 * 64;                                // total (floats)
+    off[4] = off[3] + 64 * 65;                               // F, M_c [64] each
+    off[5] = off[4] + 2 * 64;                                // total (floats)
 }
 
 __device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
@@ -326,11 +326,6 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
     const int m = a.m, d = a.d, dv = a.dv, nh = a.nh, ns = a.ns;
     const bool far_any = mt.farl0 + max(0, r0 + nr - j0) > 0;
-    // the gate rows this block merges with at the end: into L2 now
-    if (a.gate && tid < nr)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)(a.gate + ((size_t)(r0 + tid) * nh + gh) * dv)),
-                     "r"((uint32_t)dv * 4u)
-                     : "memory");
     size_t off[6];
     side_layout(a, off);
     const int nbt = (m + ns + 63) / 64;
@@ -342,7 +337,6 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     float *sR3 = sm + off[3];
     float *sRow = sm + off[4];
     float *sMc = sRow + 64;
-    float *sCs = sMc + 64, *sSm = sCs + 64, *sFa = sSm + 64, *sFb = sFa + 64;
 
     // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks
     {
@@ -473,31 +467,10 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         if (lane + 32 < m) sA6[(lane + 32) * SR_LDA + i] = g1 * fs;
         if (lane < ns) sA6[(m + 64 + lane) * SR_LDA + i] = w0;
         if (lane + 32 < ns) sA6[(m + 64 + lane + 32) * SR_LDA + i] = w1;
-        if (lane == 0) {
-            sCs[i] = cs;
-            sSm[i] = cs > -INFINITY ? side : 0.f;
-        }
+        if (i < nr && lane == 0)
+            *(float4 *)(a.sh + ((size_t)r * nh + gh) * 4) = make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    // merge factors with the window part of each row (its header from the
-    // window kernel): c = max(window max, c_s) (the pages' c_all), the
-    // denominator floored at 1e-30 in those units
-    if (tid < 64) {
-        float fa = 0.f, fb = 0.f;
-        if (tid < nr) {
-            const float4 wh = *(const float4 *)(a.fh + ((size_t)(r0 + tid) * nh + gh) * 4);
-            const float cs = sCs[tid];
-            const float cc = fmaxf(wh.z, cs);
-            const float al = expf(wh.x - cc);
-            const float be = cs > -INFINITY ? expf(cs - cc) : 0.f;
-            const float den = fmaxf(al * wh.y + be * sSm[tid], 1e-30f);
-            fa = al / den;
-            fb = be / den;
-        }
-        sFa[tid] = fa;
-        sFb[tid] = fb;
-    }
-
     // 5. in-block far coefficients, causal: W[row][jj] = sum_b gain_b(row) E_b(jj)
     //    for jj <= row, into A6 rows m + jj
     if (far_any) {
@@ -573,35 +546,21 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         }
         __syncthreads();
     }
-    // 7. out = fa * (window numerator, already in out) + fb * side numerator,
-    //    then the gate (dory_gate1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = 8 * warp + i;
         if (row >= nr) continue;
-        const float fa = sFa[row], fb = sFb[row];
-        const size_t ro = ((size_t)(r0 + row) * nh + gh) * dv;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int col = 4 * lane + 128 * v;
-            if (col < dv) {
-                const float4 ow = *(const float4 *)(a.out + ro + col);
-                float y0 = fa * ow.x + fb * acc6[i][v][0], y1 = fa * ow.y + fb * acc6[i][v][1];
-                float y2 = fa * ow.z + fb * acc6[i][v][2], y3 = fa * ow.w + fb * acc6[i][v][3];
-                if (a.gate) {
-                    const float4 gv = *(const float4 *)(a.gate + ro + col);
-                    y0 = y0 / (1.f + expf(-gv.x));
-                    y1 = y1 / (1.f + expf(-gv.y));
-                    y2 = y2 / (1.f + expf(-gv.z));
-                    y3 = y3 / (1.f + expf(-gv.w));
-                }
-                *(float4 *)(a.out + ro + col) = make_float4(y0, y1, y2, y3);
-            }
+            if (col < dv)
+                *(float4 *)(a.sn + ((size_t)(r0 + row) * nh + gh) * dv + col) =
+                    make_float4(acc6[i][v][0], acc6[i][v][1], acc6[i][v][2], acc6[i][v][3]);
         }
     }
 }
 
-// ----------------------------------------------------------- near + merge
+// ------------------------------------------------------------------ near
 
 // Block = (rows, group): 32 query slots = floor(32 / hpg) rows x hpg heads,
 // so one staged key/value tile serves every head of the group. 8 warps, 4
@@ -752,6 +711,50 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
     }
 }
 
+// ----------------------------------------------------------------- merge
+
+// One warp per (row, head): the window part (numerator in `out` relative to
+// the reference c_w; header (c_w, mass, true max)) and the side part
+// (numerator in sn relative to c_s; header (c_s, mass)) under one exponent
+// c = max(true window max, c_s) — the pages' c_all — the denominator floored
+// at 1e-30 in those units (o1b_attend), then the gate (dory_gate1).
+__global__ __launch_bounds__(256) void k_merge(O1Args a) {
+    const int lane = threadIdx.x & 31;
+    const size_t rh = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (rh >= (size_t)a.R * a.nh) return;
+    const float4 wh = *(const float4 *)(a.fh + rh * 4), sh = *(const float4 *)(a.sh + rh * 4);
+    const float cc = fmaxf(wh.z, sh.x);
+    const float al = expf(wh.x - cc);
+    const float be = sh.x > -INFINITY ? expf(sh.x - cc) : 0.f;
+    const float den = fmaxf(al * wh.y + be * sh.y, 1e-30f);
+    const float fa = al / den, fb = be / den;
+    const int dv4 = a.dv >> 2;
+    float4 ow[2], sw[2], gv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c4 = lane + 32 * u;
+        if (c4 < dv4) {
+            ow[u] = ((const float4 *)(a.out + rh * a.dv))[c4];
+            sw[u] = ((const float4 *)(a.sn + rh * a.dv))[c4];
+            gv[u] = a.gate ? ((const float4 *)(a.gate + rh * a.dv))[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c4 = lane + 32 * u;
+        if (c4 >= dv4) continue;
+        float y0 = fa * ow[u].x + fb * sw[u].x, y1 = fa * ow[u].y + fb * sw[u].y;
+        float y2 = fa * ow[u].z + fb * sw[u].z, y3 = fa * ow[u].w + fb * sw[u].w;
+        if (a.gate) {
+            y0 = y0 / (1.f + expf(-gv[u].x));
+            y1 = y1 / (1.f + expf(-gv[u].y));
+            y2 = y2 / (1.f + expf(-gv[u].z));
+            y3 = y3 / (1.f + expf(-gv[u].w));
+        }
+        ((float4 *)(a.out + rh * a.dv))[c4] = make_float4(y0, y1, y2, y3);
+    }
+}
+
 // --------------------------------------------------------------- commit
 
 // The pass's rotated keys and values into the ring (o1b_ring_commit: row j
@@ -815,7 +818,7 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a) {
 // ------------------------------------------------------------- launchers
 
 extern const char *const o1_stage_names[O1_NUM_STAGES] = {
-    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "gather_tc", "near", "side_readout", "commit"};
+    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near", "merge", "commit"};
 
 static size_t readout_smem(const O1Args &a) {
     size_t off[6];
@@ -825,6 +828,42 @@ static size_t readout_smem(const O1Args &a) {
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
+namespace {
+
+// A second stream and two events per host thread and device: the far-field
+// chain and the window run concurrently after the rotation (they share no
+// data), joined before the merge. Fork and join are event record / wait
+// pairs, so a capture of the caller's stream captures both branches.
+struct O1Aux {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t o1_aux(O1Aux **out) {
+    static thread_local O1Aux aux[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    O1Aux &x = aux[dev];
+    if (!x.st) {
+        // the far branch is the longer one: its blocks go first when SMs free up
+        int lo = 0, hi = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithPriority(&x.st, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &x;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// Stages: rope | far_logits, far_scan, far_dT, far_tscan, side_readout |
+// gather_tc, near | merge, commit. The two middle branches run concurrently,
+// the far one on the library's second stream. With `ev`, events 2i and 2i + 1
+// are recorded just before and just after stage i on the stream it runs on.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
     static bool attrs_set = false;
     if (!attrs_set) {
@@ -836,43 +875,65 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     }
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
-    int stage = 0;
-    auto mark = [&]() {
-        if (ev) cudaEventRecord(ev[stage], st);
-        ++stage;
+    auto begin = [&](int i, cudaStream_t s) {
+        if (ev) cudaEventRecord(ev[2 * i], s);
     };
-    mark();
+    auto end = [&](int i, cudaStream_t s) {
+        if (ev) cudaEventRecord(ev[2 * i + 1], s);
+    };
+    O1Aux *aux = nullptr;
+    cudaError_t e = o1_aux(&aux);
+    if (e != cudaSuccess) return e;
+    const cudaStream_t sf = aux->st;   // the far-field branch
+    begin(0, st);
     k_rope<<<R, 128, 0, st>>>(a);
-    mark();
-    k_far_logits<<<dim3(nblk, a.nh), 256, 0, st>>>(a);
-    mark();
-    k_far_scan<<<(a.nh * a.m * 32 + 255) / 256, 256, 0, st>>>(a);
-    mark();
-    k_far_dT<<<dim3(nblk, a.nh, (a.dv + 63) / 64), 256, 0, st>>>(a);
-    mark();
+    end(0, st);
+    cudaEventRecord(aux->fork, st);
+    cudaStreamWaitEvent(sf, aux->fork, 0);
+    begin(1, sf);
+    k_far_logits<<<dim3(nblk, a.nh), 256, 0, sf>>>(a);
+    end(1, sf);
+    begin(2, sf);
+    k_far_scan<<<(a.nh * a.m * 32 + 255) / 256, 256, 0, sf>>>(a);
+    end(2, sf);
+    begin(3, sf);
+    k_far_dT<<<dim3(nblk, a.nh, (a.dv + 63) / 64), 256, 0, sf>>>(a);
+    end(3, sf);
+    begin(4, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
-    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
-    mark();
-    if (a.tc) {
-        cudaError_t e = o1_launch_gather_tc(a, st);
-        if (e != cudaSuccess) return e;
-        mark();
-        e = o1_launch_near_tc(a, st);
-        if (e != cudaSuccess) return e;
-    } else {
-        mark();   // no panels to gather
-        const int RB = 32 / a.hpg;
-        const dim3 gn((R + RB - 1) / RB, a.G);
-        if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
-        else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
+    end(4, sf);
+    begin(5, sf);
+    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+    end(5, sf);
+    cudaEventRecord(aux->join, sf);
+    begin(6, st);
+    if (a.tc) e = o1_launch_gather_tc(a, st);
+    end(6, st);
+    begin(7, st);
+    if (e == cudaSuccess) {
+        if (a.tc) {
+            e = o1_launch_near_tc(a, st);
+        } else {
+            const int RB = 32 / a.hpg;
+            const dim3 gn((R + RB - 1) / RB, a.G);
+            if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
+            else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+        }
     }
-    mark();
-    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
-    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), st>>>(a);
-    mark();
+    end(7, st);
+    // the far branch is joined even when the window launch failed, so that a
+    // capture of `st` stays well formed
+    cudaStreamWaitEvent(st, aux->join, 0);
+    if (e != cudaSuccess) return e;
+    begin(8, st);
+    k_merge<<<(unsigned)(((size_t)R * a.nh + 7) / 8), 256, 0, st>>>(a);
+    end(8, st);
+    begin(9, st);
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
-    mark();
+    end(9, st);
     return cudaPeekAtLastError();
 }
 

@@ -72,12 +72,14 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   fh [cap][nh] x 4      per row-head window header, written by the window
 //                         kernel: (reference c_w, mass l, true max, -), the
 //                         window numerator being in `out` relative to c_w
+//   sh [cap][nh] x 4      per row-head side header (c_s, side mass, -, -)
+//   sn [cap][nh][dv]      side numerator (sinks + far field), relative to c_s
 // and, when the tensor-core window path serves the geometry, the window key
 // sequence as fp16 hi / lo panels (nxp keys per group, zero past the end)
 // and the rotated queries as fp16 hi / lo:
 //   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]    Qs [2][cap][nh][d]
 struct O1Scratch {
-    size_t qr, kr, E, P, Mc, Rc, Tp, fh, Xk, XvT, Qs, total;
+    size_t qr, kr, E, P, Mc, Rc, Tp, fh, sh, sn, Xk, XvT, Qs, total;
     int cap, nsub, nxp;
 };
 
@@ -109,6 +111,8 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     S.Rc = off; off += o1_al256(nh * m * ns * 4);
     S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
     S.fh = off; off += o1_al256(c * nh * 4 * 4);
+    S.sh = off; off += o1_al256(c * nh * 4 * 4);
+    S.sn = off; off += o1_al256(c * nh * dv * 4);
     S.nxp = o1_tc_supported(g) ? o1_tc_nxp(g, cap) : 0;
     const size_t nx = (size_t)S.nxp;
     S.Xk = off;  off += o1_al256(2 * G * nx * d * 2);
@@ -174,7 +178,7 @@ struct O1Args {
     float *out;
     int R, nsub;
     // scratch
-    float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh;
+    float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh, *sh, *sn;
     int cap;
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
     unsigned short *Xk, *XvT, *Qs;

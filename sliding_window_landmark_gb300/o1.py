@@ -161,7 +161,7 @@ def o1_chunk_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, s
         _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
 
 
-O1_NUM_STAGES = 9
+O1_NUM_STAGES = 10
 
 
 def o1_stage_name(stage: int):
@@ -170,8 +170,9 @@ def o1_stage_name(stage: int):
 
 
 def o1_chunk_attend_timed(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, events, stream=None) -> int:
-    """``events``: O1_NUM_STAGES + 1 torch.cuda.Event(enable_timing=True), each
-    already recorded once (so that its CUDA handle exists)."""
+    """``events``: 2 * O1_NUM_STAGES torch.cuda.Event(enable_timing=True),
+    each already recorded once (so that its CUDA handle exists); stage i's
+    time is events[2i].elapsed_time(events[2i + 1])."""
     nh, G = g.nh, g.groups
     arr = (_VP * len(events))(*[_VP(int(e.cuda_event)) for e in events])
     return LIB.o1_chunk_attend_timed(

@@ -239,3 +239,52 @@ def test_stack_layer_prompt(layer):
         stats.append(harness.assert_outputs(gpu.rows(q, k, v, g), want, diag, f"layer {layer} rows {r0}"))
     harness.assert_state(gpu.read(), orc, f"layer {layer}")
     print(f"stack layer {layer}:", stats)
+
+
+def test_timed_stages_and_stream_capture():
+    """The timed variant records a begin/end pair per stage (on the stage's
+    own stream); a CUDA-graph capture of o1_chunk_attend (whose far-field
+    branch runs on the library's second stream) replays to the oracle's
+    result."""
+    import torch
+    from sliding_window_landmark_gb300 import o1
+    sh = synth.Shape(groups=1, heads_per_group=2, d=64, dv=64, sinks=2, window=512, landmarks=4)
+    c = synth.layer_constants(sh, 9)
+    q, k, v, g = synth.layer_rows(sh, 9, 0, 300)
+    want, diag = harness.oracle_layer(sh, c).rows(q, k, v, g, diag=True)
+
+    gpu = harness.GpuLayer(sh, c, max_rows=300)
+    names = [o1.o1_stage_name(i) for i in range(o1.O1_NUM_STAGES)]
+    assert names == ["rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near",
+                     "merge", "commit"]
+    assert o1.o1_stage_name(o1.O1_NUM_STAGES) is None
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * o1.O1_NUM_STAGES)]
+    for e in evs:
+        e.record()
+    out = torch.empty((300, sh.nh, sh.dv), dtype=torch.float32, device="cuda")
+    dq, dk, dvv, dg = gpu.up(q), gpu.up(k), gpu.up(v), gpu.up(g)
+    o1.check(o1.o1_chunk_attend_timed(gpu.state, gpu.g, gpu.scratch, dq, dk, dvv, dg, 300, out, evs), "timed")
+    torch.cuda.synchronize()
+    times = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(o1.O1_NUM_STAGES)]
+    assert all(np.isfinite(t) and t >= 0 for t in times), times
+    harness.assert_outputs(out.cpu().numpy(), want, diag, "timed")
+    assert o1.o1_status_string(o1.LIB.o1_chunk_attend_timed(
+        o1._VP(gpu.state.data_ptr()), o1.ctypes.byref(gpu.g), o1._VP(gpu.scratch.data_ptr()), gpu.scratch.numel(),
+        o1._VP(dq.data_ptr()), o1._VP(dk.data_ptr()), o1._VP(dvv.data_ptr()), None, 300, o1._VP(out.data_ptr()),
+        (o1._VP * 3)(), 3, None)) == o1.o1_status_string(o1.O1_ERR_ARG)
+
+    cap = harness.GpuLayer(sh, c, max_rows=300)
+    out2 = torch.empty((300, sh.nh, sh.dv), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            o1.check(o1.o1_chunk_attend(cap.state, cap.g, cap.scratch, dq, dk, dvv, dg, 300, out2), "capture")
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    harness.assert_outputs(out2.cpu().numpy(), want, diag, "graph replay")
+    orc = harness.oracle_layer(sh, c)
+    orc.rows(q, k, v, g)
+    harness.assert_state(cap.read(), orc, "graph replay state")

@@ -148,9 +148,9 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
                     const float *q, const float *k, const float *v, const float *gate,
                     float *out, void *stream);
 
-/* Stages of one chunk pass, in launch order: rope, far_logits, far_scan,
- * far_dT, far_tscan, side_readout, gather_tc, near, merge, commit. The
- * far-field stages (far_logits .. side_readout) run on a second stream of the
+/* Stages of one chunk pass, in launch order: rope, far_block, far_tscan,
+ * side_readout, gather_tc, near, merge, commit. The far-field stages
+ * (far_block .. side_readout) run on a second, high-priority stream of the
  * library's, concurrently with gather_tc and near; it is forked from and
  * joined back into the caller's stream by events, so a stream capture of a
  * call captures both branches. The stream and its two events are created by
@@ -158,7 +158,7 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
  * stream capture) and live until the process exits. A stage that does not apply to the geometry
  * (the fp16 panel gather outside the tensor-core window path) launches
  * nothing and times as empty. */
-#define O1_NUM_STAGES 10
+#define O1_NUM_STAGES 8
 
 /* o1_chunk_attend that also records caller-created CUDA events (cudaEvent_t
  * handles, passed as void*): events[2i] just before and events[2i + 1] just

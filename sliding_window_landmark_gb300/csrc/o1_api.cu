@@ -82,8 +82,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.kr = (float *)(b + S.kr);
     a.E = (float *)(b + S.E);
     a.P = (float *)(b + S.P);
-    a.Mc = (float *)(b + S.Mc);
-    a.Rc = (float *)(b + S.Rc);
+    a.Fb = (float *)(b + S.Fb);
     a.Tp = (float *)(b + S.Tp);
     a.fh = (float *)(b + S.fh);
     a.sh = (float *)(b + S.sh);

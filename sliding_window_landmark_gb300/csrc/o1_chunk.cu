@@ -9,26 +9,26 @@
 // per-block partials compose associatively:
 //
 //  1. k_rope         rotate q and k of every row (dory.rs, dory_prep)
-//  2. k_far_logits   l = scale qt_b . k_e for every key the pass evicts
-//                    (o1b_far_e's dot, all blocks at once)
-//  3. k_far_scan     per (head, landmark): block max M_c, rescale R_c,
-//                    E = exp(l - M_c), far-mass prefix P per row (o1b_far_e's
-//                    max / rescale / prefix, as a scan over the blocks)
-//  4. k_far_dT       per block: sum_j E_bj v_ev(j)  (o1b_far_commit's sum)
-//  5. k_far_tscan    T entering each block, rescaled to its max
-//                    (o1b_far_commit's recurrence T <- R T + dT, as a scan)
-//  6. k_side_readout per row: the sinks and the far field (landmark scores,
+//  2. k_far_block    per 64-row block: l = scale qt_b . k_e for the keys the
+//                    block evicts, the block-local max, E = exp(l - max),
+//                    its prefix over rows and total, and the block's value
+//                    sum increment sum_j E_bj v_ev(j) (o1b_far_e's dot,
+//                    max and prefix; o1b_far_commit's sum; all blocks at once)
+//  3. k_far_tscan    the running far max M_c, rescale R_c, mass Z and value
+//                    sum T across the blocks (o1b_far_e's rescale and
+//                    o1b_far_commit's recurrence T <- R T + dT, as a scan)
+//  4. k_side_readout per row: the sinks and the far field (landmark scores,
 //                    u = e^{f-F} mu, gains, far mass and numerator) under one
 //                    exponent (o1b_attend's sink and far parts)
-//  7. k_gather_tc    (tensor-core geometries) the window key sequence as
+//  5. k_gather_tc    (tensor-core geometries) the window key sequence as
 //                    fp16 hi / lo panels (o1_near_tc.cu)
-//  8. k_near_tc      the sliding window on the tensor cores (o1b_attend's
+//  6. k_near_tc      the sliding window on the tensor cores (o1b_attend's
 //     or k_near      window part); k_near is the fp32 version for the other
 //                    geometries
-//  9. k_merge        window and side parts under one exponent, the 1e-30
+//  7. k_merge        window and side parts under one exponent, the 1e-30
 //                    floor, the gate (o1b_attend's normalisation; dory_gate1)
-// 10. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
-// Stages 2-6 and 7-8 share no data; they run on two streams.
+//  8. k_commit       ring rows and meta (o1b_ring_commit, o1b_meta)
+// Stages 2-4 and 5-6 share no data; they run on two streams.
 //
 // Keys are indexed in X = [ring, oldest first] ++ [this pass's rows]: row r
 // sees X[max(0, len0 + r + 1 - wg) .. len0 + r] and evicts X[r - j0] once
@@ -89,180 +89,259 @@ __global__ void k_rope(O1Args a) {
     }
 }
 
-// ------------------------------------------------------------- far field
-
-// Far logits of the evicted keys: E[gh][b][x] = scale qt[gh][b] . X[x] for
-// x < R - j0. Block = (64 evicted keys, head).
-__global__ __launch_bounds__(256) void k_far_logits(O1Args a) {
-    const int gh = blockIdx.y, g = gh / a.hpg;
-    const O1Meta mt = o1_meta(a, g);
-    const int j0 = mt.wg - mt.len0;
-    const int nev = a.R - j0;
-    const int x0 = blockIdx.x * 64;
-    if (x0 >= nev) return;
-    __shared__ float sA[64 * 33], sB[64 * 33];
-    float c[4][4];
-    blk_zero(c);
-    for (int kc = 0; kc < a.d; kc += 32) {
-        for (int idx = threadIdx.x; idx < 64 * 32; idx += 256) {
-            const int i = idx >> 5, kk = idx & 31;
-            const bool in = kc + kk < a.d;
-            sA[i * 33 + kk] = (i < a.m && in) ? a.qt[((size_t)gh * a.m + i) * a.d + kc + kk] : 0.f;
-            sB[i * 33 + kk] = (x0 + i < nev && in) ? o1_key(a, g, x0 + i, mt)[kc + kk] : 0.f;
-        }
-        __syncthreads();
-        blk_nt(c, sA, 33, sB, 33, 32);
-        __syncthreads();
-    }
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+// c[i][j] += a_i . b_j over four k (both operands k-contiguous float4s)
+__device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int b = ty + 16 * i, x = x0 + tx + 16 * j;
-            if (b < a.m && x < nev) a.E[((size_t)gh * a.m + b) * a.cap + x] = a.scale * c[i][j];
+            c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
+            c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
+            c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
+            c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
         }
 }
 
-// One warp per (head, landmark query b), sequential over the pass's blocks of
-// O1_SUB rows: the far max after each block M_c, the rescale R_c of what came
-// before (1 if the max did not move, so an empty field stays empty), E =
-// exp(l - M_c) in place of l, and for every row the far mass P = R_c Z +
-// (prefix of E within the block).
-__global__ __launch_bounds__(256) void k_far_scan(O1Args a) {
-    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= a.nh * a.m) return;
-    const int gh = wid / a.m, g = gh / a.hpg;
-    const O1Meta mt = o1_meta(a, g);
-    const int j0 = mt.wg - mt.len0;
-    float Mo = a.M[wid], Zo = a.Z[wid];
-    float *E = a.E + (size_t)wid * a.cap;
-    float *P = a.P + (size_t)wid * a.cap;
-    constexpr int NB = 4;   // blocks whose logits are loaded ahead of their stores
-    float lq[NB][2];
-    for (int c = 0; c < a.nsub; ++c) {
-        const int r0 = c * O1_SUB;
-        if (c % NB == 0) {
-#pragma unroll
-            for (int q = 0; q < NB; ++q)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int r = (c + q) * O1_SUB + hf * 32 + lane;
-                    lq[q][hf] = (r < a.R && r >= j0) ? E[r - j0] : -INFINITY;
-                }
-        }
-        float l[2];
-        bool ev[2];
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int r = r0 + hf * 32 + lane;
-            ev[hf] = r < a.R && r >= j0;
-#pragma unroll
-            for (int q = 0; q < NB; ++q)
-                if (q == c % NB) l[hf] = lq[q][hf];
-        }
-        const float Mn = fmaxf(Mo, warp_max(fmaxf(l[0], l[1])));
-        const float Rf = (Mn == Mo) ? 1.f : expf(Mo - Mn);
-        const float base = Rf * Zo;
-        float run = 0.f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int r = r0 + hf * 32 + lane;
-            const float e = ev[hf] ? expf(l[hf] - Mn) : 0.f;
-            if (ev[hf]) E[r - j0] = e;
-            float incl = e;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            if (r < a.R) P[r] = base + (run + incl);
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        Zo = base + run;
-        Mo = Mn;
-        if (lane == 0) {
-            a.Mc[(size_t)wid * a.nsub + c] = Mn;
-            a.Rc[(size_t)wid * a.nsub + c] = Rf;
-        }
-    }
-    if (lane == 0) {
-        a.M[wid] = Mo;
-        a.Z[wid] = Zo;
-    }
+// ------------------------------------------------------------- far field
+
+// Per (block c of O1_SUB rows, head): the far logits of the keys the block's
+// rows evict (row r >= j0 evicts X[r - j0]), l_bj = scale qt_b . k_ev(j); per
+// landmark the block-local max m_b = max_j l_bj, E_bj = e^{l_bj - m_b} with
+// its in-block prefix over the rows and its total s_b; and the block's value
+// sum increment dT_b = sum_j E_bj v_ev(j), also relative to m_b. The block
+// partials compose associatively: k_far_tscan moves them to the running max.
+// E and the prefix are 0 on rows that evict nothing.
+//
+// Layout (256 threads): the logits as two 128-thread halves, each over half
+// of every 32-wide k chunk, 4 x 4 register tiles (landmarks x keys) with
+// float4 k steps, the halves summed per landmark; the increment with E held
+// k-major (a warp's 4 landmarks are one broadcast float4 per key) against
+// float4 value columns, NV x 128 columns per warp.
+constexpr int FB_LDK = 36;   // 32-wide k chunk + 4
+constexpr int FB_LDE = 68;   // E^T row stride (64 landmarks + 4)
+
+__host__ __device__ inline size_t far_block_smem_floats() {
+    return (size_t)2 * 64 * FB_LDK + 64 * 65 + 64 * FB_LDE;
 }
 
-// Value-sum increment of each block: dT[c][gh][b][t] = sum over the block's
-// evicting rows j of E[b][j] v_ev(j)[t]. Block = (block c, head, 64 columns).
-__global__ __launch_bounds__(256) void k_far_dT(O1Args a) {
-    const int c = blockIdx.x, gh = blockIdx.y, tc = blockIdx.z * 64, g = gh / a.hpg;
+template <int NV>
+__global__ __launch_bounds__(256) void k_far_block(O1Args a) {
+    extern __shared__ __align__(16) float sm[];
+    const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
     const O1Meta mt = o1_meta(a, g);
     const int j0 = mt.wg - mt.len0;
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
-    float *dst = a.Tp + (size_t)(c * a.nh + gh) * a.m * a.dv;
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-    if (max(r0, j0) >= r0 + nr) {   // nothing evicted in this block
-        for (int idx = threadIdx.x; idx < a.m * 64; idx += 256) {
-            const int b = idx >> 6, t = tc + (idx & 63);
-            if (t < a.dv) dst[(size_t)b * a.dv + t] = 0.f;
+    const int jb = min(nr, max(0, j0 - r0));   // first evicting row of the block
+    const int m = a.m, d = a.d, dv = a.dv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t nm = (size_t)a.nh * m;
+    float *sA = sm;                        // [64][FB_LDK] landmark chunk
+    float *sB = sA + 64 * FB_LDK;          // [64][FB_LDK] key chunk
+    float *sL = sB + 64 * FB_LDK;          // [64][65] first half's logits
+    float *sEt = sL + 64 * 65;             // [64 rows][FB_LDE] E, k-major
+    float *sP = sA;                        // [64][65] second half's logits (after the k loop)
+    float *sV = sA;                        // [16][dv + 4] value chunk (after the landmark loop)
+    const bool any = jb < nr;
+    const int nlt = (m + 31) >> 5;
+    if (any) {
+        const int half = tid >> 7, gy = (tid & 127) >> 4, gx = tid & 15;
+        float acc[2][4][4];
+        blk_zero(acc[0]);
+        blk_zero(acc[1]);
+        for (int kc = 0; kc < d; kc += 32) {
+            for (int idx = tid; idx < 2 * 64 * 8; idx += 256) {
+                const int which = idx >> 9, row = (idx >> 3) & 63, k = kc + 4 * (idx & 7);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (k < d) {
+                    if (which == 0) {
+                        if (row < m) v = *(const float4 *)(a.qt + ((size_t)gh * m + row) * d + k);
+                    } else if (row >= jb && row < nr) {
+                        v = *(const float4 *)(o1_key(a, g, r0 + row - j0, mt) + k);
+                    }
+                }
+                *(float4 *)((which ? sB : sA) + row * FB_LDK + 4 * (idx & 7)) = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int ko = 16 * half + 4 * s4;
+                float4 av[4], bv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bv[j] = *(const float4 *)(sB + (gx + 16 * j) * FB_LDK + ko);
+#pragma unroll
+                for (int lt = 0; lt < 2; ++lt) {
+                    if (lt < nlt) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) av[i] = *(const float4 *)(sA + (32 * lt + gy + 8 * i) * FB_LDK + ko);
+                        fma4x4_k4(acc[lt], av, bv);
+                    }
+                }
+            }
+            __syncthreads();
         }
-        return;
-    }
-    __shared__ float sA[64 * 65], sB[64 * 65];
-    for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
-        const int i = idx >> 6, jj = idx & 63;
-        const int r = r0 + jj;
-        const bool evj = jj < nr && r >= j0;
-        sA[i * 65 + jj] = (i < a.m && evj) ? a.E[((size_t)gh * a.m + i) * a.cap + (r - j0)] : 0.f;
-        // row i of B is evicting row r0 + i, column jj is value column tc + jj
-        const int ri = r0 + i;
-        const bool evi = i < nr && ri >= j0 && tc + jj < a.dv;
-        sB[i * 65 + jj] = evi ? o1_val(a, g, ri - j0, mt)[tc + jj] : 0.f;
+        float *dst = half ? sP : sL;
+#pragma unroll
+        for (int lt = 0; lt < 2; ++lt)
+            if (lt < nlt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) dst[(32 * lt + gy + 8 * i) * 65 + gx + 16 * j] = acc[lt][i][j];
     }
     __syncthreads();
-    float acc[4][4];
-    blk_zero(acc);
-    blk_nn(acc, sA, 65, sB, 65, 64);
+    // one warp per landmark: max, E, prefix over the block's rows (lane, lane + 32)
+    for (int b = warp; b < m; b += 8) {
+        const size_t wid = (size_t)gh * m + b;
+        const bool e0 = lane >= jb && lane < nr, e1 = lane + 32 >= jb && lane + 32 < nr;
+        const float l0 = e0 ? a.scale * (sL[b * 65 + lane] + sP[b * 65 + lane]) : -INFINITY;
+        const float l1 = e1 ? a.scale * (sL[b * 65 + lane + 32] + sP[b * 65 + lane + 32]) : -INFINITY;
+        const float mx = warp_max(fmaxf(l0, l1));
+        const float x0 = e0 ? expf(l0 - mx) : 0.f, x1 = e1 ? expf(l1 - mx) : 0.f;
+        float p0 = x0, p1 = x1;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int b = ty + 16 * i, t = tc + tx + 16 * j;
-            if (b < a.m && t < a.dv) dst[(size_t)b * a.dv + t] = acc[i][j];
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t0 = __shfl_up_sync(0xffffffffu, p0, o), t1 = __shfl_up_sync(0xffffffffu, p1, o);
+            if (lane >= o) {
+                p0 += t0;
+                p1 += t1;
+            }
         }
+        p1 += __shfl_sync(0xffffffffu, p0, 31);
+        sEt[lane * FB_LDE + b] = x0;
+        sEt[(lane + 32) * FB_LDE + b] = x1;
+        if (lane < nr) {
+            a.E[wid * a.cap + r0 + lane] = x0;
+            a.P[wid * a.cap + r0 + lane] = p0;
+        }
+        if (lane + 32 < nr) {
+            a.E[wid * a.cap + r0 + lane + 32] = x1;
+            a.P[wid * a.cap + r0 + lane + 32] = p1;
+        }
+        if (lane == 31) {
+            a.Fb[(O1_FB_LMAX * nm + wid) * a.nsub + c] = mx;
+            a.Fb[(O1_FB_LSUM * nm + wid) * a.nsub + c] = p1;
+        }
+        if (c == 0 && lane == 0) {
+            // the entering (M, Z), which k_far_tscan reads while it replaces the state's
+            a.Fb[O1_FB_PLANES * nm * a.nsub + wid] = a.M[wid];
+            a.Fb[O1_FB_PLANES * nm * a.nsub + nm + wid] = a.Z[wid];
+        }
+    }
+    if (!any) return;   // k_far_tscan adds no increment for a block without evictions
+    __syncthreads();
+    // dT[b][t] for the warp's landmarks b = 32 s + 4 warp + (0..3), columns
+    // t = 4 lane + 128 v + (0..3)
+    float *dst = a.Tp + ((size_t)c * a.nh + gh) * m * dv;
+    const int ldv = dv + 4, dv4 = dv >> 2;
+    for (int s = 0; s < nlt; ++s) {
+        float acc[4][NV][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) acc[i][v][0] = acc[i][v][1] = acc[i][v][2] = acc[i][v][3] = 0.f;
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+            for (int idx = tid; idx < 16 * dv4; idx += 256) {
+                const int kk = idx / dv4, c4 = idx - kk * dv4, jj = k0 + kk;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (jj >= jb && jj < nr) v = ((const float4 *)o1_val(a, g, r0 + jj - j0, mt))[c4];
+                *(float4 *)(sV + kk * ldv + 4 * c4) = v;
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int kk = 0; kk < 16; ++kk) {
+                const float4 e4 = *(const float4 *)(sEt + (k0 + kk) * FB_LDE + 32 * s + 4 * warp);
+                const float er[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const int col = 4 * lane + 128 * v;
+                    const float4 bv = col < dv ? *(const float4 *)(sV + kk * ldv + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[i][v][0] = fmaf(er[i], bv.x, acc[i][v][0]);
+                        acc[i][v][1] = fmaf(er[i], bv.y, acc[i][v][1]);
+                        acc[i][v][2] = fmaf(er[i], bv.z, acc[i][v][2]);
+                        acc[i][v][3] = fmaf(er[i], bv.w, acc[i][v][3]);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int b = 32 * s + 4 * warp + i;
+            if (b >= m) continue;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int col = 4 * lane + 128 * v;
+                if (col < dv)
+                    *(float4 *)(dst + (size_t)b * dv + col) =
+                        make_float4(acc[i][v][0], acc[i][v][1], acc[i][v][2], acc[i][v][3]);
+            }
+        }
+    }
 }
 
-// The value sum entering each block, rescaled to that block's max:
-// Tp[c] <- R_c T_{c-1} (what the block's rows read), T_c = R_c T_{c-1} + dT_c;
-// the last T is the new state. One thread per (head, landmark, column).
-__global__ void k_far_tscan(O1Args a) {
-    const size_t n = (size_t)a.nh * a.m * a.dv;
+// One thread per (head, landmark, value column), sequential over the pass's
+// blocks. With block max m_c and mass s_c from k_far_block: the running far
+// max M_c = max(M_{c-1}, m_c), the rescale R_c = e^{M_{c-1} - M_c} (1 when
+// the max stays, so an empty field stays empty) and the block factor
+// f_c = e^{m_c - M_c} (0 for a block without evictions). The value sum
+// entering block c, R_c T_{c-1}, goes to Tp[c] and T_c = R_c T_{c-1} + f_c dT_c;
+// the mass likewise, Z_c = R_c Z_{c-1} + f_c s_c. Column 0's thread records
+// M_c, R_c Z_{c-1} and f_c for the side readout; the last M, Z, T are the new
+// state (o1b_far_e's max / rescale and o1b_far_commit's recurrence, taken as
+// a scan over the blocks).
+__global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
+    const size_t n = (size_t)a.nh * a.m * a.dv, nm = (size_t)a.nh * a.m;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n) return;
     const size_t wid = idx / a.dv;
+    const bool col0 = idx - wid * a.dv == 0;
+    const float *lmax = a.Fb + (O1_FB_LMAX * nm + wid) * a.nsub;
+    const float *lsum = a.Fb + (O1_FB_LSUM * nm + wid) * a.nsub;
+    float *Mc = a.Fb + (O1_FB_MC * nm + wid) * a.nsub;
+    float *Bc = a.Fb + (O1_FB_BASE * nm + wid) * a.nsub;
+    float *Fc = a.Fb + (O1_FB_FAC * nm + wid) * a.nsub;
     float T = a.T[idx];
-    // 16 blocks' loads issued before their stores (the compiler cannot
-    // reorder them itself: the stores may alias later loads for all it knows)
-    for (int c0 = 0; c0 < a.nsub; c0 += 16) {
-        float rf[16], dT[16];
+    float Mo = a.Fb[O1_FB_PLANES * nm * a.nsub + wid], Zo = a.Fb[O1_FB_PLANES * nm * a.nsub + nm + wid];
+    // 8 blocks' loads issued before their stores (the compiler cannot
+    // reorder them itself: the stores may alias later loads for all it knows);
+    // few enough registers for the scan to sit beside a window CTA
+    for (int c0 = 0; c0 < a.nsub; c0 += 8) {
+        float lm[8], ls[8], dT[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const int c = c0 + i;
-            rf[i] = c < a.nsub ? a.Rc[wid * a.nsub + c] : 1.f;
+            lm[i] = c < a.nsub ? lmax[c] : -INFINITY;
+            ls[i] = c < a.nsub ? lsum[c] : 0.f;
             dT[i] = c < a.nsub ? a.Tp[(size_t)c * n + idx] : 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const int c = c0 + i;
             if (c < a.nsub) {
-                const float Ts = rf[i] * T;
+                const float Mn = fmaxf(Mo, lm[i]);
+                const float Rf = Mn == Mo ? 1.f : expf(Mo - Mn);
+                const float f = lm[i] == -INFINITY ? 0.f : expf(lm[i] - Mn);
+                const float Ts = Rf * T;
                 a.Tp[(size_t)c * n + idx] = Ts;
-                T = Ts + dT[i];
+                T = f != 0.f ? fmaf(f, dT[i], Ts) : Ts;
+                const float base = Rf * Zo;
+                if (col0) {
+                    Mc[c] = Mn;
+                    Bc[c] = base;
+                    Fc[c] = f;
+                }
+                Zo = fmaf(f, ls[i], base);
+                Mo = Mn;
             }
         }
     }
     a.T[idx] = T;
+    if (col0) {
+        a.M[wid] = Mo;
+        a.Z[wid] = Zo;
+    }
 }
 
 // The side part of every row of block c for head gh: the sinks and the far
@@ -299,21 +378,10 @@ __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
     off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks
     off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
     off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
-    off[4] = off[3] + 64 * 65;                               // F, M_c [64] each
-    off[5] = off[4] + 2 * 64;                                // total (floats)
+    off[4] = off[3] + 64 * 65;                               // F, M_c, R_c Z_{c-1}, f_c [64] each
+    off[5] = off[4] + 4 * 64;                                // total (floats)
 }
 
-__device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
-            c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
-            c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
-            c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
-        }
-}
 
 template <int NV>
 __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
@@ -336,10 +404,29 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     float *sS = sm + off[2];
     float *sR3 = sm + off[3];
     float *sRow = sm + off[4];
-    float *sMc = sRow + 64;
+    float *sMc = sRow + 64;    // M_c, R_c Z_{c-1}, f_c per landmark
+    float *sBc = sRow + 128;
+    float *sFc = sRow + 192;
 
-    // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks
-    {
+    // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks. A block
+    //    without far field needs only the few sink columns: a warp per row.
+    if (!far_any && ns <= 8) {
+        for (int i = warp; i < nr; i += 8) {
+            const float *qrow = a.qr + ((size_t)(r0 + i) * nh + gh) * d;
+            float qv[O1_MAX_D / 32];
+#pragma unroll
+            for (int t = 0; t < O1_MAX_D / 32; ++t) qv[t] = lane + 32 * t < d ? qrow[lane + 32 * t] : 0.f;
+            for (int x = 0; x < ns; ++x) {
+                const float *sk = a.sink_k + ((size_t)g * ns + x) * d;
+                float dot = 0.f;
+#pragma unroll
+                for (int t = 0; t < O1_MAX_D / 32; ++t)
+                    if (lane + 32 * t < d) dot = fmaf(qv[t], sk[lane + 32 * t], dot);
+                dot = warp_sum(dot);
+                if (lane == 0) sS[i * ldS + m + x] = a.scale * dot;
+            }
+        }
+    } else {
         float *sQc = sR1;                    // [64][SR_LDQ]
         float *sBc = sR1 + 64 * SR_LDQ;      // [64 nbt][SR_LDQ]
         float acc[2][4][4];
@@ -397,7 +484,13 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             const int aa = idx / m, b = idx % m;
             sMu[aa * 65 + b] = a.mu[((size_t)gh * m + aa) * m + b];
         }
-        for (int b = tid; b < 64; b += 256) sMc[b] = b < m ? a.Mc[((size_t)gh * m + b) * a.nsub + c] : 0.f;
+        const size_t nm = (size_t)nh * m;
+        for (int b = tid; b < 64; b += 256) {
+            const size_t wid = (size_t)gh * m + b;
+            sMc[b] = b < m ? a.Fb[(O1_FB_MC * nm + wid) * a.nsub + c] : 0.f;
+            sBc[b] = b < m ? a.Fb[(O1_FB_BASE * nm + wid) * a.nsub + c] : 0.f;
+            sFc[b] = b < m ? a.Fb[(O1_FB_FAC * nm + wid) * a.nsub + c] : 0.f;
+        }
         __syncthreads();
         // 2. F per row and e^{f - F} (columns [0, m))
         for (int i = warp; i < 64; i += 8) {
@@ -420,12 +513,12 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             for (int j = 0; j < 4; ++j)
                 if (tx + 16 * j < m) sS[(ty + 16 * i) * ldS + tx + 16 * j] = acc[i][j];
         __syncthreads();
-        // E of this block's evicting rows, referenced to M_c by k_far_scan
+        // E of this block's evicting rows, moved from the block max to M_c
         float *sE = sR3;   // [m][65]
         for (int idx = tid; idx < m * 64; idx += 256) {
             const int b = idx >> 6, jj = idx & 63;
             const int r = r0 + jj;
-            sE[b * 65 + jj] = (jj < nr && r >= j0) ? a.E[((size_t)gh * m + b) * a.cap + (r - j0)] : 0.f;
+            sE[b * 65 + jj] = (jj < nr && r >= j0) ? sFc[b] * a.E[((size_t)gh * m + b) * a.cap + r] : 0.f;
         }
     }
 
@@ -450,8 +543,10 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             cf = warp_max(fmaxf(cb0, cb1));
             g0 = lane < m ? u0 * expf(cb0 - cf) : 0.f;
             g1 = lane + 32 < m ? u1 * expf(cb1 - cf) : 0.f;
-            const float p0 = lane < m ? a.P[((size_t)gh * m + lane) * a.cap + r] : 0.f;
-            const float p1 = lane + 32 < m ? a.P[((size_t)gh * m + lane + 32) * a.cap + r] : 0.f;
+            // far mass P_b(row) = R_c Z_{c-1} + f_c (in-block prefix)
+            const float p0 = lane < m ? fmaf(sFc[lane], a.P[((size_t)gh * m + lane) * a.cap + r], sBc[lane]) : 0.f;
+            const float p1 =
+                lane + 32 < m ? fmaf(sFc[lane + 32], a.P[((size_t)gh * m + lane + 32) * a.cap + r], sBc[lane + 32]) : 0.f;
             D = warp_sum(g0 * p0 + g1 * p1);
             have = D >= 0.f;
         }
@@ -818,7 +913,7 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a) {
 // ------------------------------------------------------------- launchers
 
 extern const char *const o1_stage_names[O1_NUM_STAGES] = {
-    "rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near", "merge", "commit"};
+    "rope", "far_block", "far_tscan", "side_readout", "gather_tc", "near", "merge", "commit"};
 
 static size_t readout_smem(const O1Args &a) {
     size_t off[6];
@@ -860,8 +955,8 @@ cudaError_t o1_aux(O1Aux **out) {
 
 }  // namespace
 
-// Stages: rope | far_logits, far_scan, far_dT, far_tscan, side_readout |
-// gather_tc, near | merge, commit. The two middle branches run concurrently,
+// Stages: rope | far_block, far_tscan, side_readout | gather_tc, near |
+// merge, commit. The two middle branches run concurrently,
 // the far one on the library's second stream. With `ev`, events 2i and 2i + 1
 // are recorded just before and just after stage i on the stream it runs on.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
@@ -869,6 +964,8 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     if (!attrs_set) {
         cudaFuncSetAttribute(k_side_readout<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+        cudaFuncSetAttribute(k_far_block<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
         cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attrs_set = true;
@@ -891,27 +988,23 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     cudaEventRecord(aux->fork, st);
     cudaStreamWaitEvent(sf, aux->fork, 0);
     begin(1, sf);
-    k_far_logits<<<dim3(nblk, a.nh), 256, 0, sf>>>(a);
+    const size_t fbs = far_block_smem_floats() * sizeof(float);
+    if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
+    else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
     end(1, sf);
     begin(2, sf);
-    k_far_scan<<<(a.nh * a.m * 32 + 255) / 256, 256, 0, sf>>>(a);
-    end(2, sf);
-    begin(3, sf);
-    k_far_dT<<<dim3(nblk, a.nh, (a.dv + 63) / 64), 256, 0, sf>>>(a);
-    end(3, sf);
-    begin(4, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
-    end(4, sf);
-    begin(5, sf);
+    end(2, sf);
+    begin(3, sf);
     if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
-    end(5, sf);
+    end(3, sf);
     cudaEventRecord(aux->join, sf);
-    begin(6, st);
+    begin(4, st);
     if (a.tc) e = o1_launch_gather_tc(a, st);
-    end(6, st);
-    begin(7, st);
+    end(4, st);
+    begin(5, st);
     if (e == cudaSuccess) {
         if (a.tc) {
             e = o1_launch_near_tc(a, st);
@@ -922,18 +1015,18 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
             else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
         }
     }
-    end(7, st);
+    end(5, st);
     // the far branch is joined even when the window launch failed, so that a
     // capture of `st` stays well formed
     cudaStreamWaitEvent(st, aux->join, 0);
     if (e != cudaSuccess) return e;
-    begin(8, st);
+    begin(6, st);
     k_merge<<<(unsigned)(((size_t)R * a.nh + 7) / 8), 256, 0, st>>>(a);
-    end(8, st);
-    begin(9, st);
+    end(6, st);
+    begin(7, st);
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
-    end(9, st);
+    end(7, st);
     return cudaPeekAtLastError();
 }
 

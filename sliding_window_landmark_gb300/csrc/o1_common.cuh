@@ -12,6 +12,13 @@
 #define O1_MAGIC 0x4C53314Fu   // "O1SL"
 #define O1_VERSION 1u
 #define O1_SUB 64              // rows of one far-field reference block
+// planes of the per-block far statistics (scratch Fb)
+#define O1_FB_LMAX 0
+#define O1_FB_LSUM 1
+#define O1_FB_MC 2
+#define O1_FB_BASE 3
+#define O1_FB_FAC 4
+#define O1_FB_PLANES 5
 #define O1_MAX_D 256
 #define O1_MAX_DV 256
 #define O1_MAX_M 64
@@ -64,11 +71,15 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 // A chunk call's scratch for up to `cap` rows per pass (nsub = reference
 // blocks of O1_SUB rows):
 //   qr [cap][nh][d]  rotated queries        kr [cap][G][d]  rotated keys
-//   E  [nh][m][cap]  far logits, then exp(l - M_block) per evicted key
-//   P  [nh][m][cap]  far mass prefix per row
-//   Mc, Rc [nh][m][nsub]  block max and rescale factor
-//   Tp [nsub][nh][m][dv]  far value sums: increments, then the value sum
-//                         entering each block, rescaled to its max
+//   E  [nh][m][cap]  per row, exp(l - block max) of the key it evicts
+//   P  [nh][m][cap]  per row, the in-block prefix of E
+//   Fb [O1_FB_PLANES][nh][m][nsub] per block: local max, local mass (from
+//                    the block kernel), running max M_c, R_c Z_{c-1} and
+//                    the factor exp(local max - M_c) (from the scan); then
+//                    [2][nh][m] the far (M, Z) entering the pass
+//   Tp [nsub][nh][m][dv]  far value sums: increments relative to the block
+//                         max, then the value sum entering each block,
+//                         rescaled to its running max
 //   fh [cap][nh] x 4      per row-head window header, written by the window
 //                         kernel: (reference c_w, mass l, true max, -), the
 //                         window numerator being in `out` relative to c_w
@@ -79,7 +90,7 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 // and the rotated queries as fp16 hi / lo:
 //   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]    Qs [2][cap][nh][d]
 struct O1Scratch {
-    size_t qr, kr, E, P, Mc, Rc, Tp, fh, sh, sn, Xk, XvT, Qs, total;
+    size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, total;
     int cap, nsub, nxp;
 };
 
@@ -107,8 +118,7 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     S.kr = off; off += o1_al256(c * G * d * 4);
     S.E = off;  off += o1_al256(nh * m * c * 4);
     S.P = off;  off += o1_al256(nh * m * c * 4);
-    S.Mc = off; off += o1_al256(nh * m * ns * 4);
-    S.Rc = off; off += o1_al256(nh * m * ns * 4);
+    S.Fb = off; off += o1_al256((O1_FB_PLANES * ns + 2) * nh * m * 4);
     S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
     S.fh = off; off += o1_al256(c * nh * 4 * 4);
     S.sh = off; off += o1_al256(c * nh * 4 * 4);
@@ -178,7 +188,7 @@ struct O1Args {
     float *out;
     int R, nsub;
     // scratch
-    float *qr, *kr, *E, *P, *Mc, *Rc, *Tp, *fh, *sh, *sn;
+    float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
     unsigned short *Xk, *XvT, *Qs;
@@ -293,7 +303,7 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 }
 
 // Launchers (o1_chunk.cu). Each returns cudaPeekAtLastError() after its launches.
-// `ev` may be null; otherwise O1_NUM_STAGES + 1 events recorded around the stages.
+// `ev` may be null; otherwise 2 * O1_NUM_STAGES events, one before and one after each stage.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);
 // Tensor-core window path (o1_near_tc.cu): panel gather, then the window

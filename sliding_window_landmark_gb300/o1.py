@@ -161,7 +161,7 @@ def o1_chunk_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, s
         _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
 
 
-O1_NUM_STAGES = 10
+O1_NUM_STAGES = 8
 
 
 def o1_stage_name(stage: int):

@@ -5,8 +5,8 @@ calls), or `--tokens` one-row calls after a prompt of `--rows` rows.
   python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 4096 --calls 3
   python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 8192 --tokens 16
 
-Launches per chunk call: rope, then far_logits, far_scan, far_dT, far_tscan,
-side_readout on a second stream beside [gather_tc], near, then merge, commit;
+Launches per chunk call: rope, then far_block, far_tscan, side_readout on a
+second stream beside [gather_tc], near, then merge, commit;
 per one-row call: k_tok_main, k_tok_merge. The library must already be built.
 """
 from __future__ import annotations

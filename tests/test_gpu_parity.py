@@ -255,8 +255,7 @@ def test_timed_stages_and_stream_capture():
 
     gpu = harness.GpuLayer(sh, c, max_rows=300)
     names = [o1.o1_stage_name(i) for i in range(o1.O1_NUM_STAGES)]
-    assert names == ["rope", "far_logits", "far_scan", "far_dT", "far_tscan", "side_readout", "gather_tc", "near",
-                     "merge", "commit"]
+    assert names == ["rope", "far_block", "far_tscan", "side_readout", "gather_tc", "near", "merge", "commit"]
     assert o1.o1_stage_name(o1.O1_NUM_STAGES) is None
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * o1.O1_NUM_STAGES)]
     for e in evs:

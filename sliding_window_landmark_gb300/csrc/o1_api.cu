@@ -128,6 +128,7 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
             const O1TokScratch T = o1_tok_layout(g);
             char *sb = (char *)scratch;
             a.part = (float *)(sb + T.part);
+            a.pml = (float *)(sb + T.pml);
             a.farp = (float *)(sb + T.farp);
             a.kcur = (float *)(sb + T.kcur);
             a.KC = T.KC;

@@ -132,33 +132,33 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     return S;
 }
 
-// Scratch of the one-row path: near partials per (group, key slice, head)
-// = (max, sum, value sum [dv]); the far part per head = (c_f, D, have, -,
-// numerator [dv]); the row's rotated key per group. KC keys per slice, NC
-// slices per group, sized for the longest near set (sinks + window), about
-// 64 per group, and capped so that a slice fits in shared memory.
+// Scratch of the one-row path: near partials per (group, key slice, head),
+// the value sums [dv] in `part` and (max, sum) in `pml`; the far part per
+// head = (c_f, D, have, -, numerator [dv]); the row's rotated key per group.
+// KC keys per slice (a multiple of 8), NC slices per group, sized for the
+// longest near set (sinks + window) so that all groups' slices make about
+// one wave of 136 blocks, and capped so that a slice fits in shared memory.
 struct O1TokScratch {
-    size_t part, farp, kcur, total;
+    size_t part, pml, farp, kcur, total;
     int KC, NC;
 };
 
 static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, dv = g.dv, d = g.d;
     const long long nmax = (long long)g.sinks + g.window;
-    // about 64 slices per group: one wave of blocks on the GPU for a couple
-    // of groups, few partials for the merge
-    long long kc = (nmax + 63) / 64;
+    long long kc = (nmax * (long long)G + 135) / 136;
     kc = kc < 8 ? 8 : (kc + 7) / 8 * 8;
-    // a slice's keys, values and scores stay within 227 KB of shared memory
-    // (rows padded by 4 floats)
+    // a slice's keys, values, scores and partial dots (8 per key and head)
+    // stay within 227 KB of shared memory, rows padded by 4 floats
     const long long kmax = ((227 * 1024 / 4) - (long long)(g.heads_per_group + 1) * (g.d + 4) - 2 * g.heads_per_group) /
-                           ((long long)g.d + 4 + g.dv + g.heads_per_group) / 8 * 8;
+                           ((long long)g.d + 4 + g.dv + 9 * g.heads_per_group) / 8 * 8;
     if (kc > kmax) kc = kmax;
     O1TokScratch S;
     S.KC = (int)kc;
     S.NC = (int)((nmax + kc - 1) / kc);
     size_t off = 0;
-    S.part = off; off += o1_al256(G * S.NC * g.heads_per_group * (2 + dv) * 4);
+    S.part = off; off += o1_al256(G * S.NC * g.heads_per_group * dv * 4);
+    S.pml = off;  off += o1_al256(G * S.NC * g.heads_per_group * 2 * 4);
     S.farp = off; off += o1_al256(nh * (4 + dv) * 4);
     S.kcur = off; off += o1_al256(G * d * 4);
     S.total = off;
@@ -194,7 +194,7 @@ struct O1Args {
     unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;
     // one-row path scratch
-    float *part, *farp, *kcur;
+    float *part, *pml, *farp, *kcur;
     int KC, NC;
 };
 

@@ -27,7 +27,8 @@
 //               O += P.V with P read from TMEM. The epilogue writes the
 //               window numerator O to `out` through shared memory with
 //               coalesced stores, and each row's (reference, mass, true max)
-//               to its window header; the side readout merges and gates.
+//               to its window header; k_merge (o1_chunk.cu) adds the
+//               side part under one exponent and gates.
 //
 // Tile width: a 128 x N x 16 MMA costs about the same time on the tensor
 // pipe for N = 64 and N = 128, so S is issued with N = 128 (48 MMAs per

@@ -21,9 +21,11 @@
 //      position.
 // Nothing waits on a flag: the only dependency is the launch order.
 //
-// The step is latency-bound (a few MB, read once), so every block issues its
-// global loads in one batch (many in flight, no integer division in the
-// address arithmetic) before computing from shared memory.
+// The step is latency-bound (a few MB, read once): every block issues its
+// global loads first, all at once (the row's inputs, bulk copies of the
+// large operands), and the dot products run lane-per-key / lane-per-landmark
+// over a warp's share of d, so that no reduction waits on a chain of
+// shuffles.
 #include <math.h>
 
 #include "o1_common.cuh"
@@ -32,7 +34,8 @@ __device__ __forceinline__ void o1_allow_dependents() { asm volatile("griddepcon
 __device__ __forceinline__ void o1_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 static size_t tok_near_floats(const O1Args &a) {
-    return 4 + (size_t)(a.hpg + 1) * a.d + (size_t)a.KC * (a.d + a.dv) + (size_t)a.KC * a.hpg + 2 * a.hpg;
+    return 4 + (size_t)(a.hpg + 1) * a.d + (size_t)a.KC * (a.d + a.dv) + (size_t)a.KC * a.hpg + 2 * a.hpg +
+           (size_t)8 * a.KC * a.hpg;
 }
 
 // Bulk copies into shared memory completing on one mbarrier: thread 0 adds
@@ -70,7 +73,7 @@ __device__ __forceinline__ void tok_wait_copies(const O1Args &a, uint64_t *bar) 
 
 static size_t tok_far_floats(const O1Args &a) {
     const size_t m = a.m;
-    return 4 + 2 * (size_t)a.d + a.dv + 2 * m * a.d + m * (m + 1) + m * a.dv + 11 * m + 32;
+    return 4 + 2 * (size_t)a.d + a.dv + 2 * m * a.d + m * (m + 1) + m * a.dv + 16 * m + 4 * m + 4;
 }
 
 static size_t tok_main_smem(const O1Args &a) {
@@ -78,65 +81,99 @@ static size_t tok_main_smem(const O1Args &a) {
     return 4 * (n > f ? n : f);
 }
 
-// Rotates the rows xs[0 .. n-1] (global, d wide) into dst[r] (shared) at
-// position p: pair (j, j + d/2), one angle per j for all rows.
-__device__ __forceinline__ void tok_rotate(const O1Args &a, long long p, const float *const *xs, float *const *dst,
-                                           int n) {
-    const int half = a.d >> 1;
-    for (int j = threadIdx.x; j < half; j += blockDim.x) {
-        float cs = 1.f, sn = 0.f;
-        if (a.rotate) o1_rope_cs(a.hdr->inv_freq[j], p, cs, sn);
-        for (int h0 = 0; h0 < n; h0 += 8) {
-            float x0[8], x1[8];
+// Rotary angle of pair j at the row's position (identity when the layer
+// does not rotate).
+__device__ __forceinline__ void tok_cs(const O1Args &a, float inv, long long p, float &cs, float &sn) {
+    cs = 1.f;
+    sn = 0.f;
+    if (a.rotate) o1_rope_cs(inv, p, cs, sn);
+}
+
+// Dot products of `n` rows of shared memory (rows of d floats, `rows`
+// apart) with `nq` vectors (d floats, `qstride` apart), lane = row, warp =
+// a contiguous share of d in float4 units, visited from a lane-dependent
+// start so that the 8 lanes of a quarter warp read 8 different bank groups.
+// Returns the warp's partial dots in acc[0 .. nq-1] (0 for lanes >= n).
+template <int NQ>
+__device__ __forceinline__ void tok_dots(const float *rows, int row, bool valid, const float *qs, int qstride,
+                                         int nq, int d, float (&acc)[NQ]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = d >> 2, U = (nu + 7) >> 3;
+    const int ub = warp * U;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const bool in = h0 + u < n;
-                x0[u] = in ? xs[h0 + u][j] : 0.f;
-                x1[u] = in ? xs[h0 + u][j + half] : 0.f;
-            }
+    for (int h = 0; h < NQ; ++h) acc[h] = 0.f;
+    if (!valid) return;
+    const float4 *kr = (const float4 *)(rows + (size_t)row * d);
+    int s = lane % U;
+    for (int t = 0; t < U; ++t) {
+        const int u = ub + s;
+        if (u < nu) {
+            const float4 kv = kr[u];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (h0 + u >= n) break;
-                dst[h0 + u][j] = x0[u] * cs - x1[u] * sn;
-                dst[h0 + u][j + half] = x1[u] * cs + x0[u] * sn;
+            for (int h = 0; h < NQ; ++h) {
+                if (h >= nq) break;
+                const float4 qv = ((const float4 *)(qs + (size_t)h * qstride))[u];
+                acc[h] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[h]))));
             }
         }
+        if (++s == U) s = 0;
     }
 }
 
 __device__ void tok_near(const O1Args &a, int g, int c, const O1Meta &mt, float *sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.d, dv = a.dv, hpg = a.hpg;
+    const int d = a.d, dv = a.dv, hpg = a.hpg, KC = a.KC;
     const bool evict = mt.len0 == mt.wg;
     const int len1 = evict ? mt.wg : mt.len0 + 1;
     const int head1 = evict ? (mt.head0 + 1) % mt.wg : mt.head0;
     const int n = a.ns + len1;
-    const int i0 = c * a.KC;
-    const int cnt = max(0, min(a.KC, n - i0));
-    float *part = a.part + (size_t)(g * a.NC + c) * hpg * (2 + dv);
+    const int i0 = c * KC;
+    const int cnt = max(0, min(KC, n - i0));
+    const size_t slot = (size_t)(g * a.NC + c) * hpg;
+    float *pv = a.part + slot * dv;   // [hpg][dv]
+    float *pml = a.pml + slot * 2;    // [hpg][2]
 
     uint64_t *sbar = (uint64_t *)sm;   // the slice's copy barrier
     float *sq = sm + 4;                // [hpg][d]
     float *sk = sq + hpg * d;          // [d]
     float *sK = sk + d;                // [KC][d]
-    float *sV = sK + a.KC * d;         // [KC][dv]
-    float *sS = sV + a.KC * dv;        // [KC][hpg]
-    float *sML = sS + a.KC * hpg;      // [hpg][2]
+    float *sV = sK + KC * d;           // [KC][dv]
+    float *sS = sV + KC * dv;          // [KC][hpg]
+    float *sML = sS + KC * hpg;        // [hpg][2]
+    float *sP = sML + 2 * hpg;         // [8 warps][KC][hpg] partial dots
 
     if (cnt == 0 && c != 0) {
-        for (int idx = tid; idx < hpg * (2 + dv); idx += blockDim.x) {
-            const int e = idx % (2 + dv);
-            part[idx] = e == 0 ? -INFINITY : 0.f;
+        for (int h = tid; h < hpg; h += blockDim.x) {
+            pml[2 * h] = -INFINITY;
+            pml[2 * h + 1] = 0.f;
         }
         return;
     }
+    // the row's inputs first, every load in flight at once: position, the
+    // rotary frequency of pair j = tid, the group's queries and key at j and
+    // j + d/2, the row's value
+    const int half = d >> 1;
+    const bool rj = tid < half;
+    const long long p = a.hdr->pos;
+    const float inv = rj ? a.hdr->inv_freq[tid] : 0.f;
+    float x0[O1_MAX_HPG + 1], x1[O1_MAX_HPG + 1];
+#pragma unroll
+    for (int h = 0; h <= O1_MAX_HPG; ++h) {
+        const float *src = h < hpg ? a.q + (size_t)(g * hpg + h) * d : a.k + (size_t)g * d;
+        const bool in = rj && h <= hpg;
+        x0[h] = in ? src[tid] : 0.f;
+        x1[h] = in ? src[tid + half] : 0.f;
+    }
+    const int ipush = a.ns + len1 - 1 - i0;
+    const bool has_push = ipush >= 0 && ipush < cnt;
+    float4 vpush = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (has_push && tid < (dv >> 2)) vpush = ((const float4 *)(a.v + (size_t)g * dv))[tid];
     // The slice's keys and values: sinks, then ring logical 0..len1-1, as at
     // most three contiguous runs (the sinks, the ring up to its end, the ring
     // from slot 0), each one bulk copy for K and one for V. The last logical
     // key is the pushed one: its slot is overwritten by this row, so its key
     // row is replaced by the row's own rotated key (sk) and its value row by
     // the row's value once the copies have landed.
-    const int ipush = a.ns + len1 - 1 - i0;
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tok_su32(sbar)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -161,20 +198,17 @@ __device__ void tok_near(const O1Args &a, int g, int c, const O1Meta &mt, float 
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tok_su32(sbar)) : "memory");
     }
     // rotate the group's queries and its key while the copies are in flight
-    {
-        const float *xs[O1_MAX_HPG + 1];
-        float *dst[O1_MAX_HPG + 1];
-        for (int h = 0; h < hpg; ++h) {
-            xs[h] = a.q + (size_t)(g * hpg + h) * d;
-            dst[h] = sq + h * d;
+    if (rj) {
+        float cs, sn;
+        tok_cs(a, inv, p, cs, sn);
+#pragma unroll
+        for (int h = 0; h <= O1_MAX_HPG; ++h) {
+            if (h > hpg) break;
+            float *dst = h < hpg ? sq + h * d : sk;
+            dst[tid] = x0[h] * cs - x1[h] * sn;
+            dst[tid + half] = x1[h] * cs + x0[h] * sn;
         }
-        xs[hpg] = a.k + (size_t)g * d;
-        dst[hpg] = sk;
-        tok_rotate(a, a.hdr->pos, xs, dst, hpg + 1);
     }
-    float4 vpush = make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool has_push = ipush >= 0 && ipush < cnt;
-    if (has_push && tid < (dv >> 2)) vpush = ((const float4 *)(a.v + (size_t)g * dv))[tid];
     __syncthreads();   // the barrier is initialised before anyone waits on it
     tok_wait_copies(a, sbar);
     if (c == 0)
@@ -183,29 +217,25 @@ __device__ void tok_near(const O1Args &a, int g, int c, const O1Meta &mt, float 
         for (int j = tid; j < d; j += blockDim.x) sK[ipush * d + j] = sk[j];
         if (tid < (dv >> 2)) ((float4 *)(sV + (size_t)ipush * dv))[tid] = vpush;   // dv <= 4 * blockDim
     }
-    if (cnt == 0) return;   // slice 0 of an empty set only publishes the key
     __syncthreads();
-    // scores: one warp per key, lanes across d (dense rows, conflict-free),
-    // every head of the group at once
-    for (int i = warp; i < cnt; i += blockDim.x >> 5) {
+    // scores: partial dots per warp (lane = key), then their sum per (key, head)
+    for (int k0 = 0; k0 < cnt; k0 += 32) {
         float acc[O1_MAX_HPG];
-#pragma unroll
-        for (int h = 0; h < O1_MAX_HPG; ++h) acc[h] = 0.f;
-        for (int j4 = lane; j4 < (d >> 2); j4 += 32) {
-            const float4 kv = ((const float4 *)(sK + (size_t)i * d))[j4];
+        const int key = k0 + lane;
+        tok_dots(sK, key, key < cnt, sq, d, hpg, d, acc);
+        if (key < cnt)
 #pragma unroll
             for (int h = 0; h < O1_MAX_HPG; ++h) {
                 if (h >= hpg) break;
-                const float4 qv = ((const float4 *)(sq + h * d))[j4];
-                acc[h] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[h]))));
+                sP[((size_t)warp * KC + key) * hpg + h] = acc[h];
             }
-        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < cnt * hpg; idx += blockDim.x) {
+        float s = 0.f;
 #pragma unroll
-        for (int h = 0; h < O1_MAX_HPG; ++h) {
-            if (h >= hpg) break;
-            const float sh = warp_sum(acc[h]);
-            if (lane == 0) sS[i * hpg + h] = sh * a.scale;
-        }
+        for (int w = 0; w < 8; ++w) s += sP[(size_t)w * KC * hpg + idx];
+        sS[idx] = s * a.scale;
     }
     __syncthreads();
     // slice-local softmax per head
@@ -221,31 +251,30 @@ __device__ void tok_near(const O1Args &a, int g, int c, const O1Meta &mt, float 
         }
         l = warp_sum(l);
         if (lane == 0) {
-            sML[2 * h] = mx;
-            sML[2 * h + 1] = l;
+            pml[2 * h] = mx;
+            pml[2 * h + 1] = l;
         }
     }
     __syncthreads();
-    // value sums: thread per (head, column), two accumulators
-    for (int idx = tid; idx < hpg * dv; idx += blockDim.x) {
-        const int h = idx / dv, t = idx - h * dv;
-        float acc0 = 0.f, acc1 = 0.f;
-        int i = 0;
-        for (; i + 1 < cnt; i += 2) {
-            acc0 = fmaf(sS[i * hpg + h], sV[i * dv + t], acc0);
-            acc1 = fmaf(sS[(i + 1) * hpg + h], sV[(i + 1) * dv + t], acc1);
+    // value sums: thread per (head, 4 columns)
+    const int dv4 = dv >> 2;
+    for (int idx = tid; idx < hpg * dv4; idx += blockDim.x) {
+        const int h = idx / dv4, c4 = idx - h * dv4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < cnt; ++i) {
+            const float w = sS[i * hpg + h];
+            const float4 v = ((const float4 *)(sV + (size_t)i * dv))[c4];
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
         }
-        if (i < cnt) acc0 = fmaf(sS[i * hpg + h], sV[i * dv + t], acc0);
-        part[h * (2 + dv) + 2 + t] = acc0 + acc1;
-    }
-    for (int h = tid; h < hpg; h += blockDim.x) {
-        part[h * (2 + dv)] = sML[2 * h];
-        part[h * (2 + dv) + 1] = sML[2 * h + 1];
+        ((float4 *)(pv + (size_t)h * dv))[c4] = acc;
     }
 }
 
 __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float *sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, dv = a.dv, m = a.m;
     const int h = g * a.hpg + hl;
     const bool evict = mt.len0 == mt.wg;
@@ -256,25 +285,38 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
         return;
     }
     uint64_t *sbar = (uint64_t *)sm;   // the block's copy barrier
-    float *sq = sm + 4;            // [d]
-    float *ske = sq + d;           // [d]
-    float *sve = ske + d;          // [dv]
-    float *sqt = sve + dv;         // [m][d]  landmark queries of this head
-    float *skt = sqt + m * d;      // [m][d]  landmark keys of the group
-    float *sT = skt + m * d;       // [m][dv] value sums
-    float *smu = sT + m * dv;      // [m][m + 1]
-    float *sMo = smu + m * (m + 1); // [m] far max before the insert
-    float *sZo = sMo + m;          // [m]
-    float *sMn = sZo + m;          // [m] far max after the insert
-    float *sZn = sMn + m;          // [m] far mass after the insert
-    float *sRho = sZn + m;         // [m]
-    float *sE = sRho + m;          // [m]
-    float *sF = sE + m;            // [m] landmark scores, then e^{f - F}
-    float *sG = sF + m;            // [m] u, then gains
-    float *sC = sG + m;            // [m] F + M_b
-    float *sRed = sC + m;          // [32]
+    float *sq = sm + 4;                // [d]
+    float *ske = sq + d;               // [d]
+    float *sve = ske + d;              // [dv]
+    float *sqt = sve + dv;             // [m][d]  landmark queries of this head
+    float *skt = sqt + m * d;          // [m][d]  landmark keys of the group
+    float *sT = skt + m * d;           // [m][dv] value sums
+    float *smu = sT + m * dv;          // [m][m + 1]
+    float *sP = smu + m * (m + 1);     // [8 warps][m][2] partial dots
+    float *se = sP + 16 * m;           // [m] e^{f - F}
+    float *sG = se + m;                // [m] gains
+    float *sRho = sG + m;              // [m]
+    float *sE = sRho + m;              // [m]
+    float *sRed = sE + m;              // [4] c_f, D
 
-    // every large input of the block by bulk copies, the small ones by loads
+    // inputs first: position, frequency and query pair j = tid, the far
+    // max and mass (warp 0, landmarks lane and lane + 32), then the bulk
+    // copies of the large operands and the mixing matrix
+    const int half = d >> 1;
+    const bool rj = tid < half;
+    const long long p = a.hdr->pos;
+    const float inv = rj ? a.hdr->inv_freq[tid] : 0.f;
+    const float qa = rj ? a.q[(size_t)h * d + tid] : 0.f, qb = rj ? a.q[(size_t)h * d + tid + half] : 0.f;
+    float Mo[2] = {-INFINITY, -INFINITY}, Zo[2] = {0.f, 0.f};
+    if (warp == 0)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int b = lane + 32 * r;
+            if (b < m) {
+                Mo[r] = a.M[(size_t)h * m + b];
+                Zo[r] = a.Z[(size_t)h * m + b];
+            }
+        }
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tok_su32(sbar)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -287,94 +329,101 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
         }
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tok_su32(sbar)) : "memory");
     }
-    for (int i = tid; i < m * m; i += blockDim.x) {
-        const int aa = i / m, b = i - aa * m;
-        smu[aa * (m + 1) + b] = a.mu[(size_t)h * m * m + i];
-    }
-    for (int b = tid; b < m; b += blockDim.x) {
-        sMo[b] = a.M[(size_t)h * m + b];
-        sZo[b] = a.Z[(size_t)h * m + b];
-    }
-    {
-        const float *xs[1] = {a.q + (size_t)h * d};
-        float *dst[1] = {sq};
-        tok_rotate(a, a.hdr->pos, xs, dst, 1);
+    for (int aa = warp; aa < m; aa += 8)
+        for (int b = lane; b < m; b += 32) smu[aa * (m + 1) + b] = a.mu[((size_t)h * m + aa) * m + b];
+    if (rj) {
+        float cs, sn;
+        tok_cs(a, inv, p, cs, sn);
+        sq[tid] = qa * cs - qb * sn;
+        sq[tid + half] = qb * cs + qa * sn;
     }
     __syncthreads();   // the barrier is initialised before anyone waits on it
     tok_wait_copies(a, sbar);
-    // far insert of the evicted key (o1b_far_e / o1b_far_commit for one row)
-    // and the landmark scores, one warp per landmark
-    for (int b = warp; b < m; b += nw) {
-        float s = 0.f;
-        if (evict) {
-            for (int j = lane; j < d; j += 32) s = fmaf(sqt[b * d + j], ske[j], s);
-            s = warp_sum(s);
+    if (!evict)
+        for (int j = tid; j < d; j += blockDim.x) ske[j] = 0.f;   // no insert: its logits are unused
+    __syncthreads();
+    // partial dots per warp, lane = landmark: qt_b . k_e (the insert) and
+    // kt_b . q' (the readout)
+    for (int b0 = 0; b0 < m; b0 += 32) {
+        const int b = b0 + lane;
+        float s1[1], s2[1];
+        tok_dots(sqt, b, b < m, ske, 0, 1, d, s1);
+        tok_dots(skt, b, b < m, sq, 0, 1, d, s2);
+        if (b < m) {
+            sP[((size_t)warp * m + b) * 2] = s1[0];
+            sP[((size_t)warp * m + b) * 2 + 1] = s2[0];
         }
-        float f = 0.f;
-        for (int j = lane; j < d; j += 32) f = fmaf(sq[j], skt[b * d + j], f);
-        f = warp_sum(f);
-        if (lane == 0) {
-            const float Mo = sMo[b], Zo = sZo[b];
-            if (evict) {
-                const float l = s * a.scale;
-                const float Mn = fmaxf(Mo, l);
-                const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
-                const float e = expf(l - Mn);
-                sMn[b] = Mn;
-                sZn[b] = Zo * rho + e;
+    }
+    __syncthreads();
+    // warp 0, landmarks lane and lane + 32: the insert of the evicted key
+    // (o1b_far_e / o1b_far_commit for one row), the readout's u, gains and D
+    if (warp == 0) {
+        float f[2], Mn[2], Zn[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int b = lane + 32 * r;
+            f[r] = -INFINITY;
+            Mn[r] = -INFINITY;
+            Zn[r] = 0.f;
+            if (b < m) {
+                float s = 0.f, ff = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    s += sP[((size_t)w * m + b) * 2];
+                    ff += sP[((size_t)w * m + b) * 2 + 1];
+                }
+                f[r] = ff * a.scale;
+                float rho = 1.f, e = 0.f;
+                Mn[r] = Mo[r];
+                Zn[r] = Zo[r];
+                if (evict) {
+                    const float l = s * a.scale;
+                    Mn[r] = fmaxf(Mo[r], l);
+                    rho = (Mn[r] == Mo[r]) ? 1.f : expf(Mo[r] - Mn[r]);
+                    e = expf(l - Mn[r]);
+                    Zn[r] = Zo[r] * rho + e;
+                    a.M[(size_t)h * m + b] = Mn[r];
+                    a.Z[(size_t)h * m + b] = Zn[r];
+                }
                 sRho[b] = rho;
                 sE[b] = e;
-            } else {
-                sMn[b] = Mo;
-                sZn[b] = Zo;
-                sRho[b] = 1.f;
-                sE[b] = 0.f;
             }
-            sF[b] = f * a.scale;
         }
-    }
-    __syncthreads();
-    if (evict)
-        for (int b = tid; b < m; b += blockDim.x) {
-            a.M[(size_t)h * m + b] = sMn[b];
-            a.Z[(size_t)h * m + b] = sZn[b];
+        const float F = warp_max(fmaxf(f[0], f[1]));
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (lane + 32 * r < m) se[lane + 32 * r] = expf(f[r] - F);
+        __syncwarp();
+        float u[2] = {0.f, 0.f}, cb[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int b = lane + 32 * r;
+            if (b < m) {
+                float acc = 0.f;
+                for (int aa = 0; aa < m; ++aa) acc = fmaf(se[aa], smu[aa * (m + 1) + b], acc);
+                u[r] = a.rect ? fmaxf(acc, 0.f) : acc;
+                cb[r] = F + Mn[r];
+            }
         }
-    if (warp == 0) {
-        float mx = -INFINITY;
-        for (int aa = lane; aa < m; aa += 32) mx = fmaxf(mx, sF[aa]);
-        mx = warp_max(mx);
-        if (lane == 0) sRed[0] = mx;
-    }
-    __syncthreads();
-    const float F = sRed[0];
-    for (int aa = tid; aa < m; aa += blockDim.x) sF[aa] = expf(sF[aa] - F);
-    __syncthreads();
-    for (int b = tid; b < m; b += blockDim.x) {
-        float u = 0.f;
-        for (int aa = 0; aa < m; ++aa) u = fmaf(sF[aa], smu[aa * (m + 1) + b], u);
-        if (a.rect) u = fmaxf(u, 0.f);
-        sG[b] = u;
-        sC[b] = F + sMn[b];
-    }
-    __syncthreads();
-    if (warp == 0) {
-        float mx = -INFINITY;
-        for (int b = lane; b < m; b += 32) mx = fmaxf(mx, sC[b]);
-        mx = warp_max(mx);
+        const float cf = warp_max(fmaxf(cb[0], cb[1]));
         float D = 0.f;
-        for (int b = lane; b < m; b += 32) {
-            const float gn = sG[b] * expf(sC[b] - mx);
-            sG[b] = gn;
-            D = fmaf(gn, sZn[b], D);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int b = lane + 32 * r;
+            if (b < m) {
+                const float gn = u[r] * expf(cb[r] - cf);
+                sG[b] = gn;
+                D = fmaf(gn, Zn[r], D);
+            }
         }
         D = warp_sum(D);
         if (lane == 0) {
-            sRed[1] = mx;
-            sRed[2] = D;
+            sRed[0] = cf;
+            sRed[1] = D;
         }
     }
     __syncthreads();
-    const float cf = sRed[1], D = sRed[2];
+    const float cf = sRed[0], D = sRed[1];
     const bool have = D >= 0.f;
     // value sums: insert the evicted value, write T back, read the far numerator
     for (int t = tid; t < dv; t += blockDim.x) {
@@ -408,31 +457,31 @@ __global__ __launch_bounds__(256) void k_tok_main(O1Args a) {
     else tok_far(a, g, r - a.NC, mt, sm);
 }
 
-// Merge per (head, 64 value columns), 256 threads = 4 slice groups x 64
-// columns, in one pass over the slices with an online max (each group keeps
-// its own max, sum and value sum, combined at the end); block (0, 0) also
-// commits the row.
+// Merge per (head, 32 value columns), 256 threads = 8 slice groups x 32
+// columns, in one pass over the slices with an online max, 16 slices' loads
+// per thread in flight at once (each group keeps its own max, sum and value
+// sum, combined at the end); block (0, 0) also commits the row.
 __global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
-    __shared__ float smx[4][64], sl[4][64], sacc[4][64];
+    __shared__ float smx[8][32], sl[8][32], sacc[8][32];
     o1_wait_primary();
     const int tid = threadIdx.x;
     const int h = blockIdx.x, g = h / a.hpg, hl = h % a.hpg;
-    const int cg = tid >> 6, col = tid & 63, t = blockIdx.y * 64 + col;
-    const size_t cs = (size_t)a.hpg * (2 + a.dv);
-    const float *part = a.part + (size_t)g * a.NC * cs + (size_t)hl * (2 + a.dv);
+    const int sgp = tid >> 5, col = tid & 31, t = blockIdx.y * 32 + col;
+    const size_t base = (size_t)g * a.NC * a.hpg + hl;   // (slice c) -> base + c * hpg
     float mx = -INFINITY, l = 0.f, acc = 0.f;
-    for (int c0 = cg; c0 < a.NC; c0 += 16) {
-        float mc[4], lc[4], vc[4];
+    for (int c0 = sgp; c0 < a.NC; c0 += 8 * 16) {
+        float mc[16], lc[16], vc[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int c = c0 + 4 * u;
+        for (int u = 0; u < 16; ++u) {
+            const int c = c0 + 8 * u;
             const bool in = c < a.NC;
-            mc[u] = in ? __ldcg(part + c * cs) : -INFINITY;
-            lc[u] = in ? __ldcg(part + c * cs + 1) : 0.f;
-            vc[u] = (in && t < a.dv) ? __ldcg(part + c * cs + 2 + t) : 0.f;
+            const size_t sl_ = base + (size_t)c * a.hpg;
+            mc[u] = in ? __ldcg(a.pml + 2 * sl_) : -INFINITY;
+            lc[u] = in ? __ldcg(a.pml + 2 * sl_ + 1) : 0.f;
+            vc[u] = (in && t < a.dv) ? __ldcg(a.part + sl_ * a.dv + t) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 16; ++u) {
             if (mc[u] == -INFINITY) continue;
             const float mn = fmaxf(mx, mc[u]);
             const float fo = expf(mx - mn), fc = expf(mc[u] - mn);
@@ -441,15 +490,17 @@ __global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
             mx = mn;
         }
     }
-    smx[cg][col] = mx;
-    sl[cg][col] = l;
-    sacc[cg][col] = acc;
+    smx[sgp][col] = mx;
+    sl[sgp][col] = l;
+    sacc[sgp][col] = acc;
     __syncthreads();
-    if (cg == 0 && t < a.dv) {
-        const float M = fmaxf(fmaxf(smx[0][col], smx[1][col]), fmaxf(smx[2][col], smx[3][col]));
+    if (sgp == 0 && t < a.dv) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) M = fmaxf(M, smx[q][col]);
         float L = 0.f, A = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
             if (smx[q][col] == -INFINITY) continue;
             const float f = expf(smx[q][col] - M);
             L = fmaf(sl[q][col], f, L);
@@ -500,7 +551,7 @@ cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
     }
     k_tok_main<<<a.G * (a.NC + a.hpg), 256, tok_main_smem(a), st>>>(a);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.nh, (a.dv + 63) / 64, 1);
+    cfg.gridDim = dim3(a.nh, (a.dv + 31) / 32, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;

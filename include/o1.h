@@ -133,10 +133,37 @@ O1_API int o1_state_init(void *state, const o1_geom *geom, const int32_t *group_
  * products). It needs every rotated query, rotated key and value to lie
  * inside the fp16 range (|x| < 65504); one outside it raises
  * O1_FLAG_FP16_RANGE in the state's flags and that pass's output is not
- * valid. Other geometries, and one-row passes, run in fp32 throughout. */
+ * valid. Other geometries, and one-row calls (which take the one-row path),
+ * run in fp32 throughout. */
 O1_API int o1_chunk_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                     const float *q, const float *k, const float *v, const float *gate,
                     int32_t rows, float *out, void *stream);
+
+/* Speculative verification ("cortiq-engine 0.8.82 src/gpu_metal/o1c.rs":
+ * encode with commit = false, then spec_commit over the accepted rows).
+ *
+ * o1_chunk_attend_spec: the attention of `rows` draft rows, exactly as
+ * o1_chunk_attend would compute it (same arguments, layouts, checks and
+ * output), but the state is left as it was: no far insert, ring push, meta
+ * or position change. The draft must fit in one pass of the scratch
+ * (rows <= the max_rows the scratch was sized for), else O1_ERR_ARG. A
+ * one-row draft runs as a one-row pass of the chunk path, not the decode
+ * path. Asynchronous.
+ *
+ * o1_spec_commit: moves the state over the first `rows` accepted rows, given
+ * their keys and values again (k [rows][G][d] unrotated, v [rows][G][dv],
+ * device, 16-byte aligned; the same values the verify call was given): the
+ * rotation of the keys at the state's position, the far insert of every key
+ * they evict, the ring push, meta and position. The state afterwards equals
+ * the one o1_chunk_attend over those rows leaves, up to rounding; nothing is
+ * attended and no output is written. rows = 0 does nothing. Rows above the
+ * scratch's capacity run as several passes. Same scratch rules as
+ * o1_chunk_attend. Asynchronous. */
+O1_API int o1_chunk_attend_spec(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                                const float *q, const float *k, const float *v, const float *gate,
+                                int32_t rows, float *out, void *stream);
+O1_API int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                          const float *k, const float *v, int32_t rows, void *stream);
 
 /* One row (a decode step): the same as o1_chunk_attend with rows = 1, by a
  * path built for it ("cortiq-engine 0.8.82 src/gpu_metal/o1c.rs" encode_tok:

@@ -50,6 +50,7 @@ O1Args state_args(void *state, const o1_geom &g) {
     char *b = (char *)state;
     O1Args a;
     memset(&a, 0, sizeof(a));
+    a.commit = 1;
     a.G = g.groups;
     a.hpg = g.heads_per_group;
     a.nh = g.groups * g.heads_per_group;
@@ -97,7 +98,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
           const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream,
-          cudaEvent_t const *ev = nullptr) {
+          cudaEvent_t const *ev = nullptr, int commit = 1) {
     if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
     if (rows < 0) return O1_ERR_ARG;
     if (rows == 0) return O1_OK;
@@ -119,11 +120,15 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
         return O1_ERR_ARG;
     const int cap = scratch_cap(g, scratch_bytes);
     if (cap < 1 || scratch_bytes < o1_tok_layout(g).total) return O1_ERR_ARG;
+    // attend-only calls run as one pass: a later pass would need the state
+    // the earlier one leaves
+    if (!commit && rows > cap) return O1_ERR_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     O1Args a = state_args(state, g);
+    a.commit = commit;
     for (int r0 = 0; r0 < rows; r0 += cap) {
         const int R = rows - r0 < cap ? rows - r0 : cap;
-        if (R == 1 && !ev) {
+        if (R == 1 && !ev && commit) {
             // one row: the decode path
             const O1TokScratch T = o1_tok_layout(g);
             char *sb = (char *)scratch;
@@ -264,6 +269,41 @@ int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch, size_
         if (!events[i]) return O1_ERR_ARG;
     return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream,
                  (cudaEvent_t const *)events);
+}
+
+int o1_chunk_attend_spec(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
+                         const float *k, const float *v, const float *gate, int32_t rows, float *out,
+                         void *stream) {
+    return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream, nullptr, 0);
+}
+
+int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *k,
+                   const float *v, int32_t rows, void *stream) {
+    if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
+    if (rows < 0) return O1_ERR_ARG;
+    if (rows == 0) return O1_OK;
+    if (!state || !scratch || !k || !v) return O1_ERR_ARG;
+    if (!aligned(state, 256) || !aligned(scratch, 256) || !aligned(k, 16) || !aligned(v, 16)) return O1_ERR_ARG;
+    const o1_geom &g = *geom;
+    const int cap = scratch_cap(g, scratch_bytes);
+    if (cap < 1 || scratch_bytes < o1_tok_layout(g).total) return O1_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    O1Args a = state_args(state, g);
+    for (int r0 = 0; r0 < rows; r0 += cap) {
+        const int R = rows - r0 < cap ? rows - r0 : cap;
+        const O1Scratch S = o1_scratch_layout(g, R);
+        scratch_args(a, scratch, S);
+        a.tc = 0;   // no window attention in this pass
+        a.q = nullptr;
+        a.k = k + (size_t)r0 * g.groups * g.d;
+        a.v = v + (size_t)r0 * g.groups * g.dv;
+        a.gate = nullptr;
+        a.out = nullptr;
+        a.R = R;
+        a.nsub = S.nsub;
+        if (o1_launch_commit_pass(a, st) != cudaSuccess) return O1_ERR_CUDA;
+    }
+    return O1_OK;
 }
 
 const char *o1_stage_name(int32_t stage) {

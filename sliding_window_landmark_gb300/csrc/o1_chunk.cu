@@ -52,8 +52,8 @@ __global__ void k_rope(O1Args a) {
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
         float c = 1.f, s = 0.f;
         if (a.rotate) o1_rope_cs(a.hdr->inv_freq[j], p, c, s);
-        // 8 heads' loads ahead of their stores
-        for (int h0 = 0; h0 < a.nh; h0 += 8) {
+        // 8 heads' loads ahead of their stores (no queries in a commit pass)
+        for (int h0 = 0; a.q && h0 < a.nh; h0 += 8) {
             float x0[8], x1[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -89,12 +89,35 @@ __global__ void k_rope(O1Args a) {
     }
 }
 
-// c[i][j] += a_i . b_j over four k (both operands k-contiguous float4s)
+// 16-byte asynchronous global -> shared copies (zero-filled when !valid; src
+// must still be a valid address then), committed as groups so that the next
+// chunk lands while the current one is computed on.
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, bool valid) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// c[i][j] += a_i . b_j over four k (both operands k-contiguous float4s);
+// fma4x3_k4 for the first three columns only
 __device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+            c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
+            c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
+            c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
+            c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
+        }
+}
+__device__ __forceinline__ void fma4x3_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
             c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
             c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
             c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
@@ -121,7 +144,7 @@ constexpr int FB_LDK = 36;   // 32-wide k chunk + 4
 constexpr int FB_LDE = 68;   // E^T row stride (64 landmarks + 4)
 
 __host__ __device__ inline size_t far_block_smem_floats() {
-    return (size_t)2 * 64 * FB_LDK + 64 * 65 + 64 * FB_LDE;
+    return (size_t)4 * 64 * FB_LDK + 64 * 65 + 64 * FB_LDE;
 }
 
 template <int NV>
@@ -135,12 +158,11 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
     const int m = a.m, d = a.d, dv = a.dv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t nm = (size_t)a.nh * m;
-    float *sA = sm;                        // [64][FB_LDK] landmark chunk
-    float *sB = sA + 64 * FB_LDK;          // [64][FB_LDK] key chunk
-    float *sL = sB + 64 * FB_LDK;          // [64][65] first half's logits
+    // two stages of [landmark chunk [64][FB_LDK] | key chunk [64][FB_LDK]]
+    float *sL = sm + 4 * 64 * FB_LDK;      // [64][65] first half's logits
     float *sEt = sL + 64 * 65;             // [64 rows][FB_LDE] E, k-major
-    float *sP = sA;                        // [64][65] second half's logits (after the k loop)
-    float *sV = sA;                        // [16][dv + 4] value chunk (after the landmark loop)
+    float *sP = sm;                        // [64][65] second half's logits (after the k loop)
+                                           // then two stages of [16][dv + 4] values
     const bool any = jb < nr;
     const int nlt = (m + 31) >> 5;
     if (any) {
@@ -148,20 +170,36 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
         float acc[2][4][4];
         blk_zero(acc[0]);
         blk_zero(acc[1]);
-        for (int kc = 0; kc < d; kc += 32) {
+        auto stage = [&](int kc, float *buf) {
             for (int idx = tid; idx < 2 * 64 * 8; idx += 256) {
                 const int which = idx >> 9, row = (idx >> 3) & 63, k = kc + 4 * (idx & 7);
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *src = a.qt;
+                bool ok = false;
                 if (k < d) {
                     if (which == 0) {
-                        if (row < m) v = *(const float4 *)(a.qt + ((size_t)gh * m + row) * d + k);
+                        if (row < m) {
+                            src = a.qt + ((size_t)gh * m + row) * d + k;
+                            ok = true;
+                        }
                     } else if (row >= jb && row < nr) {
-                        v = *(const float4 *)(o1_key(a, g, r0 + row - j0, mt) + k);
+                        src = o1_key(a, g, r0 + row - j0, mt) + k;
+                        ok = true;
                     }
                 }
-                *(float4 *)((which ? sB : sA) + row * FB_LDK + 4 * (idx & 7)) = v;
+                cp_async16(buf + which * 64 * FB_LDK + row * FB_LDK + 4 * (idx & 7), src, ok);
+            }
+            cp_async_commit();
+        };
+        stage(0, sm);
+        for (int kc = 0, it = 0; kc < d; kc += 32, ++it) {
+            if (kc + 32 < d) {
+                stage(kc + 32, sm + ((it + 1) & 1) * 2 * 64 * FB_LDK);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncthreads();
+            const float *sA = sm + (it & 1) * 2 * 64 * FB_LDK, *sB = sA + 64 * FB_LDK;
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
                 const int ko = 16 * half + 4 * s4;
@@ -233,20 +271,30 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
     // t = 4 lane + 128 v + (0..3)
     float *dst = a.Tp + ((size_t)c * a.nh + gh) * m * dv;
     const int ldv = dv + 4, dv4 = dv >> 2;
+    auto stage_v = [&](int k0, float *buf) {
+        for (int idx = tid; idx < 16 * dv4; idx += 256) {
+            const int kk = idx / dv4, c4 = idx - kk * dv4, jj = k0 + kk;
+            const bool ok = jj >= jb && jj < nr;
+            cp_async16(buf + kk * ldv + 4 * c4, ok ? o1_val(a, g, r0 + jj - j0, mt) + 4 * c4 : a.qt, ok);
+        }
+        cp_async_commit();
+    };
     for (int s = 0; s < nlt; ++s) {
         float acc[4][NV][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int v = 0; v < NV; ++v) acc[i][v][0] = acc[i][v][1] = acc[i][v][2] = acc[i][v][3] = 0.f;
-        for (int k0 = 0; k0 < 64; k0 += 16) {
-            for (int idx = tid; idx < 16 * dv4; idx += 256) {
-                const int kk = idx / dv4, c4 = idx - kk * dv4, jj = k0 + kk;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (jj >= jb && jj < nr) v = ((const float4 *)o1_val(a, g, r0 + jj - j0, mt))[c4];
-                *(float4 *)(sV + kk * ldv + 4 * c4) = v;
+        stage_v(0, sm);
+        for (int k0 = 0, it = 0; k0 < 64; k0 += 16, ++it) {
+            if (k0 + 16 < 64) {
+                stage_v(k0 + 16, sm + ((it + 1) & 1) * 16 * ldv);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncthreads();
+            const float *sV = sm + (it & 1) * 16 * ldv;
 #pragma unroll 4
             for (int kk = 0; kk < 16; ++kk) {
                 const float4 e4 = *(const float4 *)(sEt + (k0 + kk) * FB_LDE + 32 * s + 4 * warp);
@@ -337,6 +385,7 @@ __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
             }
         }
     }
+    if (!a.commit) return;   // attend only: the state keeps its far field
     a.T[idx] = T;
     if (col0) {
         a.M[wid] = Mo;
@@ -373,9 +422,10 @@ constexpr int SR_LDA = 68;   // A6 row stride (64 rows + 4)
 __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
     const int nbt = (a.m + a.ns + 63) / 64;
     const int K6 = a.m + 64 + a.ns;
-    const size_t r1a = (size_t)64 * SR_LDQ * (1 + nbt), r1b = (size_t)32 * (a.dv + 4);
+    // two stages of each: score chunks, then 16-row B6 chunks
+    const size_t r1a = (size_t)2 * 64 * SR_LDQ * (1 + nbt), r1b = (size_t)2 * 16 * (a.dv + 4);
     off[0] = 0;                                              // A6 [K6][SR_LDA]
-    off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks
+    off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks (2 stages)
     off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
     off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
     off[4] = off[3] + 64 * 65;                               // F, M_c, R_c Z_{c-1}, f_c [64] each
@@ -427,31 +477,51 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             }
         }
     } else {
-        float *sQc = sR1;                    // [64][SR_LDQ]
-        float *sBc = sR1 + 64 * SR_LDQ;      // [64 nbt][SR_LDQ]
+        // two stages of [query rows [64][SR_LDQ] | landmark and sink rows [64 nbt][SR_LDQ]]
         float acc[2][4][4];
 #pragma unroll
         for (int t = 0; t < 2; ++t) blk_zero(acc[t]);
         const int nrow = 64 * (1 + nbt);
-        for (int kc = 0; kc < d; kc += 32) {
+        const bool narrow = m + ns <= 48;   // one tile, its last 16 columns unused
+        auto stage = [&](int kc, float *buf) {
             for (int idx = tid; idx < nrow * 8; idx += 256) {
                 const int row = idx >> 3, k = kc + 4 * (idx & 7);
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float *src = a.qr;
+                bool ok = false;
                 if (k < d) {
                     if (row < 64) {
-                        if (row < nr) v = *(const float4 *)(a.qr + ((size_t)(r0 + row) * nh + gh) * d + k);
+                        if (row < nr) {
+                            src = a.qr + ((size_t)(r0 + row) * nh + gh) * d + k;
+                            ok = true;
+                        }
                     } else {
                         const int col = row - 64;
                         if (col < m) {
-                            if (far_any) v = *(const float4 *)(a.kt + ((size_t)g * m + col) * d + k);
+                            if (far_any) {
+                                src = a.kt + ((size_t)g * m + col) * d + k;
+                                ok = true;
+                            }
                         } else if (col < m + ns) {
-                            v = *(const float4 *)(a.sink_k + ((size_t)g * ns + col - m) * d + k);
+                            src = a.sink_k + ((size_t)g * ns + col - m) * d + k;
+                            ok = true;
                         }
                     }
                 }
-                *(float4 *)(sR1 + row * SR_LDQ + 4 * (idx & 7)) = v;
+                cp_async16(buf + row * SR_LDQ + 4 * (idx & 7), src, ok);
+            }
+            cp_async_commit();
+        };
+        stage(0, sR1);
+        for (int kc = 0, it = 0; kc < d; kc += 32, ++it) {
+            if (kc + 32 < d) {
+                stage(kc + 32, sR1 + ((it + 1) & 1) * nrow * SR_LDQ);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncthreads();
+            const float *sQc = sR1 + (it & 1) * nrow * SR_LDQ;   // [64][SR_LDQ]
+            const float *sBc = sQc + 64 * SR_LDQ;                // [64 nbt][SR_LDQ]
 #pragma unroll 2
             for (int k4 = 0; k4 < 8; ++k4) {
                 float4 av[4], bv[4];
@@ -460,10 +530,18 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (t < nbt) {
+                        if (narrow) {
+                            // columns 48..63 are padding: three 16-column groups
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
-                        fma4x4_k4(acc[t], av, bv);
+                            for (int j = 0; j < 3; ++j)
+                                bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
+                            fma4x3_k4(acc[t], av, bv);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
+                            fma4x4_k4(acc[t], av, bv);
+                        }
                     }
                 }
             }
@@ -605,31 +683,49 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int v = 0; v < NV; ++v) acc6[i][v][0] = acc6[i][v][1] = acc6[i][v][2] = acc6[i][v][3] = 0.f;
-    for (int k0 = kbeg; k0 < K6; k0 += 32) {
-        const int kn = min(32, K6 - k0);
+    auto stage6 = [&](int k0, float *buf) {
+        const int kn = min(16, K6 - k0);
         for (int idx = tid; idx < kn * dv4; idx += 256) {
-            const int kk = idx / dv4, c4 = idx % dv4, k = k0 + kk;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int kk = idx / dv4, c4 = idx - kk * dv4, k = k0 + kk;
+            const float *src = a.qr;
+            bool ok = true;
             if (k < m) {
-                v = *(const float4 *)(Tp + (size_t)k * dv + 4 * c4);
+                src = Tp + (size_t)k * dv + 4 * c4;
             } else if (k < m + 64) {
                 const int jj = k - m, r = r0 + jj;
-                if (jj < nr && r >= j0) v = ((const float4 *)o1_val(a, g, r - j0, mt))[c4];
+                ok = jj < nr && r >= j0;
+                if (ok) src = o1_val(a, g, r - j0, mt) + 4 * c4;
             } else {
-                v = *(const float4 *)(sinks_v + (size_t)(k - m - 64) * dv + 4 * c4);
+                src = sinks_v + (size_t)(k - m - 64) * dv + 4 * c4;
             }
-            *(float4 *)(sR1 + kk * ldB + 4 * c4) = v;
+            cp_async16(buf + kk * ldB + 4 * c4, src, ok);
+        }
+        cp_async_commit();
+    };
+    if (kbeg < K6) stage6(kbeg, sR1);
+    for (int k0 = kbeg, it = 0; k0 < K6; k0 += 16, ++it) {
+        const int kn = min(16, K6 - k0);
+        if (k0 + 16 < K6) {
+            stage6(k0 + 16, sR1 + ((it + 1) & 1) * 16 * ldB);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
+        const float *sB = sR1 + (it & 1) * 16 * ldB;
+        // the in-block coefficients of the warp's rows 8 warp .. 8 warp + 7 are
+        // zero past row 8 warp + 7 (causal): those k are skipped
+        const int kskip0 = m + 8 * warp + 8, kskip1 = m + 64;
 #pragma unroll 2
         for (int kk = 0; kk < kn; ++kk) {
+            if (k0 + kk >= kskip0 && k0 + kk < kskip1) continue;
             const float4 a0 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp);
             const float4 a1 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp + 4);
             const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 const int col = 4 * lane + 128 * v;
-                const float4 bv = col < dv ? *(const float4 *)(sR1 + kk * ldB + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 bv = col < dv ? *(const float4 *)(sB + kk * ldB + col) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     acc6[i][v][0] = fmaf(ar[i], bv.x, acc6[i][v][0]);
@@ -923,6 +1019,19 @@ static size_t readout_smem(const O1Args &a) {
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
+// Dynamic shared memory above 48 KB for the kernels that take it, set once.
+static void chunk_attrs() {
+    static bool attrs_set = false;
+    if (attrs_set) return;
+    cudaFuncSetAttribute(k_side_readout<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaFuncSetAttribute(k_far_block<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    attrs_set = true;
+}
+
 namespace {
 
 // A second stream and two events per host thread and device: the far-field
@@ -960,16 +1069,7 @@ cudaError_t o1_aux(O1Aux **out) {
 // the far one on the library's second stream. With `ev`, events 2i and 2i + 1
 // are recorded just before and just after stage i on the stream it runs on.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
-    static bool attrs_set = false;
-    if (!attrs_set) {
-        cudaFuncSetAttribute(k_side_readout<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        cudaFuncSetAttribute(k_far_block<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attrs_set = true;
-    }
+    chunk_attrs();
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
     auto begin = [&](int i, cudaStream_t s) {
@@ -1025,8 +1125,27 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     end(6, st);
     begin(7, st);
     const int live = R < a.w ? R : a.w;
-    k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
+    if (a.commit) k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
     end(7, st);
+    return cudaPeekAtLastError();
+}
+
+// The state-advancing stages of a pass, without the attention: keys
+// rotated, the far insert of every key the rows evict (block partials and
+// the scan), the surviving rows into the ring, meta and position. Launched
+// on one stream; a.commit must be set and a.tc clear.
+cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
+    chunk_attrs();
+    const int R = a.R;
+    const int nblk = (R + O1_SUB - 1) / O1_SUB;
+    k_rope<<<R, 128, 0, st>>>(a);
+    const size_t fbs = far_block_smem_floats() * sizeof(float);
+    if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
+    else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
+    const size_t n = (size_t)a.nh * a.m * a.dv;
+    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    const int live = R < a.w ? R : a.w;
+    k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
     return cudaPeekAtLastError();
 }
 

@@ -187,6 +187,7 @@ struct O1Args {
     const float *q, *k, *v, *gate;
     float *out;
     int R, nsub;
+    int commit;   // 0: attend only, the state is left as it was (speculative verify)
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;
@@ -306,6 +307,10 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 // `ev` may be null; otherwise 2 * O1_NUM_STAGES events, one before and one after each stage.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);
+// The state-advancing stages alone over a.R rows whose keys and values are
+// in a.k and a.v (a.q unused): rotation of the keys, far insert, ring push,
+// meta and position.
+cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st);
 // Tensor-core window path (o1_near_tc.cu): panel gather, then the window
 // attention with the side merge and the gate.
 cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st);

@@ -68,6 +68,11 @@ def _load(path: str | None = None):
     lib.o1_chunk_attend_timed.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, ctypes.c_int32,
                                           _VP, ctypes.POINTER(_VP), ctypes.c_int32, _VP]
     lib.o1_chunk_attend_timed.restype = ctypes.c_int
+    lib.o1_chunk_attend_spec.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP,
+                                         _VP]
+    lib.o1_chunk_attend_spec.restype = ctypes.c_int
+    lib.o1_spec_commit.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, ctypes.c_int32, _VP]
+    lib.o1_spec_commit.restype = ctypes.c_int
     lib.o1_stage_name.argtypes = [ctypes.c_int32]
     lib.o1_stage_name.restype = ctypes.c_char_p
     lib.o1_token_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]
@@ -159,6 +164,25 @@ def o1_chunk_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, s
         scratch.numel() * scratch.element_size(),
         _dev(q, rows * nh * g.d, "q"), _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"),
         _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
+
+
+def o1_chunk_attend_spec(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, stream=None) -> int:
+    """Attend ``rows`` draft rows without moving the state."""
+    nh, G = g.nh, g.groups
+    return LIB.o1_chunk_attend_spec(
+        _dev(state, None, "state", dtype=None), ctypes.byref(g), _dev(scratch, None, "scratch", dtype=None),
+        scratch.numel() * scratch.element_size(),
+        _dev(q, rows * nh * g.d, "q"), _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"),
+        _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
+
+
+def o1_spec_commit(state, g: o1_geom, scratch, k, v, rows: int, stream=None) -> int:
+    """Move the state over the first ``rows`` accepted rows (their k and v)."""
+    G = g.groups
+    return LIB.o1_spec_commit(
+        _dev(state, None, "state", dtype=None), ctypes.byref(g), _dev(scratch, None, "scratch", dtype=None),
+        scratch.numel() * scratch.element_size(),
+        _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"), int(rows), _stream(stream))
 
 
 O1_NUM_STAGES = 8

@@ -83,6 +83,18 @@ def test_validation_before_any_launch(o1):
     # token path: same checks
     assert L.o1_token_attend(None, gp, aligned, 1 << 20, aligned, aligned, aligned, None, aligned,
                              None) == o1.O1_ERR_ARG
+    # speculative pair: attend-only drafts must fit one pass; commit checks its own buffers
+    assert L.o1_chunk_attend_spec(None, gp, aligned, 1 << 20, aligned, aligned, aligned, None, 4, aligned,
+                                  None) == o1.O1_ERR_ARG
+    assert L.o1_chunk_attend_spec(aligned, gp, aligned, 1 << 20, V(1 << 24), V(1 << 26), V(1 << 28), None,
+                                  1 << 16, V(1 << 30), None) == o1.O1_ERR_ARG
+    assert L.o1_spec_commit(aligned, gp, aligned, 1 << 20, aligned, aligned, 0, None) == o1.O1_OK
+    assert L.o1_spec_commit(aligned, gp, aligned, 1 << 20, aligned, aligned, -1, None) == o1.O1_ERR_ARG
+    assert L.o1_spec_commit(aligned, gp, aligned, 1 << 20, None, aligned, 4, None) == o1.O1_ERR_ARG
+    assert L.o1_spec_commit(aligned, gp, aligned, 1 << 20, aligned, V((1 << 21) + 8), 4, None) == o1.O1_ERR_ARG
+    assert L.o1_spec_commit(aligned, gp, aligned, 16, aligned, aligned, 4, None) == o1.O1_ERR_ARG
+    assert L.o1_spec_commit(aligned, ctypes.byref(bad), aligned, 1 << 20, aligned, aligned, 4,
+                            None) == o1.O1_ERR_UNSUPPORTED
     # init: bad group window, missing landmarks
     gw = (ctypes.c_int32 * 1)(17)
     assert L.o1_state_init(aligned, gp, ctypes.cast(gw, V), aligned, aligned, aligned, aligned, aligned, 0,

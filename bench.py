@@ -341,6 +341,31 @@ def our_arm(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
     d2h = host_out.numel() * 4
 
+    # ---- comparator: exact causal attention over the same 4096-row prompt
+    # (window = the prompt, no sinks, no far field) through o1_window_attend,
+    # the same window kernels, on the same rotating input sets
+    gx = o1.geom(sh.groups, sh.heads_per_group, sh.d, sh.dv, 0, ROWS, sh.landmarks, rope_base=sh.rope_base)
+    xstate = torch.empty(o1.o1_state_bytes(gx), dtype=torch.uint8, device=dev)
+    o1.check(o1.o1_state_init(xstate, gx, None, None, None, consts[2], consts[3], consts[4], 0), "init")
+    xscratch = torch.empty(o1.o1_scratch_bytes(gx, ROWS), dtype=torch.uint8, device=dev)
+
+    def x_step(i):
+        s = sets[i % N_SETS]
+        o1.check(o1.o1_window_attend(xstate, gx, xscratch, s["q"], s["k"], s["v"], s["g"], ROWS, s["out"]), "exact")
+
+    for i in range(args.warmup):
+        x_step(i)
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for i in range(args.steps):
+        x_step(args.warmup + i)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    x_ms = x0.elapsed_time(x1) / args.steps
+    x_flops = window_flops(synth.Shape(sh.groups, sh.heads_per_group, sh.d, sh.dv, 0, ROWS, sh.landmarks), ROWS)
+    del xstate, xscratch
+
     # ---- decode: 8192-row prompt (untimed), then one-row steps
     dstate = torch.empty(sbytes, dtype=torch.uint8, device=dev)
     o1.check(o1.o1_state_init(dstate, g, None, *consts, 0), "init")
@@ -451,6 +476,12 @@ def our_arm(args, rank, world, local_rank):
                        "hbm_peak_gbs": pk_["hbm_gbs"],
                        "frac_of_hbm": dec_bytes / (dec_us * 1e-6) / 1e9 / pk_["hbm_gbs"],
                        "note": "the 9.3 MB state stays in L2 across steps"},
+            "comparator": {"metric": "exact causal attention rows/s (same prompt, window = 4096, no sinks, "
+                                     "no far field)", "value": ROWS / (x_ms * 1e-3), "unit": "rows/s",
+                           "ms_per_prompt": x_ms, "sealed_ms_per_prompt": ms_max / args.steps,
+                           "algorithmic_tflops": x_flops / (x_ms * 1e-3) / 1e12,
+                           "config": "o1_window_attend over the 4096-row prompt from a fresh state, the inputs "
+                                     "rotating through the same sets as the prefill steps"},
             "speculative": {"metric": "sealed-layer speculative verify + commit us/cycle", "value": spec_us,
                             "unit": "us/cycle", "higher_is_better": False,
                             "accepted_rows_per_s": SPEC_ACC / (spec_us * 1e-6),

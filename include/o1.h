@@ -165,6 +165,22 @@ O1_API int o1_chunk_attend_spec(void *state, const o1_geom *geom, void *scratch,
 O1_API int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                           const float *k, const float *v, int32_t rows, void *stream);
 
+/* Exact sliding-window attention, the comparator of the sealed layer (the
+ * pages time the same model chunk with exact attention against the sealed
+ * layer's per-row loop; "cortiq-engine 0.8.77 src/gpu_wgpu/dory.rs",
+ * dory_score / dory_soft / dory_sum / dory_gate). Each row attends to the
+ * sinks and to the last min(group window, len + r + 1) keys of [ring, oldest
+ * first] ++ [this call's rows] ending at its own; keys that leave the window
+ * are dropped, and there is no far field. Same arguments, layouts, checks,
+ * rotation and gate as o1_chunk_attend, and the same window kernels. The
+ * state is only read (no push, no position change), so the rows must fit in
+ * one pass of the scratch, else O1_ERR_ARG. From a fresh state with a window
+ * of at least `rows`, the output is exact causal softmax attention over the
+ * sinks and every key. Asynchronous. */
+O1_API int o1_window_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
+                            const float *q, const float *k, const float *v, const float *gate,
+                            int32_t rows, float *out, void *stream);
+
 /* One row (a decode step): the same as o1_chunk_attend with rows = 1, by a
  * path built for it ("cortiq-engine 0.8.82 src/gpu_metal/o1c.rs" encode_tok:
  * near partials split across blocks, the far part, a merge, the commit).
@@ -243,6 +259,22 @@ O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host 
                                     that pass's output is incomplete      */
 #define O1_FLAG_FP16_RANGE 2u    /* an operand of the tensor-core window path
                                     was outside the fp16 range             */
+#define O1_FLAG_BACK_REFUSED 4u  /* an o1_state_back was larger than some
+                                    group could rewind; nothing was changed */
+
+/* Rewind the last `rows` ring pushes of every KV group, for looped-layer KV
+ * modes that push the same positions again ("cortiq-engine 0.8.77
+ * src/gpu_wgpu/dory.rs", dory_o1_back, applied once per row): a full ring
+ * (len == group window) steps its head back by one and forgets one eviction
+ * (farl - 1) per row; a ring not yet full drops its newest entry (len - 1).
+ * The position moves back by `rows`. Ring contents and the far field (M, Z,
+ * T) are not undone, as on the page: keys already folded into the far field
+ * stay there. A rewind some group cannot take in full (len < rows while not
+ * full, farl < rows while full) or one longer than the position is refused on
+ * the device, with nothing changed, and raises O1_FLAG_BACK_REFUSED (the
+ * state's meta lives on the device, so this call cannot see it). rows = 0
+ * does nothing. One single-thread launch; asynchronous. */
+O1_API int o1_state_back(void *state, const o1_geom *geom, int32_t rows, void *stream);
 
 /* Read the state's flags into *flags (host) and, if `clear` is non-zero,
  * reset them to 0. Synchronises `stream`. */

@@ -69,6 +69,8 @@ def load_library(path: str):
     lib.oo_rows.argtypes = [ctypes.POINTER(_Geom), ctypes.POINTER(_State), _P, _P, _P, _P,
                             ctypes.c_int32, _P, ctypes.POINTER(_Diag), ctypes.c_int32]
     lib.oo_rows.restype = ctypes.c_int32
+    lib.oo_back.argtypes = [ctypes.POINTER(_Geom), ctypes.POINTER(_State), ctypes.c_int32]
+    lib.oo_back.restype = ctypes.c_int32
     lib.oo_rope.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_float, _P, _P]
     lib.oo_rope.restype = None
     return lib
@@ -178,6 +180,11 @@ class OracleLayer:
                                                 _ptr(q), _ptr(k), _ptr(v), _ptr(gate), rows,
                                                 _ptr(out), dgp, int(threads))
         return (out, dg) if diag else out
+
+    def back(self, rows: int) -> bool:
+        """Rewind ``rows`` ring pushes (meta and position only); False, with
+        nothing changed, when a group cannot rewind that far."""
+        return self._lib.oo_back(ctypes.byref(self._g), ctypes.byref(self._st), int(rows)) == 0
 
     def snapshot(self) -> dict:
         """The mutable state, copied: meta, pos, ring, far field."""

@@ -369,3 +369,36 @@ int32_t oo_rows(const oo_geom *g, oo_state *st, const float *q, const float *k,
     free(jobs);
     return used;
 }
+
+/* Rewind `rows` pushes of every group's ring ("cortiq-engine 0.8.77
+ * src/gpu_wgpu/dory.rs", dory_o1_back, the looped-layer KV mode's rewind),
+ * one row at a time as the page does it: a full ring (len == wg) steps its
+ * head back by one and forgets one eviction (farl - 1); a ring not yet full
+ * drops its newest entry (len - 1). Ring contents and the far field (M, Z,
+ * T) are not undone, as on the page. The position moves back by `rows`.
+ * Reading where the page is silent: a rewind no group can take in full
+ * (len < rows while not full, farl < rows while full, or pos < rows) is
+ * refused before anything changes. Returns 0, or -1 when refused. */
+int32_t oo_back(const oo_geom *g, oo_state *st, int32_t rows)
+{
+    if (rows < 0 || *st->pos < rows) return -1;
+    for (int gi = 0; gi < g->groups; gi++) {
+        const int32_t *mt = st->meta + 4 * gi;
+        if (mt[0] == mt[3] ? mt[2] < rows : mt[0] < rows) return -1;
+    }
+    for (int gi = 0; gi < g->groups; gi++) {
+        int32_t *mt = st->meta + 4 * gi;
+        for (int r = 0; r < rows; r++) {
+            const int32_t wg = mt[3];
+            if (mt[0] == wg) {
+                mt[1] = (mt[1] + wg - 1) % wg;
+                mt[2] -= 1;
+            } else {
+                mt[0] -= 1;
+            }
+        }
+    }
+    *st->pos -= rows;
+    return 0;
+}
+

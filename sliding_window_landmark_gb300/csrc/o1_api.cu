@@ -98,7 +98,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
           const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream,
-          cudaEvent_t const *ev = nullptr, int commit = 1) {
+          cudaEvent_t const *ev = nullptr, int commit = 1, int exact = 0) {
     if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
     if (rows < 0) return O1_ERR_ARG;
     if (rows == 0) return O1_OK;
@@ -126,6 +126,7 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
     cudaStream_t st = (cudaStream_t)stream;
     O1Args a = state_args(state, g);
     a.commit = commit;
+    a.exact = exact;
     for (int r0 = 0; r0 < rows; r0 += cap) {
         const int R = rows - r0 < cap ? rows - r0 : cap;
         if (R == 1 && !ev && commit) {
@@ -277,6 +278,11 @@ int o1_chunk_attend_spec(void *state, const o1_geom *geom, void *scratch, size_t
     return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream, nullptr, 0);
 }
 
+int o1_window_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
+                     const float *k, const float *v, const float *gate, int32_t rows, float *out, void *stream) {
+    return chunk(state, geom, scratch, scratch_bytes, q, k, v, gate, rows, out, stream, nullptr, 0, 1);
+}
+
 int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *k,
                    const float *v, int32_t rows, void *stream) {
     if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
@@ -304,6 +310,14 @@ int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scrat
         if (o1_launch_commit_pass(a, st) != cudaSuccess) return O1_ERR_CUDA;
     }
     return O1_OK;
+}
+
+int o1_state_back(void *state, const o1_geom *geom, int32_t rows, void *stream) {
+    if (!geom_ok(geom)) return O1_ERR_UNSUPPORTED;
+    if (!state || !aligned(state, 256) || rows < 0) return O1_ERR_ARG;
+    if (rows == 0) return O1_OK;
+    const O1Args a = state_args(state, *geom);
+    return o1_launch_back(a, rows, (cudaStream_t)stream) == cudaSuccess ? O1_OK : O1_ERR_CUDA;
 }
 
 const char *o1_stage_name(int32_t stage) {

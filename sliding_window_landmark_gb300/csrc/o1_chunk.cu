@@ -443,7 +443,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     const int j0 = mt.wg - mt.len0;
     const int r0 = c * O1_SUB, nr = min(O1_SUB, a.R - r0);
     const int m = a.m, d = a.d, dv = a.dv, nh = a.nh, ns = a.ns;
-    const bool far_any = mt.farl0 + max(0, r0 + nr - j0) > 0;
+    const bool far_any = !a.exact && mt.farl0 + max(0, r0 + nr - j0) > 0;
     size_t off[6];
     side_layout(a, off);
     const int nbt = (m + ns + 63) / 64;
@@ -1089,12 +1089,14 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     cudaStreamWaitEvent(sf, aux->fork, 0);
     begin(1, sf);
     const size_t fbs = far_block_smem_floats() * sizeof(float);
-    if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
-    else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
+    if (!a.exact) {   // the comparator has no far field
+        if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
+        else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
+    }
     end(1, sf);
     begin(2, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
-    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
+    if (!a.exact) k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
     end(2, sf);
     begin(3, sf);
     if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
@@ -1168,5 +1170,37 @@ __global__ void k_init_state(O1Args a) {
 
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st) {
     k_init_state<<<304, 256, 0, st>>>(a);
+    return cudaPeekAtLastError();
+}
+
+// One thread: check that every group can rewind `rows` pushes (dory.rs
+// dory_o1_back: a full ring steps head back and farl down, a ring not yet
+// full drops its newest entry; a full ring stays full), then apply them all
+// and move the position back; otherwise change nothing and raise the flag.
+__global__ void k_back(O1Args a, int rows) {
+    bool ok = a.hdr->pos >= rows;
+    for (int g = 0; g < a.G; ++g) {
+        const uint32_t len = a.meta[g * 4 + 0], farl = a.meta[g * 4 + 2], wg = a.meta[g * 4 + 3];
+        ok = ok && (len == wg ? farl >= (uint32_t)rows : len >= (uint32_t)rows);
+    }
+    if (!ok) {
+        a.hdr->flags |= (uint32_t)O1_FLAG_BACK_REFUSED;
+        return;
+    }
+    for (int g = 0; g < a.G; ++g) {
+        uint32_t *mt = a.meta + g * 4;
+        const uint32_t wg = mt[3];
+        if (mt[0] == wg) {
+            mt[1] = (uint32_t)(((long long)mt[1] + wg - (long long)rows % wg) % wg);
+            mt[2] -= (uint32_t)rows;
+        } else {
+            mt[0] -= (uint32_t)rows;
+        }
+    }
+    a.hdr->pos -= rows;
+}
+
+cudaError_t o1_launch_back(const O1Args &a, int rows, cudaStream_t st) {
+    k_back<<<1, 1, 0, st>>>(a, rows);
     return cudaPeekAtLastError();
 }

@@ -188,6 +188,7 @@ struct O1Args {
     float *out;
     int R, nsub;
     int commit;   // 0: attend only, the state is left as it was (speculative verify)
+    int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;
@@ -307,6 +308,8 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
 // `ev` may be null; otherwise 2 * O1_NUM_STAGES events, one before and one after each stage.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);
+// Rewind `rows` ring pushes of every group (meta and position).
+cudaError_t o1_launch_back(const O1Args &a, int rows, cudaStream_t st);
 // The state-advancing stages alone over a.R rows whose keys and values are
 // in a.k and a.v (a.q unused): rotation of the keys, far insert, ring push,
 // meta and position.

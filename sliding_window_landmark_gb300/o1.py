@@ -73,6 +73,10 @@ def _load(path: str | None = None):
     lib.o1_chunk_attend_spec.restype = ctypes.c_int
     lib.o1_spec_commit.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, ctypes.c_int32, _VP]
     lib.o1_spec_commit.restype = ctypes.c_int
+    lib.o1_window_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, ctypes.c_int32, _VP, _VP]
+    lib.o1_window_attend.restype = ctypes.c_int
+    lib.o1_state_back.argtypes = [_VP, _G, ctypes.c_int32, _VP]
+    lib.o1_state_back.restype = ctypes.c_int
     lib.o1_stage_name.argtypes = [ctypes.c_int32]
     lib.o1_stage_name.restype = ctypes.c_char_p
     lib.o1_token_attend.argtypes = [_VP, _G, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]
@@ -185,6 +189,21 @@ def o1_spec_commit(state, g: o1_geom, scratch, k, v, rows: int, stream=None) -> 
         _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"), int(rows), _stream(stream))
 
 
+def o1_window_attend(state, g: o1_geom, scratch, q, k, v, gate, rows: int, out, stream=None) -> int:
+    """Exact sliding-window attention (sinks + window, no far field), attend only."""
+    nh, G = g.nh, g.groups
+    return LIB.o1_window_attend(
+        _dev(state, None, "state", dtype=None), ctypes.byref(g), _dev(scratch, None, "scratch", dtype=None),
+        scratch.numel() * scratch.element_size(),
+        _dev(q, rows * nh * g.d, "q"), _dev(k, rows * G * g.d, "k"), _dev(v, rows * G * g.dv, "v"),
+        _dev(gate, rows * nh * g.dv, "gate"), int(rows), _dev(out, rows * nh * g.dv, "out"), _stream(stream))
+
+
+def o1_state_back(state, g: o1_geom, rows: int, stream=None) -> int:
+    """Rewind the last ``rows`` ring pushes (meta and position)."""
+    return LIB.o1_state_back(_dev(state, None, "state", dtype=None), ctypes.byref(g), int(rows), _stream(stream))
+
+
 O1_NUM_STAGES = 8
 
 
@@ -263,6 +282,7 @@ def o1_state_write(state, g: o1_geom, src: dict, stream=None) -> int:
 
 O1_FLAG_WAIT_EXPIRED = 1
 O1_FLAG_FP16_RANGE = 2
+O1_FLAG_BACK_REFUSED = 4
 
 
 def o1_state_flags(state, g: o1_geom, clear: bool = False, stream=None) -> int:

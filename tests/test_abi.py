@@ -95,6 +95,17 @@ def test_validation_before_any_launch(o1):
     assert L.o1_spec_commit(aligned, gp, aligned, 16, aligned, aligned, 4, None) == o1.O1_ERR_ARG
     assert L.o1_spec_commit(aligned, ctypes.byref(bad), aligned, 1 << 20, aligned, aligned, 4,
                             None) == o1.O1_ERR_UNSUPPORTED
+    # comparator: same checks; attend-only, so one pass
+    assert L.o1_window_attend(None, gp, aligned, 1 << 20, aligned, aligned, aligned, None, 4, aligned,
+                              None) == o1.O1_ERR_ARG
+    assert L.o1_window_attend(aligned, gp, aligned, 1 << 20, V(1 << 24), V(1 << 26), V(1 << 28), None,
+                              1 << 16, V(1 << 30), None) == o1.O1_ERR_ARG
+    # rewind: checks before any launch; zero rows is a no-op
+    assert L.o1_state_back(None, gp, 1, None) == o1.O1_ERR_ARG
+    assert L.o1_state_back(V((1 << 20) + 16), gp, 1, None) == o1.O1_ERR_ARG
+    assert L.o1_state_back(aligned, gp, -1, None) == o1.O1_ERR_ARG
+    assert L.o1_state_back(aligned, gp, 0, None) == o1.O1_OK
+    assert L.o1_state_back(aligned, ctypes.byref(bad), 1, None) == o1.O1_ERR_UNSUPPORTED
     # init: bad group window, missing landmarks
     gw = (ctypes.c_int32 * 1)(17)
     assert L.o1_state_init(aligned, gp, ctypes.cast(gw, V), aligned, aligned, aligned, aligned, aligned, 0,

@@ -9,6 +9,10 @@ state the oracle has after exactly those rows, and the calls after it keep
 matching. The expected values come from two oracle runs: one over the
 committed history (advanced by the accepted rows only), and one replaying
 that history and then the whole draft.
+
+The meta rewind of looped-layer KV modes (o1_state_back; "cortiq-engine
+0.8.77 src/gpu_wgpu/dory.rs", dory_o1_back) is checked the same way against
+the oracle's rewind, including a refused rewind.
 """
 import numpy as np
 import pytest
@@ -121,4 +125,53 @@ def test_spec_draft_above_capacity_is_refused():
                                  out)
     assert st == o1.O1_ERR_ARG
     torch.cuda.synchronize()
+    assert torch.equal(gpu.state, before)
+
+
+# (shape, prompt rows, chunk rows, rewind rows)
+BACK_CASES = [
+    # ring not yet full: the rewind drops the newest entries
+    (synth.Shape(groups=2, heads_per_group=2, d=64, dv=64, sinks=4, window=256, landmarks=8), 60, 40, 40),
+    # full ring with evictions: head and eviction count step back
+    (synth.Shape(groups=2, heads_per_group=2, d=64, dv=64, sinks=4, window=48, landmarks=8), 150, 70, 30),
+    # tensor-core window, group windows of different widths
+    (synth.Shape(groups=2, heads_per_group=2, d=64, dv=64, sinks=2, window=512, landmarks=4,
+                 group_windows=(512, 384)), 700, 130, 100),
+]
+
+
+@pytest.mark.parametrize("case", range(len(BACK_CASES)))
+def test_state_back_then_repush(case):
+    """o1_state_back against the oracle's rewind (dory.rs dory_o1_back): the
+    state after the rewind, then the outputs and state of the rows pushed
+    over it, match; a rewind longer than a group can take is refused on the
+    device with nothing changed."""
+    import torch
+    from sliding_window_landmark_gb300 import o1
+    shape, prompt, n, back = BACK_CASES[case]
+    seed = 60 + case
+    c = synth.layer_constants(shape, seed)
+    orc = harness.oracle_layer(shape, c)
+    gpu = harness.GpuLayer(shape, c, max_rows=max(prompt, n))
+    q, k, v, g = synth.layer_rows(shape, seed, 0, prompt + n)
+    for a, b in ((0, prompt), (prompt, prompt + n)):
+        want, diag = orc.rows(q[a:b], k[a:b], v[a:b], g[a:b], diag=True)
+        harness.assert_outputs(gpu.rows(q[a:b], k[a:b], v[a:b], g[a:b]), want, diag, f"rows {a}..{b}")
+    assert orc.back(back)
+    o1.check(o1.o1_state_back(gpu.state, gpu.g, back), "back")
+    torch.cuda.synchronize()
+    assert o1.o1_state_flags(gpu.state, gpu.g) == 0
+    harness.assert_state(gpu.read(), orc, "after the rewind")
+    # other rows pushed over the rewound positions
+    q2, k2, v2, g2 = synth.layer_rows(shape, seed + 100, 0, back + 20)
+    want, diag = orc.rows(q2, k2, v2, g2, diag=True)
+    harness.assert_outputs(gpu.rows(q2, k2, v2, g2), want, diag, "rows after the rewind")
+    harness.assert_state(gpu.read(), orc, "after pushing again")
+    # refused: more than the position allows
+    before = gpu.state.clone()
+    too_many = int(orc.pos[0]) + 1
+    assert not orc.back(too_many)
+    o1.check(o1.o1_state_back(gpu.state, gpu.g, too_many), "back")
+    torch.cuda.synchronize()
+    assert o1.o1_state_flags(gpu.state, gpu.g, clear=True) == o1.O1_FLAG_BACK_REFUSED
     assert torch.equal(gpu.state, before)

@@ -36,6 +36,9 @@ MUTANTS = [
     ("window read from wrong slot", "int slot = (head + x) % wg;", "int slot = (head + x + 1) % wg;"),
     ("gate sign", "y = y / (1.0 + exp(-gl));", "y = y / (1.0 + exp(gl));"),
     ("attend before far insert", "if (len == wg) {\n            const double *ke", "if (0) {\n            const double *ke"),
+    ("rewind steps the head forward", "mt[1] = (mt[1] + wg - 1) % wg;", "mt[1] = (mt[1] + 1) % wg;"),
+    ("rewind keeps the eviction count", "mt[2] -= 1;", "mt[2] -= 0;"),
+    ("rewind leaves the position", "*st->pos -= rows;", "*st->pos -= 0;"),
     ("far readout uses landmark keys unscaled", "f[a] = scale * oo_dot(qr, kt + (size_t)a * d, d);",
      "f[a] = oo_dot(qr, kt + (size_t)a * d, d);"),
 ]
@@ -45,7 +48,8 @@ def _pin_calls():
     calls = [pins.test_rope_worked_values, pins.test_rope_invariants,
              pins.test_unit_kernel_closed_form, pins.test_far_state_recomputation_and_monotone_max,
              pins.test_meta_closed_form_and_ring_slots, pins.test_position_shift_invariance,
-             pins.test_forced_far_branches]
+             pins.test_forced_far_branches, pins.test_meta_rewind_closed_form,
+             pins.test_rewind_then_repush_reproduces_rows]
     calls += [lambda lib, rb=rb: pins.test_no_eviction_is_exact_softmax(rb, lib=lib) for rb in (1e6, 0.0)]
     calls += [lambda lib, c=c: pins.test_brute_force_far_algebra(c, lib=lib) for c in pins.BRUTE_CASES]
     return calls

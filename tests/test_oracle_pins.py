@@ -330,3 +330,61 @@ def test_threads_do_not_change_results(lib=None):
     np.testing.assert_array_equal(res[0][0], res[1][0])
     for key in ("meta", "ring_k", "M", "Z", "T"):
         np.testing.assert_array_equal(res[0][1][key], res[1][1][key])
+
+
+def test_meta_rewind_closed_form(lib=None):
+    """Rewinding pushes (dory.rs dory_o1_back, applied once per row): on a ring
+    not yet full, k rewinds after n pushes leave len = n - k (head, farl
+    unchanged); on a full ring after n pushes (ev = n - wg evictions), k <= ev
+    rewinds leave len = wg, farl = ev - k, head = (ev - k) mod wg; the position
+    moves back by k; ring contents and the far field are untouched; a rewind
+    some group cannot take is refused with nothing changed."""
+    sh = synth.Shape(groups=3, heads_per_group=1, d=8, dv=4, sinks=1, window=7, landmarks=2,
+                     rope_base=0.0, group_windows=(7, 3, 5))
+    lay, c, g = _layer(sh, 6, lib=lib)
+    q, k, v, _ = synth.layer_rows(sh, 6, 0, 40, gate=False)
+    lay.rows(q[:2], k[:2], v[:2])
+    # group windows 7, 3, 5 after 2 pushes: none full
+    snap = lay.snapshot()
+    assert lay.back(2)
+    for gi, wg in enumerate(sh.group_windows):
+        assert tuple(lay.meta[gi]) == (0, 0, 0, wg)
+    assert int(lay.pos[0]) == 0
+    for key in ("ring_k", "ring_v", "M", "Z", "T"):
+        np.testing.assert_array_equal(lay.snapshot()[key], snap[key])
+    # refused: a ring with fewer entries than the rewind
+    assert not lay.back(1)
+    assert int(lay.pos[0]) == 0
+    n = 23
+    lay.rows(q[:n], k[:n], v[:n])
+    for kk in (1, 3, 9):
+        before = lay.snapshot()
+        assert lay.back(kk)
+        for gi, wg in enumerate(sh.group_windows):
+            ev = n - wg
+            assert tuple(lay.meta[gi]) == (wg, (ev - kk) % wg, ev - kk, wg)
+        assert int(lay.pos[0]) == n - kk
+        for key in ("ring_k", "ring_v", "M", "Z", "T"):
+            np.testing.assert_array_equal(lay.snapshot()[key], before[key])
+        lay.rows(q[n - kk:n], k[n - kk:n], v[n - kk:n])   # push the same rows again
+    # more evictions to rewind than group 0 (window 7, 16 evictions) has
+    assert not lay.back(17)
+    for gi, wg in enumerate(sh.group_windows):
+        assert tuple(lay.meta[gi]) == (wg, (n - wg) % wg, n - wg, wg)
+
+
+def test_rewind_then_repush_reproduces_rows(lib=None):
+    """On a ring that never fills, nothing reaches the far field, so rewinding
+    n rows and pushing the same n rows again gives the same outputs and the
+    same state, exactly."""
+    sh = synth.Shape(groups=2, heads_per_group=2, d=16, dv=8, sinks=2, window=32, landmarks=3)
+    lay, c, g = _layer(sh, 8, lib=lib)
+    q, k, v, gt = synth.layer_rows(sh, 8, 0, 20)
+    lay.rows(q[:10], k[:10], v[:10], gt[:10])
+    first = lay.rows(q[10:], k[10:], v[10:], gt[10:])
+    snap = lay.snapshot()
+    assert lay.back(10)
+    again = lay.rows(q[10:], k[10:], v[10:], gt[10:])
+    np.testing.assert_array_equal(first, again)
+    for key, val in lay.snapshot().items():
+        np.testing.assert_array_equal(val, snap[key], err_msg=key)

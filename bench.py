@@ -243,6 +243,22 @@ def reference_arm(args, rank):
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The slowest rank's time: every rank runs the same replica workload,
+    so the job ends when the last one does (gloo all-reduce on the host)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(rows_per_step: int, steps: int, world: int, ms_max: float) -> float:
+    """Rows/s over all ranks: each rank processes its own rows (weak scaling)."""
+    return rows_per_step * steps * world / (ms_max * 1e-3)
+
+
 def our_arm(args, rank, world, local_rank):
     import torch
     from sliding_window_landmark_gb300 import build
@@ -307,11 +323,7 @@ def our_arm(args, rank, world, local_rank):
     stage_ms = [[evs[args.warmup + i][2 * j].elapsed_time(evs[args.warmup + i][2 * j + 1]) for j in range(nst)]
                 for i in range(args.steps)]
     stage_avg = np.mean(np.array(stage_ms), axis=0)
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world)
 
     # parity spot check of the timed output against a fresh run (same inputs)
     out0 = sets[(args.warmup + args.steps - 1) % N_SETS]["out"]
@@ -422,6 +434,23 @@ def our_arm(args, rank, world, local_rank):
     d1.record(stream)
     torch.cuda.synchronize()
     spec_us = 1e3 * d0.elapsed_time(d1) / SPEC_CYCLES
+
+    # ---- meta rewind: one-row rewinds then the same row pushed again by
+    # o1_spec_commit, as a looped layer would, in one graph
+    rk, rv = sk[:1], sv[:1]
+    rgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(rgraph, stream=cap_stream):
+            for i in range(SPEC_CYCLES):
+                o1.check(o1.o1_state_back(dstate, g, 1), "back")
+                o1.check(o1.o1_spec_commit(dstate, g, dscratch, rk, rv, 1), "commit")
+    torch.cuda.synchronize()
+    d0.record(stream)
+    rgraph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    back_us = 1e3 * d0.elapsed_time(d1) / SPEC_CYCLES
+    assert o1.o1_state_flags(dstate, g) == 0, "state flags raised"
     dec_bytes = decode_bytes(sh)
 
     # ---- roofline of the dominant kernel (the window attention)
@@ -451,8 +480,7 @@ def our_arm(args, rank, world, local_rank):
                 "algorithmic_flops_per_launch": flops, "launch_ms": near_ms}
         launches = nst - 1   # no panel gather
 
-    rows_total = ROWS * args.steps * world
-    value = rows_total / (ms_max * 1e-3)
+    value = whole_job_rate(ROWS, args.steps, world, ms_max)
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -482,6 +510,9 @@ def our_arm(args, rank, world, local_rank):
                            "algorithmic_tflops": x_flops / (x_ms * 1e-3) / 1e12,
                            "config": "o1_window_attend over the 4096-row prompt from a fresh state, the inputs "
                                      "rotating through the same sets as the prefill steps"},
+            "rewind": {"metric": "o1_state_back(1) + one-row o1_spec_commit us/pair", "value": back_us,
+                       "unit": "us/pair", "higher_is_better": False,
+                       "config": f"{SPEC_CYCLES} pairs on the decode state, captured once in a CUDA graph"},
             "speculative": {"metric": "sealed-layer speculative verify + commit us/cycle", "value": spec_us,
                             "unit": "us/cycle", "higher_is_better": False,
                             "accepted_rows_per_s": SPEC_ACC / (spec_us * 1e-6),

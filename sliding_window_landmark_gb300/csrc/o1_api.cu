@@ -94,6 +94,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.Qs = (unsigned short *)(b + S.Qs);
     a.nxp = S.nxp;
     a.tc = S.nxp > 0;
+    a.Sp = S.cap >= 2 ? (float *)(b + S.Sp) : nullptr;
 }
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,

@@ -100,29 +100,22 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// c[i][j] += a_i . b_j over four k (both operands k-contiguous float4s);
-// fma4x3_k4 for the first three columns only
-__device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
+// c[i][j] += a_i . b_j over four k (both operands k-contiguous float4s),
+// for the first NI row groups and NJ column groups
+template <int NI, int NJ>
+__device__ __forceinline__ void fma_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < NI; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
             c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
             c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
             c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
         }
 }
-__device__ __forceinline__ void fma4x3_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            c[i][j] = fmaf(av[i].x, bv[j].x, c[i][j]);
-            c[i][j] = fmaf(av[i].y, bv[j].y, c[i][j]);
-            c[i][j] = fmaf(av[i].z, bv[j].z, c[i][j]);
-            c[i][j] = fmaf(av[i].w, bv[j].w, c[i][j]);
-        }
+__device__ __forceinline__ void fma4x4_k4(float (&c)[4][4], const float4 (&av)[4], const float4 (&bv)[4]) {
+    fma_k4<4, 4>(c, av, bv);
 }
 
 // ------------------------------------------------------------- far field
@@ -483,6 +476,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         for (int t = 0; t < 2; ++t) blk_zero(acc[t]);
         const int nrow = 64 * (1 + nbt);
         const bool narrow = m + ns <= 48;   // one tile, its last 16 columns unused
+        const bool short_blk = nr <= 16;     // rows 16 .. 63 are past the pass
         auto stage = [&](int kc, float *buf) {
             for (int idx = tid; idx < nrow * 8; idx += 256) {
                 const int row = idx >> 3, k = kc + 4 * (idx & 7);
@@ -526,7 +520,9 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             for (int k4 = 0; k4 < 8; ++k4) {
                 float4 av[4], bv[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) av[i] = *(const float4 *)(sQc + (ty + 16 * i) * SR_LDQ + 4 * k4);
+                for (int i = 0; i < 4; ++i)
+                    av[i] = (i == 0 || !short_blk) ? *(const float4 *)(sQc + (ty + 16 * i) * SR_LDQ + 4 * k4)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (t < nbt) {
@@ -535,12 +531,14 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 #pragma unroll
                             for (int j = 0; j < 3; ++j)
                                 bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
-                            fma4x3_k4(acc[t], av, bv);
+                            if (short_blk) fma_k4<1, 3>(acc[t], av, bv);
+                            else fma_k4<4, 3>(acc[t], av, bv);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
                                 bv[j] = *(const float4 *)(sBc + (64 * t + tx + 16 * j) * SR_LDQ + 4 * k4);
-                            fma4x4_k4(acc[t], av, bv);
+                            if (short_blk) fma_k4<1, 4>(acc[t], av, bv);
+                            else fma_k4<4, 4>(acc[t], av, bv);
                         }
                     }
                 }
@@ -716,8 +714,9 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         // the in-block coefficients of the warp's rows 8 warp .. 8 warp + 7 are
         // zero past row 8 warp + 7 (causal): those k are skipped
         const int kskip0 = m + 8 * warp + 8, kskip1 = m + 64;
+        const int kend = 8 * warp < nr ? kn : 0;   // a warp whose rows are all past the pass skips
 #pragma unroll 2
-        for (int kk = 0; kk < kn; ++kk) {
+        for (int kk = 0; kk < kend; ++kk) {
             if (k0 + kk >= kskip0 && k0 + kk < kskip1) continue;
             const float4 a0 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp);
             const float4 a1 = *(const float4 *)(sA6 + (k0 + kk) * SR_LDA + 8 * warp + 4);
@@ -902,6 +901,201 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
     }
 }
 
+// ------------------------------------------------------- short passes
+
+// Window of a short pass (2 .. O1_SMALL_NQ / hpg rows, e.g. a speculative
+// draft): the group's keys X[xlo .. len0 + R - 1] (row 0's window start to
+// the last row's own key) split into key slices of KS, one block per
+// (slice, group) for all R x hpg query vectors at once, each a slice-local
+// softmax (max, sum, value sums); k_near_small_merge combines the slices.
+// The row-block tensor-core kernel would give one CTA per head a whole
+// window to walk. Smem: queries [nq][d], keys [KS][d], values [KS][dv],
+// scores [nq][KS + 1].
+static size_t near_small_smem(const O1Args &a, int KS) {
+    const size_t nq = (size_t)a.R * a.hpg;
+    return (nq * a.d + (size_t)KS * (a.d + a.dv) + nq * (KS + 1)) * sizeof(float);
+}
+
+__global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
+    extern __shared__ __align__(16) float sm[];
+    const int s = blockIdx.x, g = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const O1Meta mt = o1_meta(a, g);
+    const int R = a.R, hpg = a.hpg, d = a.d, dv = a.dv, nq = R * hpg;
+    const int xlo = max(0, mt.len0 + 1 - mt.wg);   // row 0's first window key
+    const int x0 = xlo + s * KS;
+    const int cnt = max(0, min(KS, mt.len0 + R - x0));
+    const size_t slot = (size_t)g * O1_SMALL_NS + s;
+    float *pv = a.Sp + slot * O1_SMALL_NQ * dv;                                          // [nq][dv]
+    float *pml = a.Sp + (size_t)a.G * O1_SMALL_NS * O1_SMALL_NQ * dv + slot * O1_SMALL_NQ * 2;   // [nq][2]
+    if (cnt == 0) {
+        for (int q = tid; q < nq; q += blockDim.x) {
+            pml[2 * q] = -INFINITY;
+            pml[2 * q + 1] = 0.f;
+        }
+        return;
+    }
+    const int ldS = KS + 1;
+    float *sQ = sm;                  // [nq][d]
+    float *sK = sQ + nq * d;         // [KS][d]
+    float *sV = sK + KS * d;         // [KS][dv]
+    float *sS = sV + KS * dv;        // [nq][ldS]
+    const int d4 = d >> 2, dv4 = dv >> 2;
+    // the pass's rotated queries of this group (query q = row q / hpg, head q % hpg)
+    for (int idx = tid; idx < nq * d4; idx += blockDim.x) {
+        const int q = idx / d4, c4 = idx - q * d4, r = q / hpg, h = q - r * hpg;
+        cp_async16(sQ + q * d + 4 * c4, a.qr + ((size_t)r * a.nh + g * hpg + h) * d + 4 * c4, true);
+    }
+    for (int idx = tid; idx < cnt * d4; idx += blockDim.x) {
+        const int i = idx / d4, c4 = idx - i * d4;
+        cp_async16(sK + i * d + 4 * c4, o1_key(a, g, x0 + i, mt) + 4 * c4, true);
+    }
+    for (int idx = tid; idx < cnt * dv4; idx += blockDim.x) {
+        const int i = idx / dv4, c4 = idx - i * dv4;
+        cp_async16(sV + i * dv + 4 * c4, o1_val(a, g, x0 + i, mt) + 4 * c4, true);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    // scores: lane = key, warp = query vectors warp, warp + 8, ...; each lane
+    // walks its key row from a lane-dependent unit, so that the 8 lanes of a
+    // quarter warp read 8 different bank groups
+    for (int k0 = 0; k0 < cnt; k0 += 32) {
+        const int i = k0 + lane;
+        const int x = x0 + i;
+        float acc[O1_SMALL_NQ / 8];
+#pragma unroll
+        for (int j = 0; j < O1_SMALL_NQ / 8; ++j) acc[j] = 0.f;
+        if (i < cnt) {
+            const float4 *kr = (const float4 *)(sK + i * d);
+            int u = lane % d4;
+            for (int t = 0; t < d4; ++t) {
+                const float4 kv = kr[u];
+#pragma unroll
+                for (int j = 0; j < O1_SMALL_NQ / 8; ++j) {
+                    const int q = warp + 8 * j;
+                    if (q < nq) {
+                        const float4 qv = ((const float4 *)(sQ + q * d))[u];
+                        acc[j] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[j]))));
+                    }
+                }
+                if (++u == d4) u = 0;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < O1_SMALL_NQ / 8; ++j) {
+            const int q = warp + 8 * j;
+            if (q < nq && i < cnt) {
+                const int r = q / hpg;
+                // row r's window: X[max(0, len0 + r + 1 - wg) .. len0 + r]
+                const bool vis = x <= mt.len0 + r && x >= mt.len0 + r + 1 - mt.wg;
+                sS[q * ldS + i] = vis ? a.scale * acc[j] : -INFINITY;
+            }
+        }
+    }
+    __syncthreads();
+    // slice-local softmax per query vector (one warp each)
+    for (int q = warp; q < nq; q += 8) {
+        float mx = -INFINITY;
+        for (int i = lane; i < cnt; i += 32) mx = fmaxf(mx, sS[q * ldS + i]);
+        mx = warp_max(mx);
+        float l = 0.f;
+        for (int i = lane; i < cnt; i += 32) {
+            const float sv = sS[q * ldS + i];
+            const float e = sv > -INFINITY ? expf(sv - mx) : 0.f;
+            sS[q * ldS + i] = e;
+            l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            pml[2 * q] = mx;
+            pml[2 * q + 1] = l;
+        }
+    }
+    __syncthreads();
+    // value sums: thread per (query vector, 4 columns)
+    for (int idx = tid; idx < nq * dv4; idx += blockDim.x) {
+        const int q = idx / dv4, c4 = idx - q * dv4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < cnt; ++i) {
+            const float w = sS[q * ldS + i];
+            const float4 v = ((const float4 *)(sV + i * dv))[c4];
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        ((float4 *)(pv + (size_t)q * dv))[c4] = acc;
+    }
+}
+
+// Combine the key slices of a short pass per (row, head, 64 columns): 256
+// threads = 4 slice groups x 64 columns, an online max over the slices, then
+// the window numerator into `out` (relative to the window max c_w) and the
+// window header (c_w, mass, c_w, 0), as the row-block window kernels write
+// them for k_merge.
+__global__ __launch_bounds__(256) void k_near_small_merge(O1Args a, int nsl) {
+    __shared__ float smx[4][64], sl[4][64], sacc[4][64];
+    const int rh = blockIdx.x, r = rh / a.nh, gh = rh - r * a.nh, g = gh / a.hpg;
+    const int q = r * a.hpg + (gh - g * a.hpg);
+    const int tid = threadIdx.x, sg = tid >> 6, col = tid & 63, t = blockIdx.y * 64 + col;
+    const float *pvb = a.Sp + (size_t)g * O1_SMALL_NS * O1_SMALL_NQ * a.dv;
+    const float *pmb = a.Sp + (size_t)a.G * O1_SMALL_NS * O1_SMALL_NQ * a.dv + (size_t)g * O1_SMALL_NS * O1_SMALL_NQ * 2;
+    float mx = -INFINITY, l = 0.f, acc = 0.f;
+    for (int c0 = sg; c0 < nsl; c0 += 4 * 8) {
+        float mc[8], lc[8], vc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = c0 + 4 * u;
+            const bool in = c < nsl;
+            const size_t sq = (size_t)c * O1_SMALL_NQ + q;
+            mc[u] = in ? pmb[2 * sq] : -INFINITY;
+            lc[u] = in ? pmb[2 * sq + 1] : 0.f;
+            vc[u] = (in && t < a.dv) ? pvb[sq * a.dv + t] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (mc[u] == -INFINITY) continue;
+            const float mn = fmaxf(mx, mc[u]);
+            const float fo = expf(mx - mn), fc = expf(mc[u] - mn);
+            l = l * fo + lc[u] * fc;
+            acc = acc * fo + vc[u] * fc;
+            mx = mn;
+        }
+    }
+    smx[sg][col] = mx;
+    sl[sg][col] = l;
+    sacc[sg][col] = acc;
+    __syncthreads();
+    if (sg == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) M = fmaxf(M, smx[u][col]);
+        float L = 0.f, A = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (smx[u][col] == -INFINITY) continue;
+            const float f = expf(smx[u][col] - M);
+            L = fmaf(sl[u][col], f, L);
+            A = fmaf(sacc[u][col], f, A);
+        }
+        if (t < a.dv) a.out[((size_t)r * a.nh + gh) * a.dv + t] = A;
+        if (blockIdx.y == 0 && col == 0) *(float4 *)(a.fh + ((size_t)r * a.nh + gh) * 4) = make_float4(M, L, M, 0.f);
+    }
+}
+
+// Host side of the short-pass window: slices of KS keys covering the widest
+// window plus the pass, at most O1_SMALL_NS per group; 0 when the pass is not
+// short or a slice would not fit in shared memory.
+static int near_small_ks(const O1Args &a) {
+    if (!a.Sp || a.R < 2 || a.R * a.hpg > O1_SMALL_NQ) return 0;
+    const int nx = a.w + a.R - 1;
+    int KS = (nx + O1_SMALL_NS - 1) / O1_SMALL_NS;
+    KS = KS < 8 ? 8 : (KS + 7) / 8 * 8;
+    if (near_small_smem(a, KS) > 227 * 1024) return 0;
+    return KS;
+}
+
 // ----------------------------------------------------------------- merge
 
 // One warp per (row, head): the window part (numerator in `out` relative to
@@ -1027,6 +1221,7 @@ static void chunk_attrs() {
     cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     cudaFuncSetAttribute(k_far_block<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    cudaFuncSetAttribute(k_near_small, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     attrs_set = true;
@@ -1068,8 +1263,11 @@ cudaError_t o1_aux(O1Aux **out) {
 // merge, commit. The two middle branches run concurrently,
 // the far one on the library's second stream. With `ev`, events 2i and 2i + 1
 // are recorded just before and just after stage i on the stream it runs on.
-cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev) {
+cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t const *ev) {
     chunk_attrs();
+    O1Args a = a_in;
+    const int KS = near_small_ks(a);   // > 0: a short pass, its window split over key slices
+    if (KS) a.tc = 0;
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
     auto begin = [&](int i, cudaStream_t s) {
@@ -1108,7 +1306,11 @@ cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *
     end(4, st);
     begin(5, st);
     if (e == cudaSuccess) {
-        if (a.tc) {
+        if (KS) {
+            const int nsl = (a.w + R - 1 + KS - 1) / KS;
+            k_near_small<<<dim3(nsl, a.G), 256, near_small_smem(a, KS), st>>>(a, KS);
+            k_near_small_merge<<<dim3(R * a.nh, (a.dv + 63) / 64), 256, 0, st>>>(a, nsl);
+        } else if (a.tc) {
             e = o1_launch_near_tc(a, st);
         } else {
             const int RB = 32 / a.hpg;

@@ -12,6 +12,10 @@
 #define O1_MAGIC 0x4C53314Fu   // "O1SL"
 #define O1_VERSION 1u
 #define O1_SUB 64              // rows of one far-field reference block
+// Short passes (R >= 2, R * hpg <= O1_SMALL_NQ query vectors): the window
+// split over at most O1_SMALL_NS key slices per group
+#define O1_SMALL_NQ 64
+#define O1_SMALL_NS 64
 // planes of the per-block far statistics (scratch Fb)
 #define O1_FB_LMAX 0
 #define O1_FB_LSUM 1
@@ -89,8 +93,10 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 // sequence as fp16 hi / lo panels (nxp keys per group, zero past the end)
 // and the rotated queries as fp16 hi / lo:
 //   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]    Qs [2][cap][nh][d]
+// and, for passes of 2 .. O1_SMALL_NQ / hpg rows, the window partials
+//   Sp  [G][O1_SMALL_NS][O1_SMALL_NQ][dv] value sums, then [..][2] (max, sum)
 struct O1Scratch {
-    size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, total;
+    size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, Sp, total;
     int cap, nsub, nxp;
 };
 
@@ -128,16 +134,29 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     S.Xk = off;  off += o1_al256(2 * G * nx * d * 2);
     S.XvT = off; off += o1_al256(2 * G * dv * nx * 2);
     S.Qs = off;  off += o1_al256(S.nxp ? 2 * c * nh * d * 2 : 0);
+    // short passes: window partials per (group, key slice, query vector),
+    // present from two rows up (a one-row pass never takes that path)
+    S.Sp = off;  off += o1_al256(cap >= 2 ? G * O1_SMALL_NS * O1_SMALL_NQ * (dv + 2) * 4 : 0);
     S.total = off;
     return S;
 }
 
+// Far blocks of the one-row path per head, each over dv / O1_TOK_FS value
+// columns (rounded up to a multiple of 4). More than one block per head
+// measured slower: each recomputes the landmark part, and the shares of T are
+// strided rows that a bulk copy cannot bring in whole.
+#define O1_TOK_FS 1
+__host__ __device__ inline int o1_tok_far_cols(int dv) { return (dv + 4 * O1_TOK_FS - 1) / (4 * O1_TOK_FS) * 4; }
+// The far record per head: (c_f, D, have, evicted, numerator [dv], M' [m], Z' [m]).
+static inline size_t o1_tok_far_stride(const o1_geom &g) { return 4 + (size_t)g.dv + 2 * (size_t)g.landmarks; }
+
 // Scratch of the one-row path: near partials per (group, key slice, head),
-// the value sums [dv] in `part` and (max, sum) in `pml`; the far part per
-// head = (c_f, D, have, -, numerator [dv]); the row's rotated key per group.
+// the value sums [dv] in `part` and (max, sum) in `pml`; the far record per
+// head; the row's rotated key per group.
 // KC keys per slice (a multiple of 8), NC slices per group, sized for the
 // longest near set (sinks + window) so that all groups' slices make about
-// one wave of 136 blocks, and capped so that a slice fits in shared memory.
+// 136 blocks (one wave with the far blocks), and capped so that a slice fits
+// in shared memory.
 struct O1TokScratch {
     size_t part, pml, farp, kcur, total;
     int KC, NC;
@@ -159,7 +178,7 @@ static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     size_t off = 0;
     S.part = off; off += o1_al256(G * S.NC * g.heads_per_group * dv * 4);
     S.pml = off;  off += o1_al256(G * S.NC * g.heads_per_group * 2 * 4);
-    S.farp = off; off += o1_al256(nh * (4 + dv) * 4);
+    S.farp = off; off += o1_al256(nh * o1_tok_far_stride(g) * 4);
     S.kcur = off; off += o1_al256(G * d * 4);
     S.total = off;
     return S;
@@ -195,6 +214,7 @@ struct O1Args {
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
     unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;
+    float *Sp;   // short-pass window partials (null when the layout has none)
     // one-row path scratch
     float *part, *pml, *farp, *kcur;
     int KC, NC;

@@ -13,8 +13,11 @@
 //      row's own rotated key and value, so the ring is not written before
 //      every block has read it), scores for every head of the group, a
 //      slice-local softmax -> partial (max, sum, value sum) per head.
-//    far blocks (one per head): the evicted key's far insert (M, Z, T in
-//      place) fused with the far readout, which reads the updated T once.
+//    far blocks (O1_TOK_FS per head, one unless configured otherwise, each
+//      over a share of the value columns): the evicted key's far insert
+//      fused with the far readout, which reads the updated T once; T is
+//      updated in place, and so are M and Z with one block per head (with
+//      several, they go through the far record to the merge).
 //  k_tok_merge  launched with programmatic dependent launch: waits for the
 //      main grid, merges the slices and the far part under one exponent
 //      (1e-30 floor), gates, and one block commits ring slot, meta and
@@ -72,8 +75,8 @@ __device__ __forceinline__ void tok_wait_copies(const O1Args &a, uint64_t *bar) 
 }
 
 static size_t tok_far_floats(const O1Args &a) {
-    const size_t m = a.m;
-    return 4 + 2 * (size_t)a.d + a.dv + 2 * m * a.d + m * (m + 1) + m * a.dv + 16 * m + 4 * m + 4;
+    const size_t m = a.m, cps = o1_tok_far_cols(a.dv);
+    return 4 + 2 * (size_t)a.d + a.dv + 2 * m * a.d + m * cps + m * (m + 1) + 16 * m + 4 * m + 4 + 256;
 }
 
 static size_t tok_main_smem(const O1Args &a) {
@@ -98,25 +101,35 @@ template <int NQ>
 __device__ __forceinline__ void tok_dots(const float *rows, int row, bool valid, const float *qs, int qstride,
                                          int nq, int d, float (&acc)[NQ]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nu = d >> 2, U = (nu + 7) >> 3;
+    const int nu = d >> 2, U = (nu + 7) >> 3;   // U <= 8 for d <= 256
     const int ub = warp * U;
 #pragma unroll
     for (int h = 0; h < NQ; ++h) acc[h] = 0.f;
     if (!valid) return;
     const float4 *kr = (const float4 *)(rows + (size_t)row * d);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the row's units first, all in flight, then each vector's
+    float4 kv[8];
+    int us[8];
     int s = lane % U;
-    for (int t = 0; t < U; ++t) {
-        const int u = ub + s;
-        if (u < nu) {
-            const float4 kv = kr[u];
 #pragma unroll
-            for (int h = 0; h < NQ; ++h) {
-                if (h >= nq) break;
-                const float4 qv = ((const float4 *)(qs + (size_t)h * qstride))[u];
-                acc[h] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[h]))));
-            }
-        }
+    for (int t = 0; t < 8; ++t) {
+        us[t] = ub + s;
+        kv[t] = (t < U && us[t] < nu) ? kr[us[t]] : z;
         if (++s == U) s = 0;
+    }
+#pragma unroll
+    for (int h = 0; h < NQ; ++h) {
+        if (h >= nq) break;
+        const float4 *qh = (const float4 *)(qs + (size_t)h * qstride);
+        float4 qv[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) qv[t] = (t < U && us[t] < nu) ? qh[us[t]] : z;
+        float a0 = 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            a0 = fmaf(qv[t].x, kv[t].x, fmaf(qv[t].y, kv[t].y, fmaf(qv[t].z, kv[t].z, fmaf(qv[t].w, kv[t].w, a0))));
+        acc[h] = a0;
     }
 }
 
@@ -273,15 +286,28 @@ __device__ void tok_near(const O1Args &a, int g, int c, const O1Meta &mt, float 
     }
 }
 
-__device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float *sm) {
+// Far split fs of head (g, hl): the insert of the evicted key and the
+// readout, with the value sums of columns [fs * cps, fs * cps + cps) only.
+// Every split computes the landmark part (scores, insert, u, gains, D) in
+// full; split 0 records c_f, D and have. With one split per head the block
+// writes the new M and Z itself; with several, split 0 puts them in the far
+// record and the merge kernel writes them once every block has read the old
+// ones.
+__device__ void tok_far(const O1Args &a, int g, int hl, int fs, const O1Meta &mt, float *sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, dv = a.dv, m = a.m;
     const int h = g * a.hpg + hl;
+    const int cps = o1_tok_far_cols(dv), t0 = fs * cps;
+    const int ncol = max(0, min(cps, dv - t0));
     const bool evict = mt.len0 == mt.wg;
     const int farl1 = mt.farl0 + (evict ? 1 : 0);
-    float *fp = a.farp + (size_t)h * (4 + dv);
-    if (farl1 == 0) {
-        for (int idx = tid; idx < 4 + dv; idx += blockDim.x) fp[idx] = idx == 0 ? -INFINITY : 0.f;
+    float *fp = a.farp + (size_t)h * (4 + dv + 2 * m);
+    if (farl1 == 0) {   // no far field: an empty record (the merge multiplies the numerator by 0)
+        for (int c = tid; c < ncol; c += blockDim.x) fp[4 + t0 + c] = 0.f;
+        if (fs == 0 && tid == 0) {
+            fp[0] = -INFINITY;
+            fp[1] = fp[2] = fp[3] = 0.f;
+        }
         return;
     }
     uint64_t *sbar = (uint64_t *)sm;   // the block's copy barrier
@@ -290,18 +316,20 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
     float *sve = ske + d;              // [dv]
     float *sqt = sve + dv;             // [m][d]  landmark queries of this head
     float *skt = sqt + m * d;          // [m][d]  landmark keys of the group
-    float *sT = skt + m * d;           // [m][dv] value sums
-    float *smu = sT + m * dv;          // [m][m + 1]
+    float *sT = skt + m * d;           // [m][cps] this split's value sums
+    float *smu = sT + m * cps;         // [m][m + 1]
     float *sP = smu + m * (m + 1);     // [8 warps][m][2] partial dots
     float *se = sP + 16 * m;           // [m] e^{f - F}
     float *sG = se + m;                // [m] gains
     float *sRho = sG + m;              // [m]
     float *sE = sRho + m;              // [m]
     float *sRed = sE + m;              // [4] c_f, D
+    float *sNum = sRed + 4;            // [256] numerator partials
 
-    // inputs first: position, frequency and query pair j = tid, the far
-    // max and mass (warp 0, landmarks lane and lane + 32), then the bulk
-    // copies of the large operands and the mixing matrix
+    // inputs first: position, frequency and query pair j = tid, the far max
+    // and mass (warp 0, landmarks lane and lane + 32), this split's value
+    // sums and the mixing matrix by plain loads, the large operands by bulk
+    // copies
     const int half = d >> 1;
     const bool rj = tid < half;
     const long long p = a.hdr->pos;
@@ -322,15 +350,40 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tok_bulk(sqt, a.qt + (size_t)h * m * d, (uint32_t)m * d * 4, sbar);
         tok_bulk(skt, a.kt + (size_t)g * m * d, (uint32_t)m * d * 4, sbar);
-        tok_bulk(sT, a.T + (size_t)h * m * dv, (uint32_t)m * dv * 4, sbar);
+        if (cps == dv) tok_bulk(sT, a.T + (size_t)h * m * dv, (uint32_t)m * dv * 4, sbar);   // all columns: one run
         if (evict) {
             tok_bulk(ske, a.ring_k + ((size_t)g * a.w + mt.head0) * d, (uint32_t)d * 4, sbar);
             tok_bulk(sve, a.ring_v + ((size_t)g * a.w + mt.head0) * dv, (uint32_t)dv * 4, sbar);
         }
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tok_su32(sbar)) : "memory");
     }
-    for (int aa = warp; aa < m; aa += 8)
-        for (int b = lane; b < m; b += 32) smu[aa * (m + 1) + b] = a.mu[((size_t)h * m + aa) * m + b];
+    // a share of T's columns and the mixing matrix by plain loads, every
+    // load issued before any store
+    if (cps != dv)
+        for (int i0 = 0; i0 < m * cps; i0 += 8 * blockDim.x) {
+            float tv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = i0 + u * blockDim.x + tid, b = idx / cps, c = idx - b * cps;
+                tv[u] = (idx < m * cps && c < ncol) ? a.T[((size_t)h * m + b) * dv + t0 + c] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u * blockDim.x + tid < m * cps) sT[i0 + u * blockDim.x + tid] = tv[u];
+        }
+    for (int i0 = 0; i0 < m * m; i0 += 8 * blockDim.x) {
+        float mv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = i0 + u * blockDim.x + tid;
+            mv[u] = idx < m * m ? a.mu[(size_t)h * m * m + idx] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = i0 + u * blockDim.x + tid, aa = idx / m;
+            if (idx < m * m) smu[aa * (m + 1) + (idx - aa * m)] = mv[u];
+        }
+    }
     if (rj) {
         float cs, sn;
         tok_cs(a, inv, p, cs, sn);
@@ -382,8 +435,14 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
                     rho = (Mn[r] == Mo[r]) ? 1.f : expf(Mo[r] - Mn[r]);
                     e = expf(l - Mn[r]);
                     Zn[r] = Zo[r] * rho + e;
-                    a.M[(size_t)h * m + b] = Mn[r];
-                    a.Z[(size_t)h * m + b] = Zn[r];
+                    if (O1_TOK_FS == 1) {
+                        // the only block of this head that reads M and Z
+                        a.M[(size_t)h * m + b] = Mn[r];
+                        a.Z[(size_t)h * m + b] = Zn[r];
+                    } else if (fs == 0) {
+                        fp[4 + dv + b] = Mn[r];
+                        fp[4 + dv + m + b] = Zn[r];
+                    }
                 }
                 sRho[b] = rho;
                 sE[b] = e;
@@ -425,36 +484,44 @@ __device__ void tok_far(const O1Args &a, int g, int hl, const O1Meta &mt, float 
     __syncthreads();
     const float cf = sRed[0], D = sRed[1];
     const bool have = D >= 0.f;
-    // value sums: insert the evicted value, write T back, read the far numerator
-    for (int t = tid; t < dv; t += blockDim.x) {
-        const float vt = evict ? sve[t] : 0.f;
+    // this split's value sums: thread = (column c, landmark group lg); insert
+    // the evicted value, write T back, partial far numerators, then their sum
+    const int nlg = blockDim.x / cps, c = tid % cps, lg = tid / cps;
+    if (lg < nlg) {
+        const float vt = (evict && c < ncol) ? sve[t0 + c] : 0.f;
         float acc = 0.f;
-        for (int b = 0; b < m; ++b) {
-            float x = sT[b * dv + t];
+        for (int b = lg; b < m; b += nlg) {
+            float x = sT[b * cps + c];
             if (evict) {
                 x = sRho[b] * x + sE[b] * vt;
-                a.T[((size_t)h * m + b) * dv + t] = x;
+                if (c < ncol) a.T[((size_t)h * m + b) * dv + t0 + c] = x;
             }
             acc = fmaf(sG[b], x, acc);
         }
-        fp[4 + t] = have ? acc : 0.f;
+        sNum[lg * cps + c] = acc;
     }
-    if (tid == 0) {
+    __syncthreads();
+    if (tid < ncol) {
+        float acc = 0.f;
+        for (int q = 0; q < nlg; ++q) acc += sNum[q * cps + tid];
+        fp[4 + t0 + tid] = have ? acc : 0.f;
+    }
+    if (fs == 0 && tid == 0) {
         fp[0] = cf;
         fp[1] = have ? D : 0.f;
         fp[2] = have ? 1.f : 0.f;
-        fp[3] = 0.f;
+        fp[3] = evict ? 1.f : 0.f;
     }
 }
 
 __global__ __launch_bounds__(256) void k_tok_main(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     o1_allow_dependents();
-    const int per = a.NC + a.hpg;
+    const int per = a.NC + a.hpg * O1_TOK_FS;
     const int g = blockIdx.x / per, r = blockIdx.x % per;
     const O1Meta mt = o1_meta(a, g);
     if (r < a.NC) tok_near(a, g, r, mt, sm);
-    else tok_far(a, g, r - a.NC, mt, sm);
+    else tok_far(a, g, (r - a.NC) / O1_TOK_FS, (r - a.NC) % O1_TOK_FS, mt, sm);
 }
 
 // Merge per (head, 32 value columns), 256 threads = 8 slice groups x 32
@@ -463,11 +530,23 @@ __global__ __launch_bounds__(256) void k_tok_main(O1Args a) {
 // sum, combined at the end); block (0, 0) also commits the row.
 __global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
     __shared__ float smx[8][32], sl[8][32], sacc[8][32];
-    o1_wait_primary();
     const int tid = threadIdx.x;
     const int h = blockIdx.x, g = h / a.hpg, hl = h % a.hpg;
     const int sgp = tid >> 5, col = tid & 31, t = blockIdx.y * 32 + col;
     const size_t base = (size_t)g * a.NC * a.hpg + hl;   // (slice c) -> base + c * hpg
+    // the gate is this call's input, not the main grid's output: read it
+    // before waiting
+    const float gl = (sgp == 0 && a.gate && t < a.dv) ? a.gate[(size_t)h * a.dv + t] : 0.f;
+    o1_wait_primary();
+    const size_t fstride = 4 + (size_t)a.dv + 2 * (size_t)a.m;
+    const float *fp = a.farp + (size_t)h * fstride;
+    float cf = -INFINITY, Df = 0.f, hv = 0.f, fnum = 0.f;
+    if (sgp == 0) {   // the far part, in the same round as the slices' partials
+        cf = __ldcg(fp);
+        Df = __ldcg(fp + 1);
+        hv = __ldcg(fp + 2);
+        fnum = t < a.dv ? __ldcg(fp + 4 + t) : 0.f;
+    }
     float mx = -INFINITY, l = 0.f, acc = 0.f;
     for (int c0 = sgp; c0 < a.NC; c0 += 8 * 16) {
         float mc[16], lc[16], vc[16];
@@ -506,16 +585,22 @@ __global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
             L = fmaf(sl[q][col], f, L);
             A = fmaf(sacc[q][col], f, A);
         }
-        const float *fp = a.farp + (size_t)h * (4 + a.dv);
-        const float cf = __ldcg(fp), Df = __ldcg(fp + 1);
-        const bool have = __ldcg(fp + 2) > 0.5f;
+        const bool have = hv > 0.5f;
         const float c = cf > -INFINITY ? fmaxf(M, cf) : M;
         const float al = expf(M - c);
         const float be = have ? expf(cf - c) : 0.f;
         const float den = fmaxf(be * Df + al * L, 1e-30f);
-        float y = (be * __ldcg(fp + 4 + t) + al * A) / den;
-        if (a.gate) y = y / (1.f + expf(-a.gate[(size_t)h * a.dv + t]));
+        float y = (be * fnum + al * A) / den;
+        if (a.gate) y = y / (1.f + expf(-gl));
         a.out[(size_t)h * a.dv + t] = y;
+    }
+    if (O1_TOK_FS > 1 && blockIdx.y == 0 && __ldcg(fp + 3) > 0.5f) {
+        // the far insert's new max and mass (written by far split 0), now
+        // that every block of the main grid has read the old ones
+        for (int b = tid; b < a.m; b += blockDim.x) {
+            a.M[(size_t)h * a.m + b] = __ldcg(fp + 4 + a.dv + b);
+            a.Z[(size_t)h * a.m + b] = __ldcg(fp + 4 + a.dv + a.m + b);
+        }
     }
     if (blockIdx.x == 0 && blockIdx.y == 0) {
         // ring push and meta for every group (o1b_ring_commit / o1b_meta, one row)
@@ -549,7 +634,7 @@ cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
         cudaFuncSetAttribute(k_tok_main, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attrs_set = true;
     }
-    k_tok_main<<<a.G * (a.NC + a.hpg), 256, tok_main_smem(a), st>>>(a);
+    k_tok_main<<<a.G * (a.NC + a.hpg * O1_TOK_FS), 256, tok_main_smem(a), st>>>(a);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.nh, (a.dv + 31) / 32, 1);
     cfg.blockDim = dim3(256, 1, 1);

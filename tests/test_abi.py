@@ -49,6 +49,15 @@ def test_sizes(o1):
         assert o1.o1_state_bytes(bad) == 0
 
 
+def test_scratch_grows_with_rows(o1):
+    """The library finds a scratch's row capacity by bisection, so the bytes
+    it needs must not shrink as rows grow."""
+    for g in (o1.geom(2, 4, 256, 256, 4, 2048, 32), o1.geom(4, 4, 128, 128, 4, 1024, 64),
+              o1.geom(1, 2, 64, 64, 4, 16, 4), o1.geom(3, 16, 72, 20, 0, 40, 1)):
+        sizes = [o1.o1_scratch_bytes(g, r) for r in list(range(1, 300)) + [1000, 4096, 4097]]
+        assert all(b >= a for a, b in zip(sizes, sizes[1:]))
+
+
 def test_validation_before_any_launch(o1):
     L = o1.LIB
     g = o1.geom(1, 2, 64, 64, 4, 16, 4)

@@ -19,8 +19,11 @@
  *
  * Conventions, for every entry point:
  *  - Ownership: the caller allocates and frees every buffer. The library
- *    never allocates device or host memory and keeps no global state; a
- *    state buffer carries its own header.
+ *    allocates no device or host memory for a call; a state buffer carries
+ *    its own header. What it keeps itself: the second CUDA stream and two
+ *    events of the chunk path (one set per host thread and device, made by
+ *    the first chunk call; see O1_NUM_STAGES) and the static scratch array of
+ *    o1_token_attend_noalloc.
  *  - Pointers: "device" pointers are CUDA global memory of the current
  *    device, "host" pointers are ordinary process memory. Device buffers must
  *    be 16-byte aligned (a torch or cudaMalloc allocation always is); the

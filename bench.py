@@ -39,6 +39,7 @@ ROWS = 4096
 DECODE_PREFILL = 8192
 DECODE_STEPS = 256
 SPEC_DRAFT, SPEC_ACC, SPEC_CYCLES = 8, 5, 64
+STACK_LAYERS, STACK_PREFILL, STACK_STEPS = 24, 1100, 32
 N_SETS = 3
 WORKLOAD = ("Qwen3.5-0.8B-shaped sealed layer: G=2 KV groups x 4 query heads, d=dv=256, 4 sinks, "
             "window 2048, 32 landmarks/head, rope base 1e6, sigmoid gate; 4096-row prompt from a fresh "
@@ -453,6 +454,53 @@ def our_arm(args, rank, world, local_rank):
     assert o1.o1_state_flags(dstate, g) == 0, "state flags raised"
     dec_bytes = decode_bytes(sh)
 
+    # ---- decode across a stack of STACK_LAYERS independent layers of the
+    # stack shape, whose states together exceed L2: each layer prefilled past
+    # its window (shared prompt rows, per-layer constants), then one-row steps
+    # through every layer in turn, captured once in a CUDA graph
+    ss = synth.STACK_LAYER
+    gs = o1.geom(ss.groups, ss.heads_per_group, ss.d, ss.dv, ss.sinks, ss.window, ss.landmarks,
+                 rope_base=ss.rope_base)
+    sscr = torch.empty(o1.o1_scratch_bytes(gs, STACK_PREFILL), dtype=torch.uint8, device=dev)
+    sp = [up(x) for x in synth.layer_rows(ss, 1000, 0, STACK_PREFILL)]
+    st_rows = [up(x) for x in synth.layer_rows(ss, 1000, STACK_PREFILL, STACK_STEPS + 2)]
+    pout = torch.empty((STACK_PREFILL, ss.nh, ss.dv), dtype=torch.float32, device=dev)
+    sstates = []
+    for layer in range(STACK_LAYERS):
+        cl = synth.layer_constants(ss, 1000 + layer)
+        cst = [up(cl.sink_k), up(cl.sink_v), up(cl.k_tilde), up(cl.q_tilde), up(cl.mu)]
+        st_ = torch.empty(o1.o1_state_bytes(gs), dtype=torch.uint8, device=dev)
+        o1.check(o1.o1_state_init(st_, gs, None, *cst, 0), "init")
+        o1.check(o1.o1_chunk_attend(st_, gs, sscr, *sp, STACK_PREFILL, pout), "prefill")
+        sstates.append(st_)
+    del sp, pout
+    sq_, sk_, sv_, sg_ = st_rows
+    sout = torch.empty((ss.nh, ss.dv), dtype=torch.float32, device=dev)
+
+    def stack_step(i):
+        for st_ in sstates:
+            o1.check(o1.o1_token_attend(st_, gs, sscr, sq_[i], sk_[i], sv_[i], sg_[i], sout), "token")
+
+    for i in range(2):
+        stack_step(STACK_STEPS + i)
+    torch.cuda.synchronize()
+    kgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(kgraph, stream=cap_stream):
+            for i in range(STACK_STEPS):
+                stack_step(i)
+    torch.cuda.synchronize()
+    d0.record(stream)
+    kgraph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    stack_us = 1e3 * d0.elapsed_time(d1) / STACK_STEPS
+    stack_bytes = STACK_LAYERS * decode_bytes(ss)
+    stack_state_mb = STACK_LAYERS * o1.o1_state_bytes(gs) / 1e6
+    for st_ in sstates:
+        assert o1.o1_state_flags(st_, gs) == 0, "state flags raised"
+    del sstates, sscr
+
     # ---- roofline of the dominant kernel (the window attention)
     pk_, src = peaks()
     names = [o1.o1_stage_name(j) for j in range(nst)]
@@ -510,6 +558,17 @@ def our_arm(args, rank, world, local_rank):
                            "algorithmic_tflops": x_flops / (x_ms * 1e-3) / 1e12,
                            "config": "o1_window_attend over the 4096-row prompt from a fresh state, the inputs "
                                      "rotating through the same sets as the prefill steps"},
+            "decode_stack": {"metric": "sealed-layer decode us per 24-layer token (stack shape, states larger than "
+                                       "L2)", "value": stack_us, "unit": "us/token", "higher_is_better": False,
+                             "config": f"{STACK_LAYERS} independent layers G=4 x 4 heads, d=dv=128, 4 sinks, "
+                                       f"window 1024, 64 landmarks, each prefilled with {STACK_PREFILL} rows; "
+                                       f"{STACK_STEPS} steps through all layers captured once in a CUDA graph",
+                             "states_mb": stack_state_mb,
+                             "gpu_launches_per_step": 2 * STACK_LAYERS,
+                             "algorithmic_bytes_per_step": stack_bytes,
+                             "achieved_gbs": stack_bytes / (stack_us * 1e-6) / 1e9,
+                             "hbm_peak_gbs": pk_["hbm_gbs"],
+                             "frac_of_hbm": stack_bytes / (stack_us * 1e-6) / 1e9 / pk_["hbm_gbs"]},
             "rewind": {"metric": "o1_state_back(1) + one-row o1_spec_commit us/pair", "value": back_us,
                        "unit": "us/pair", "higher_is_better": False,
                        "config": f"{SPEC_CYCLES} pairs on the decode state, captured once in a CUDA graph"},

@@ -64,6 +64,10 @@ WINDOW_CASES = [
     # tensor-core window kernel: full causal, then sliding after a prompt
     (synth.Shape(groups=1, heads_per_group=2, d=64, dv=64, sinks=0, window=768, landmarks=4), 0, 700),
     (synth.Shape(groups=2, heads_per_group=2, d=128, dv=64, sinks=3, window=512, landmarks=4), 600, 300),
+    # a short pass (rows x heads per group <= 64: the key-slice window path),
+    # on a tensor-core geometry and on an fp32 one
+    (synth.Shape(groups=2, heads_per_group=4, d=64, dv=64, sinks=2, window=512, landmarks=4), 700, 12),
+    (synth.Shape(groups=1, heads_per_group=2, d=32, dv=32, sinks=4, window=40, landmarks=2), 90, 5),
 ]
 
 

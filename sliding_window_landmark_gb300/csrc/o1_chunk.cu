@@ -1213,10 +1213,12 @@ static size_t readout_smem(const O1Args &a) {
 
 static size_t near_smem(const O1Args &a) { return (size_t)(32 * (a.d + 4) * 2 + 32 * (a.dv + 4)) * sizeof(float); }
 
-// Dynamic shared memory above 48 KB for the kernels that take it, set once.
+// Dynamic shared memory above 48 KB for the kernels that take it, set once
+// per device.
 static void chunk_attrs() {
-    static bool attrs_set = false;
-    if (attrs_set) return;
+    static unsigned long long done = 0;
+    unsigned long long bit = 0;
+    if (!o1_attrs_needed(&done, &bit)) return;
     cudaFuncSetAttribute(k_side_readout<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_side_readout<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
@@ -1224,7 +1226,7 @@ static void chunk_attrs() {
     cudaFuncSetAttribute(k_near_small, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    attrs_set = true;
+    o1_attrs_done(&done, bit);
 }
 
 namespace {

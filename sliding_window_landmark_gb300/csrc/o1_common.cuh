@@ -324,6 +324,24 @@ __device__ __forceinline__ void blk_zero(float (&c)[4][4]) {
         for (int j = 0; j < 4; ++j) c[i][j] = 0.f;
 }
 
+// Per-device once: a kernel's dynamic shared memory limit is a setting of the
+// current device, so each launcher keeps one bit per device (up to 64) in
+// `mask`, set after its attributes are. Two host threads racing on a
+// device's first call both set them (the setting is idempotent); none
+// launches before they are set.
+static inline bool o1_attrs_needed(const unsigned long long *mask, unsigned long long *bit) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *bit = 0;
+        return true;
+    }
+    *bit = 1ull << dev;
+    return !(__atomic_load_n(mask, __ATOMIC_ACQUIRE) & *bit);
+}
+static inline void o1_attrs_done(unsigned long long *mask, unsigned long long bit) {
+    __atomic_fetch_or(mask, bit, __ATOMIC_RELEASE);
+}
+
 // Launchers (o1_chunk.cu). Each returns cudaPeekAtLastError() after its launches.
 // `ev` may be null; otherwise 2 * O1_NUM_STAGES events, one before and one after each stage.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);

@@ -643,13 +643,14 @@ cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st) {
 }
 
 cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
-    static bool attrs_set = false;
+    static unsigned long long done = 0;
     int nslot = 0;
     const size_t smem = tc_smem(a.d, &nslot);
     const int NXp = a.nxp;
-    if (!attrs_set) {
+    unsigned long long bit = 0;
+    if (o1_attrs_needed(&done, &bit)) {
         cudaFuncSetAttribute(k_near_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attrs_set = true;
+        o1_attrs_done(&done, bit);
     }
     CUtensorMap mk, mv;
     if (!make_map(&mk, a.Xk, (uint64_t)a.d, (uint64_t)a.G * NXp, 64, TC_BN)) return cudaErrorInvalidValue;

@@ -629,10 +629,11 @@ __global__ __launch_bounds__(256) void k_tok_merge(O1Args a) {
 }
 
 cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
-    static bool attrs_set = false;
-    if (!attrs_set) {
+    static unsigned long long done = 0;
+    unsigned long long bit = 0;
+    if (o1_attrs_needed(&done, &bit)) {
         cudaFuncSetAttribute(k_tok_main, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        attrs_set = true;
+        o1_attrs_done(&done, bit);
     }
     k_tok_main<<<a.G * (a.NC + a.hpg * O1_TOK_FS), 256, tok_main_smem(a), st>>>(a);
     cudaLaunchConfig_t cfg = {};

@@ -37,6 +37,12 @@
  *    and returns O1_OK or a negative status; nothing falls back to another
  *    implementation. O1_ERR_CUDA reports a failed launch or copy
  *    (cudaPeekAtLastError / the copy's status).
+ *  - State and geometry: the state's header (magic, geometry) lives on the
+ *    device. The calls that synchronise anyway (o1_state_read, _write,
+ *    _flags) check it against `geom` and return O1_ERR_STATE on a mismatch.
+ *    The attend, commit and rewind calls do not read it back: that would
+ *    cost a device round trip per call and make them uncapturable. They
+ *    must be given the geometry the state was initialised with.
  */
 #ifndef O1_H
 #define O1_H

@@ -4,10 +4,15 @@ calls), or `--tokens` one-row calls after a prompt of `--rows` rows.
 
   python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 4096 --calls 3
   python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 8192 --tokens 16
+  python -m sliding_window_landmark_gb300.profile_run --shape qwen --rows 8192 --spec 8,5 --cycles 3
 
 Launches per chunk call: rope, then far_block, far_tscan, side_readout on a
 second stream beside [gather_tc], near, then merge, commit;
-per one-row call: k_tok_main, k_tok_merge. The library must already be built.
+per one-row call: k_tok_main, k_tok_merge; per speculative cycle (`--spec
+DRAFT,ACCEPTED`): the attend-only pass of the draft (no commit kernel; the
+key-slice window kernels for a short draft), then the commit pass of the
+accepted rows (rope, far_block, far_tscan, commit). The library must already
+be built.
 """
 from __future__ import annotations
 
@@ -29,6 +34,8 @@ def main():
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0)
     ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--spec", default="", help="DRAFT,ACCEPTED rows of speculative cycles after the prompt")
+    ap.add_argument("--cycles", type=int, default=3)
     args = ap.parse_args()
     sh = SHAPES[args.shape]
     dev = torch.device("cuda")
@@ -43,7 +50,17 @@ def main():
     scratch = torch.empty(o1.o1_scratch_bytes(g, args.rows), dtype=torch.uint8, device=dev)
     q, k, v, gt = (up(x) for x in synth.layer_rows(sh, args.seed, 0, args.rows))
     out = torch.empty((args.rows, sh.nh, sh.dv), dtype=torch.float32, device=dev)
-    if args.tokens:
+    if args.spec:
+        nd, na = (int(x) for x in args.spec.split(","))
+        o1.check(o1.o1_chunk_attend(state, g, scratch, q, k, v, gt, args.rows, out), "prompt")
+        sq, sk, sv, sg = (up(x) for x in synth.layer_rows(sh, args.seed, args.rows, nd * args.cycles))
+        sout = torch.empty((nd, sh.nh, sh.dv), dtype=torch.float32, device=dev)
+        for i in range(args.cycles):
+            a, b = i * nd, (i + 1) * nd
+            o1.check(o1.o1_chunk_attend_spec(state, g, scratch, sq[a:b], sk[a:b], sv[a:b], sg[a:b], nd, sout), "spec")
+            o1.check(o1.o1_spec_commit(state, g, scratch, sk[a:a + na], sv[a:a + na], na), "commit")
+        out = sout
+    elif args.tokens:
         o1.check(o1.o1_chunk_attend(state, g, scratch, q, k, v, gt, args.rows, out), "prompt")
         tq, tk, tv, tg = (up(x) for x in synth.layer_rows(sh, args.seed, args.rows, args.tokens))
         tout = torch.empty((args.tokens, sh.nh, sh.dv), dtype=torch.float32, device=dev)

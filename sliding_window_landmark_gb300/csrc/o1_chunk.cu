@@ -905,21 +905,39 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
 
 // Window of a short pass (2 .. O1_SMALL_NQ / hpg rows, e.g. a speculative
 // draft): the group's keys X[xlo .. len0 + R - 1] (row 0's window start to
-// the last row's own key) split into key slices of KS, one block per
+// the last row's own key) split into key slices of KS <= 64, one block per
 // (slice, group) for all R x hpg query vectors at once, each a slice-local
 // softmax (max, sum, value sums); k_near_small_merge combines the slices.
 // The row-block tensor-core kernel would give one CTA per head a whole
-// window to walk. Smem: queries [nq][d], keys [KS][d], values [KS][dv],
-// scores [nq][KS + 1].
+// window to walk. Register-tiled: queries and keys k-contiguous in padded
+// rows, the 64 x 64 score tile as 4 x 4 per thread over float4 k steps (only
+// the query row groups the pass has), P.V as 16 query rows x 4 columns per
+// thread. Smem: queries [64][d + 4], keys [64][d + 4], values [64][dv + 4],
+// scores [64][65].
+constexpr int NS_LD = 65;
 static size_t near_small_smem(const O1Args &a, int KS) {
-    const size_t nq = (size_t)a.R * a.hpg;
-    return (nq * a.d + (size_t)KS * (a.d + a.dv) + nq * (KS + 1)) * sizeof(float);
+    (void)KS;
+    return ((size_t)128 * (a.d + 4) + (size_t)64 * (a.dv + 4) + 64 * NS_LD) * sizeof(float);
+}
+
+template <int NI>
+__device__ __forceinline__ void ns_scores(float (&c)[4][4], const float *sQ, const float *sK, int ld, int d4) {
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+    for (int k4 = 0; k4 < d4; ++k4) {
+        float4 av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) av[i] = *(const float4 *)(sQ + (ty + 16 * i) * ld + 4 * k4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = *(const float4 *)(sK + (tx + 16 * j) * ld + 4 * k4);
+        fma_k4<NI, 4>(c, av, bv);
+    }
 }
 
 __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
     extern __shared__ __align__(16) float sm[];
     const int s = blockIdx.x, g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = tid >> 4, tx = tid & 15;
     const O1Meta mt = o1_meta(a, g);
     const int R = a.R, hpg = a.hpg, d = a.d, dv = a.dv, nq = R * hpg;
     const int xlo = max(0, mt.len0 + 1 - mt.wg);   // row 0's first window key
@@ -935,97 +953,97 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
         }
         return;
     }
-    const int ldS = KS + 1;
-    float *sQ = sm;                  // [nq][d]
-    float *sK = sQ + nq * d;         // [KS][d]
-    float *sV = sK + KS * d;         // [KS][dv]
-    float *sS = sV + KS * dv;        // [nq][ldS]
-    const int d4 = d >> 2, dv4 = dv >> 2;
-    // the pass's rotated queries of this group (query q = row q / hpg, head q % hpg)
-    for (int idx = tid; idx < nq * d4; idx += blockDim.x) {
+    const int ld = d + 4, ldv = dv + 4, d4 = d >> 2, dv4 = dv >> 2;
+    const int ngi = (nq + 15) >> 4;   // query row groups of 16 in use
+    float *sQ = sm;                   // [64][ld]
+    float *sK = sQ + 64 * ld;         // [64][ld]
+    float *sV = sK + 64 * ld;         // [64][ldv]
+    float *sS = sV + 64 * ldv;        // [64][NS_LD]
+    // the pass's rotated queries of this group (query q = row q / hpg, head
+    // q % hpg; rows up to 16 ngi, the ones past nq zero) and the slice's keys
+    // and values (the 64 rows, the ones past cnt zero)
+    for (int idx = tid; idx < 16 * ngi * d4; idx += blockDim.x) {
         const int q = idx / d4, c4 = idx - q * d4, r = q / hpg, h = q - r * hpg;
-        cp_async16(sQ + q * d + 4 * c4, a.qr + ((size_t)r * a.nh + g * hpg + h) * d + 4 * c4, true);
+        const bool ok = q < nq;
+        cp_async16(sQ + q * ld + 4 * c4, ok ? a.qr + ((size_t)r * a.nh + g * hpg + h) * d + 4 * c4 : a.qr, ok);
     }
-    for (int idx = tid; idx < cnt * d4; idx += blockDim.x) {
+    for (int idx = tid; idx < 64 * d4; idx += blockDim.x) {
         const int i = idx / d4, c4 = idx - i * d4;
-        cp_async16(sK + i * d + 4 * c4, o1_key(a, g, x0 + i, mt) + 4 * c4, true);
+        const bool ok = i < cnt;
+        cp_async16(sK + i * ld + 4 * c4, ok ? o1_key(a, g, x0 + i, mt) + 4 * c4 : a.qr, ok);
     }
-    for (int idx = tid; idx < cnt * dv4; idx += blockDim.x) {
+    for (int idx = tid; idx < 64 * dv4; idx += blockDim.x) {
         const int i = idx / dv4, c4 = idx - i * dv4;
-        cp_async16(sV + i * dv + 4 * c4, o1_val(a, g, x0 + i, mt) + 4 * c4, true);
+        const bool ok = i < cnt;
+        cp_async16(sV + i * ldv + 4 * c4, ok ? o1_val(a, g, x0 + i, mt) + 4 * c4 : a.qr, ok);
     }
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
-    // scores: lane = key, warp = query vectors warp, warp + 8, ...; each lane
-    // walks its key row from a lane-dependent unit, so that the 8 lanes of a
-    // quarter warp read 8 different bank groups
-    for (int k0 = 0; k0 < cnt; k0 += 32) {
-        const int i = k0 + lane;
-        const int x = x0 + i;
-        float acc[O1_SMALL_NQ / 8];
-#pragma unroll
-        for (int j = 0; j < O1_SMALL_NQ / 8; ++j) acc[j] = 0.f;
-        if (i < cnt) {
-            const float4 *kr = (const float4 *)(sK + i * d);
-            int u = lane % d4;
-            for (int t = 0; t < d4; ++t) {
-                const float4 kv = kr[u];
-#pragma unroll
-                for (int j = 0; j < O1_SMALL_NQ / 8; ++j) {
-                    const int q = warp + 8 * j;
-                    if (q < nq) {
-                        const float4 qv = ((const float4 *)(sQ + q * d))[u];
-                        acc[j] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[j]))));
-                    }
-                }
-                if (++u == d4) u = 0;
-            }
+    // scores, masked to each query row's window, into sS
+    {
+        float c[4][4];
+        blk_zero(c);
+        switch (ngi) {
+            case 1: ns_scores<1>(c, sQ, sK, ld, d4); break;
+            case 2: ns_scores<2>(c, sQ, sK, ld, d4); break;
+            case 3: ns_scores<3>(c, sQ, sK, ld, d4); break;
+            default: ns_scores<4>(c, sQ, sK, ld, d4); break;
         }
 #pragma unroll
-        for (int j = 0; j < O1_SMALL_NQ / 8; ++j) {
-            const int q = warp + 8 * j;
-            if (q < nq && i < cnt) {
-                const int r = q / hpg;
+        for (int i = 0; i < 4; ++i) {
+            const int q = ty + 16 * i;
+            if (i >= ngi || q >= nq) continue;
+            const int r = q / hpg;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int key = tx + 16 * j, x = x0 + key;
                 // row r's window: X[max(0, len0 + r + 1 - wg) .. len0 + r]
-                const bool vis = x <= mt.len0 + r && x >= mt.len0 + r + 1 - mt.wg;
-                sS[q * ldS + i] = vis ? a.scale * acc[j] : -INFINITY;
+                const bool vis = key < cnt && x <= mt.len0 + r && x >= mt.len0 + r + 1 - mt.wg;
+                sS[q * NS_LD + key] = vis ? a.scale * c[i][j] : -INFINITY;
             }
         }
     }
     __syncthreads();
-    // slice-local softmax per query vector (one warp each)
+    // slice-local softmax per query vector (one warp each; keys lane, lane + 32)
     for (int q = warp; q < nq; q += 8) {
-        float mx = -INFINITY;
-        for (int i = lane; i < cnt; i += 32) mx = fmaxf(mx, sS[q * ldS + i]);
-        mx = warp_max(mx);
-        float l = 0.f;
-        for (int i = lane; i < cnt; i += 32) {
-            const float sv = sS[q * ldS + i];
-            const float e = sv > -INFINITY ? expf(sv - mx) : 0.f;
-            sS[q * ldS + i] = e;
-            l += e;
-        }
-        l = warp_sum(l);
+        const float s0 = sS[q * NS_LD + lane], s1 = sS[q * NS_LD + lane + 32];
+        const float mx = warp_max(fmaxf(s0, s1));
+        const float e0 = s0 > -INFINITY ? expf(s0 - mx) : 0.f, e1 = s1 > -INFINITY ? expf(s1 - mx) : 0.f;
+        sS[q * NS_LD + lane] = e0;
+        sS[q * NS_LD + lane + 32] = e1;
+        const float l = warp_sum(e0 + e1);
         if (lane == 0) {
             pml[2 * q] = mx;
             pml[2 * q + 1] = l;
         }
     }
     __syncthreads();
-    // value sums: thread per (query vector, 4 columns)
-    for (int idx = tid; idx < nq * dv4; idx += blockDim.x) {
-        const int q = idx / dv4, c4 = idx - q * dv4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < cnt; ++i) {
-            const float w = sS[q * ldS + i];
-            const float4 v = ((const float4 *)(sV + i * dv))[c4];
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+    // value sums: thread = (group of 16 query rows, 4 columns), 64 accumulators
+    {
+        const int qg = tid >> 6, c4 = tid & 63;
+        if (qg < ngi && c4 < dv4) {
+            float acc[16][4];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            for (int key = 0; key < cnt; ++key) {
+                const float4 v = *(const float4 *)(sV + key * ldv + 4 * c4);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float w = sS[(16 * qg + i) * NS_LD + key];
+                    acc[i][0] = fmaf(w, v.x, acc[i][0]);
+                    acc[i][1] = fmaf(w, v.y, acc[i][1]);
+                    acc[i][2] = fmaf(w, v.z, acc[i][2]);
+                    acc[i][3] = fmaf(w, v.w, acc[i][3]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int q = 16 * qg + i;
+                if (q < nq)
+                    *(float4 *)(pv + (size_t)q * dv + 4 * c4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            }
         }
-        ((float4 *)(pv + (size_t)q * dv))[c4] = acc;
     }
 }
 
@@ -1085,14 +1103,15 @@ __global__ __launch_bounds__(256) void k_near_small_merge(O1Args a, int nsl) {
 }
 
 // Host side of the short-pass window: slices of KS keys covering the widest
-// window plus the pass, at most O1_SMALL_NS per group; 0 when the pass is not
-// short or a slice would not fit in shared memory.
+// window plus the pass, at most O1_SMALL_NS per group and at most 64 keys
+// each (windows up to about 4 k keys); 0 when the pass is not short or the
+// window too long, and the row-block window kernels take it.
 static int near_small_ks(const O1Args &a) {
     if (!a.Sp || a.R < 2 || a.R * a.hpg > O1_SMALL_NQ) return 0;
     const int nx = a.w + a.R - 1;
     int KS = (nx + O1_SMALL_NS - 1) / O1_SMALL_NS;
     KS = KS < 8 ? 8 : (KS + 7) / 8 * 8;
-    if (near_small_smem(a, KS) > 227 * 1024) return 0;
+    if (KS > 64 || near_small_smem(a, KS) > 227 * 1024) return 0;   // a slice is one 64-key score tile
     return KS;
 }
 

@@ -10,7 +10,11 @@ each step's inputs out of L2 (their total is well above the 129 MB L2).
 
 Prints one JSON line: prefill rows/s (whole job over all ranks), the dominant
 kernel against its roofline, the oracle on the host cores, the end-to-end
-rate with host buffers, decode us/token after an 8192-row prompt, clocks.
+rate with host buffers, clocks, and beside them: decode us/token after an
+8192-row prompt (`decode`) and across a 24-layer stack whose states exceed
+L2 (`decode_stack`), both against HBM; exact causal attention over the same
+prompt (`comparator`); speculative verify + commit cycles (`speculative`);
+ring rewinds (`rewind`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """

@@ -41,6 +41,9 @@ MUTANTS = [
     ("rewind leaves the position", "*st->pos -= rows;", "*st->pos -= 0;"),
     ("far readout uses landmark keys unscaled", "f[a] = scale * oo_dot(qr, kt + (size_t)a * d, d);",
      "f[a] = oo_dot(qr, kt + (size_t)a * d, d);"),
+    ("denominator floor dropped", "if (den < 1e-30) den = 1e-30;", "(void)0;"),
+    ("floor taken before the far mass is added", "if (den < 1e-30) den = 1e-30;",
+     "den = (den - D < 1e-30 ? 1e-30 : den - D) + D;"),
 ]
 
 
@@ -52,6 +55,7 @@ def _pin_calls():
              pins.test_rewind_then_repush_reproduces_rows]
     calls += [lambda lib, rb=rb: pins.test_no_eviction_is_exact_softmax(rb, lib=lib) for rb in (1e6, 0.0)]
     calls += [lambda lib, c=c: pins.test_brute_force_far_algebra(c, lib=lib) for c in pins.BRUTE_CASES]
+    calls += [lambda lib, mv=mv: pins.test_denominator_floor(mv, lib=lib) for mv in pins.FLOOR_CASES]
     return calls
 
 

@@ -319,6 +319,65 @@ def test_forced_far_branches(lib=None):
                     assert (D[r, h] == 0.0) if rect else (D[r, h] < 0.0)
 
 
+def _floor_layer(mu_value, lib=None):
+    """One group, one head, one landmark, window 2, rotation off. Every key
+    is e0 and the landmark query is 400 e0, so an evicted key's far logit is
+    l = scale * 400 (about 141) while every near score stays below 1: once a
+    key is evicted the far max F + M dominates the row's exponent c by more
+    than 100, every near weight e^{s - c} is below e^-140, and the
+    denominator meets the 1e-30 floor unless the far mass carries it.
+    The landmark key is zero (F = 0) and mu = mu_value."""
+    sh = synth.Shape(groups=1, heads_per_group=1, d=8, dv=4, sinks=1, window=2, landmarks=1, rope_base=0.0)
+    c = synth.layer_constants(sh, 17)
+    c.sink_k[:] = 0.0
+    c.k_tilde[:] = 0.0
+    c.q_tilde[:] = 0.0
+    c.q_tilde[0, 0, 0, 0] = 400.0
+    c.mu[:] = np.float32(mu_value)
+    lay, _, g = _layer(sh, 17, consts=c, lib=lib)
+    rows = 5
+    q, _, v, _ = synth.layer_rows(sh, 17, 0, rows, gate=False)
+    q = (0.1 * q).astype(np.float32)
+    k = np.zeros((rows, 1, 8), dtype=np.float32)
+    k[:, 0, 0] = 1.0
+    return sh, c, g, lay, q, k, v
+
+
+FLOOR_CASES = [3e-31, 4e-30, -1.0]
+
+
+@pytest.mark.parametrize("mu_value", FLOOR_CASES)
+def test_denominator_floor(mu_value, lib=None):
+    """The 1e-30 floor on the denominator (o1_batch.rs o1b_attend; dory.rs
+    dory_osoft), taken in the units where the row's largest exponent is 0.
+    With the far max dominating (see _floor_layer), after n evictions the far
+    field holds M = l, Z = n, T = v_0 + ... + v_{n-1} exactly (every logit is
+    equal), the gain is mu, and the near terms are below e^-140:
+      mu > 0: out = mu T / max(mu Z, 1e-30): the evicted values' sum scaled
+              by mu / 1e-30 while mu Z < 1e-30 (3e-31: a floored
+              denominator), their mean once mu Z > 1e-30 (4e-30);
+      mu < 0: the far part is dropped but its max still sets the exponent,
+              so out = sum_x e^{s_x - l} v_x / 1e-30, about 1e-31 |v|."""
+    sh, c, g, lay, q, k, v = _floor_layer(mu_value, lib=lib)
+    got = lay.rows(q, k, v, None)
+    scale = g.scale_f32()
+    l = scale * 400.0
+    mu = float(np.float32(mu_value))
+    for r in range(2, 5):
+        n = r - 1   # keys 0 .. r - 2 evicted
+        if mu > 0:
+            T = v[:n, 0].astype(np.float64).sum(axis=0)
+            want = mu * T / max(mu * n, 1e-30)
+            np.testing.assert_allclose(got[r, 0], want, rtol=1e-9, atol=0)
+        else:
+            keys = np.concatenate([c.sink_k[0].astype(np.float64), k[r - 1:r + 1, 0].astype(np.float64)])
+            vals = np.concatenate([c.sink_v[0].astype(np.float64), v[r - 1:r + 1, 0].astype(np.float64)])
+            s = scale * keys @ q[r, 0].astype(np.float64)
+            want = np.exp(s - l) @ vals / 1e-30
+            np.testing.assert_allclose(got[r, 0], want, rtol=1e-9, atol=0)
+            assert 0 < np.abs(want).max() < 1e-29
+
+
 def test_threads_do_not_change_results(lib=None):
     sh = synth.Shape(groups=3, heads_per_group=2, d=16, dv=8, sinks=2, window=6, landmarks=3,
                      group_windows=(6, 4, 5))

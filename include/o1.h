@@ -99,12 +99,23 @@ typedef struct o1_state_host {
 } o1_state_host;
 
 /* Bytes of device memory a state of this geometry needs (0 if the geometry is
- * outside the limits). Host-only; no CUDA call. */
+ * outside the limits). Host-only; no CUDA call.
+ * The state holds the buffers of one sealed layer that "cortiq-engine 0.8.51
+ * src/gpu_wgpu/o1_batch.rs" lists in struct State (meta, ring_k, ring_v,
+ * sink_k, sink_v, k_tilde, qt, mu, the far max and mass mz, the far value
+ * sum that), sized from struct Geom, plus a header of this library's
+ * (magic, geometry, position, rotary frequencies, flags). */
 O1_API size_t o1_state_bytes(const o1_geom *geom);
 
 /* Bytes of device scratch that lets one o1_chunk_attend launch process up to
  * `max_rows` rows in one pass (longer calls run in passes of that many rows).
- * 0 if the geometry is unsupported or max_rows < 1. Host-only. */
+ * 0 if the geometry is unsupported or max_rows < 1. Host-only.
+ * The pages size a per-call scratch from the geometry ("cortiq-engine 0.8.51
+ * src/gpu_wgpu/o1_batch.rs", Geom::scratch_len: the far-field exponents and
+ * prefixes of one 64-row sub-chunk plus a max and a rescale per head and
+ * landmark). This library runs every 64-row block of a pass at once, so its
+ * scratch holds those planes for all of them, plus the rotated rows, the
+ * window and side partials and, on the tensor-core path, fp16 panels. */
 O1_API size_t o1_scratch_bytes(const o1_geom *geom, int32_t max_rows);
 
 /* Start a sealed layer from an empty ring and far field ("cortiq-engine
@@ -225,7 +236,11 @@ O1_API int o1_chunk_attend_timed(void *state, const o1_geom *geom, void *scratch
                                  int32_t rows, float *out, void *const *events, int32_t n_events,
                                  void *stream);
 
-/* Name of stage i of a chunk pass (NULL outside [0, O1_NUM_STAGES)). */
+/* Name of stage i of a chunk pass (NULL outside [0, O1_NUM_STAGES)). The
+ * pages time a forward stage by stage by keeping only some dispatch kinds
+ * ("cortiq-engine 0.8.77 src/gpu_wgpu/dory.rs", the keep-one stage table);
+ * here each stage records events around itself instead, and every stage
+ * still runs. */
 O1_API const char *o1_stage_name(int32_t stage);
 
 /* Size of the library's own device scratch used by o1_token_attend_noalloc:
@@ -253,13 +268,24 @@ O1_API int o1_token_attend_noalloc(void *state, const o1_geom *geom, const float
 
 /* Copy the state's mutable parts to host memory (NULL fields skipped).
  * Synchronises `stream`. Returns O1_ERR_STATE if the state's header does not
- * hold this geometry. */
+ * hold this geometry.
+ * What is read is the state a chunk leaves behind for the next chunk or the
+ * one-row path to carry on from ("cortiq-engine 0.8.51
+ * src/gpu_wgpu/o1_batch.rs", module doc on o1b_far_commit, o1b_ring_commit
+ * and o1b_meta; the buffers of struct State): meta, ring keys and values by
+ * slot, and the far field M, Z, T. */
 O1_API int o1_state_read(const void *state, const o1_geom *geom, o1_state_host *dst, void *stream);
 
 /* Overwrite the state's mutable parts from host memory (NULL fields kept):
  * snapshots and test set-up. Synchronises `stream`. The caller keeps the
  * state consistent (len <= group window, head < group window, M = -inf
- * exactly where farl == 0, ...). */
+ * exactly where farl == 0, ...).
+ * The same parts as o1_state_read: the state a chunk hands on to the next
+ * chunk or to the one-row path ("cortiq-engine 0.8.51
+ * src/gpu_wgpu/o1_batch.rs", module doc and struct State). The pages upload
+ * a sealed layer's state from the host the same way ("cortiq-engine 0.8.77
+ * src/gpu_wgpu/dory.rs", seal: the far states built on the CPU are
+ * uploaded). */
 O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host *src, void *stream);
 
 /* Sticky conditions a kernel records in the state header (bits of the value
@@ -286,10 +312,18 @@ O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host 
 O1_API int o1_state_back(void *state, const o1_geom *geom, int32_t rows, void *stream);
 
 /* Read the state's flags into *flags (host) and, if `clear` is non-zero,
- * reset them to 0. Synchronises `stream`. */
+ * reset them to 0. Synchronises `stream`.
+ * The pages report a failed dispatch or readback through the encoder's
+ * boolean result ("cortiq-engine 0.8.82 src/gpu_metal/o1c.rs", encode and
+ * spec_commit return false; the command buffer's error status is checked).
+ * A kernel here cannot return a value, so it records such conditions as
+ * these sticky bits. */
 O1_API int o1_state_flags(void *state, const o1_geom *geom, uint32_t *flags, int32_t clear, void *stream);
 
-/* A static, human-readable name for a status code. */
+/* A static, human-readable name for a status code. (The pages' geometry
+ * gates refuse a shape instead of running it: "cortiq-engine 0.8.82
+ * src/gpu_metal/o1c.rs", admits and tok_ok; this library returns
+ * O1_ERR_UNSUPPORTED there.) */
 O1_API const char *o1_status_string(int status);
 
 #ifdef __cplusplus

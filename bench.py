@@ -12,9 +12,12 @@ Prints one JSON line: prefill rows/s (whole job over all ranks), the dominant
 kernel against its roofline, the oracle on the host cores, the end-to-end
 rate with host buffers, clocks, and beside them: decode us/token after an
 8192-row prompt (`decode`) and across a 24-layer stack whose states exceed
-L2 (`decode_stack`), both against HBM; exact causal attention over the same
-prompt (`comparator`); speculative verify + commit cycles (`speculative`);
-ring rewinds (`rewind`).
+L2 (`decode_stack`), both against HBM; the same prompt as 64-row calls
+(`prefill_chunked`); a 32768-row prompt with group windows 1024 / 2048
+(`long_prompt`); the 24-layer stack's prefill in 64-row chunks
+(`stack_prefill`); exact causal attention over the same prompt
+(`comparator`); speculative verify + commit cycles (`speculative`); ring
+rewinds (`rewind`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -64,6 +67,23 @@ def window_flops(shape: synth.Shape, rows: int, len0: int = 0) -> float:
     for wg in wins:
         tot += shape.heads_per_group * float(np.sum(2.0 * np.minimum(wg, len0 + r + 1) * (shape.d + shape.dv)))
     return tot
+
+
+def device_rows(torch, shape: synth.Shape, seed: int, rows: int, dev, gate: bool = True):
+    """Seeded N(0,1) rows made on the device with torch's generator (one
+    stream per (seed, tensor)), for workloads too large to draw through the
+    host generator within a benchmark run. Untimed, and never compared with
+    the oracle (the parity tests draw their inputs from synth)."""
+    g = torch.Generator(device=dev)
+
+    def draw(tensor, shp):
+        g.manual_seed(seed * 16 + tensor)
+        return torch.randn(shp, generator=g, device=dev, dtype=torch.float32)
+    q = draw(synth.Q, (rows, shape.nh, shape.d))
+    k = draw(synth.K, (rows, shape.groups, shape.d))
+    v = draw(synth.V, (rows, shape.groups, shape.dv))
+    gt = draw(synth.GATE, (rows, shape.nh, shape.dv)) if gate else None
+    return q, k, v, gt
 
 
 def tensor_core_window(shape: synth.Shape) -> bool:
@@ -187,6 +207,24 @@ def oracle_prompt_rate(rows: int, threads: int):
     lay.rows(q, k, v, gt, threads=threads)
     dt = time.perf_counter() - t0
     return rows / dt, dt, lay.threads_used
+
+
+def oracle_one_thread_rates():
+    """The oracle on one thread: the tiny workload in full (16 + 64 rows) and
+    the first 1024 rows of the Qwen-layer prompt."""
+    import oracle
+    out = {}
+    for name, sh, seed, rows in (("tiny", synth.TINY, 0, 80), ("qwen_layer_1024_rows", SHAPE, SEED, 1024)):
+        c = synth.layer_constants(sh, seed)
+        g = oracle.Geom(sh.groups, sh.heads_per_group, sh.d, sh.dv, sh.sinks, sh.window, sh.landmarks,
+                        rope_base=sh.rope_base)
+        lay = oracle.OracleLayer(g, c.sink_k, c.sink_v, c.k_tilde, c.q_tilde, c.mu)
+        q, k, v, gt = synth.layer_rows(sh, seed, 0, rows)
+        t0 = time.perf_counter()
+        lay.rows(q, k, v, gt, threads=1)
+        out[name] = {"rows": rows, "seconds": time.perf_counter() - t0,
+                     "rows_per_s": rows / (time.perf_counter() - t0)}
+    return out
 
 
 def reference_arm(args, rank):
@@ -411,7 +449,7 @@ def our_arm(args, rank, world, local_rank):
     d1.record(stream)
     torch.cuda.synchronize()
     dec_us = 1e3 * d0.elapsed_time(d1) / DECODE_STEPS
-    dec_launches = 2
+    dec_launches = 1
 
     # ---- speculative verify + commit on the same state: SPEC_DRAFT-row
     # drafts attended without moving the state, SPEC_ACC rows of each
@@ -466,24 +504,24 @@ def our_arm(args, rank, world, local_rank):
     gs = o1.geom(ss.groups, ss.heads_per_group, ss.d, ss.dv, ss.sinks, ss.window, ss.landmarks,
                  rope_base=ss.rope_base)
     sscr = torch.empty(o1.o1_scratch_bytes(gs, STACK_PREFILL), dtype=torch.uint8, device=dev)
-    sp = [up(x) for x in synth.layer_rows(ss, 1000, 0, STACK_PREFILL)]
-    st_rows = [up(x) for x in synth.layer_rows(ss, 1000, STACK_PREFILL, STACK_STEPS + 2)]
     pout = torch.empty((STACK_PREFILL, ss.nh, ss.dv), dtype=torch.float32, device=dev)
-    sstates = []
+    sstates, st_rows = [], []
     for layer in range(STACK_LAYERS):
         cl = synth.layer_constants(ss, 1000 + layer)
         cst = [up(cl.sink_k), up(cl.sink_v), up(cl.k_tilde), up(cl.q_tilde), up(cl.mu)]
         st_ = torch.empty(o1.o1_state_bytes(gs), dtype=torch.uint8, device=dev)
         o1.check(o1.o1_state_init(st_, gs, None, *cst, 0), "init")
-        o1.check(o1.o1_chunk_attend(st_, gs, sscr, *sp, STACK_PREFILL, pout), "prefill")
+        rq, rk, rv, rg = device_rows(torch, ss, 1000 + layer, STACK_PREFILL + STACK_STEPS + 2, dev)
+        o1.check(o1.o1_chunk_attend(st_, gs, sscr, rq[:STACK_PREFILL], rk[:STACK_PREFILL], rv[:STACK_PREFILL],
+                                    rg[:STACK_PREFILL], STACK_PREFILL, pout), "prefill")
         sstates.append(st_)
-    del sp, pout
-    sq_, sk_, sv_, sg_ = st_rows
-    sout = torch.empty((ss.nh, ss.dv), dtype=torch.float32, device=dev)
+        st_rows.append((rq[STACK_PREFILL:], rk[STACK_PREFILL:], rv[STACK_PREFILL:], rg[STACK_PREFILL:]))
+    del pout
+    souts = [torch.empty((ss.nh, ss.dv), dtype=torch.float32, device=dev) for _ in range(STACK_LAYERS)]
 
     def stack_step(i):
-        for st_ in sstates:
-            o1.check(o1.o1_token_attend(st_, gs, sscr, sq_[i], sk_[i], sv_[i], sg_[i], sout), "token")
+        for st_, (sq_, sk_, sv_, sg_), so_ in zip(sstates, st_rows, souts):
+            o1.check(o1.o1_token_attend(st_, gs, sscr, sq_[i], sk_[i], sv_[i], sg_[i], so_), "token")
 
     for i in range(2):
         stack_step(STACK_STEPS + i)
@@ -505,8 +543,120 @@ def our_arm(args, rank, world, local_rank):
         assert o1.o1_state_flags(st_, gs) == 0, "state flags raised"
     del sstates, sscr
 
-    # ---- roofline of the dominant kernel (the window attention)
     pk_, src = peaks()
+    steps_big = max(2, min(args.steps, 5))
+
+    def graph_of(fn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(gr, stream=cap_stream):
+                fn()
+        torch.cuda.synchronize()
+        return gr
+
+    def timed_replays(graphs, restore, n):
+        """Mean ms of a graph replay; restore() runs before each, untimed."""
+        tot = 0.0
+        for i in range(n):
+            restore(i)
+            torch.cuda.synchronize()
+            d0.record(stream)
+            graphs[i % len(graphs)].replay()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            tot += d0.elapsed_time(d1)
+        return tot / n
+
+    # ---- the same 4096-row prompt as 64 calls of 64 rows (the pages' model
+    # calls the batch kernels once per 64-row chunk), each input set's 64
+    # calls captured once in a CUDA graph; the fresh state restored before
+    # each replay, outside the timed region
+    cscratch = torch.empty(o1.o1_scratch_bytes(g, 64), dtype=torch.uint8, device=dev)
+    cstate = torch.empty(sbytes, dtype=torch.uint8, device=dev)
+
+    def chunk_calls(s_):
+        def run():
+            for r0 in range(0, ROWS, 64):
+                o1.check(o1.o1_chunk_attend(cstate, g, cscratch, s_["q"][r0:r0 + 64], s_["k"][r0:r0 + 64],
+                                            s_["v"][r0:r0 + 64], s_["g"][r0:r0 + 64], 64, s_["out"][r0:r0 + 64]),
+                         "chunk")
+        return run
+    cstate.copy_(pristine)
+    chunk_calls(sets[0])()   # first calls on this thread: the library's second stream, attributes
+    cgraphs = [graph_of(chunk_calls(s_)) for s_ in sets]
+    c64_ms = timed_replays(cgraphs, lambda i: cstate.copy_(pristine), max(3, args.steps))
+    c64_flops = window_flops(sh, ROWS)
+    del cgraphs, cscratch, cstate
+
+    # ---- the long prompt: 32768 rows, group windows 1024 and 2048, one call
+    lsh = synth.QWEN_LONG
+    gl = o1.geom(lsh.groups, lsh.heads_per_group, lsh.d, lsh.dv, lsh.sinks, lsh.window, lsh.landmarks,
+                 rope_base=lsh.rope_base)
+    LROWS = 32768
+    lc = synth.layer_constants(lsh, 3)
+    lconsts = [up(lc.sink_k), up(lc.sink_v), up(lc.k_tilde), up(lc.q_tilde), up(lc.mu)]
+    lpristine = torch.empty(o1.o1_state_bytes(gl), dtype=torch.uint8, device=dev)
+    o1.check(o1.o1_state_init(lpristine, gl, lsh.group_windows, *lconsts, 0), "init")
+    lstate = torch.empty_like(lpristine)
+    lscratch = torch.empty(o1.o1_scratch_bytes(gl, LROWS), dtype=torch.uint8, device=dev)
+    lq, lk, lv, lg = device_rows(torch, lsh, 3, LROWS, dev)
+    lout = torch.empty((LROWS, lsh.nh, lsh.dv), dtype=torch.float32, device=dev)
+    lgraph = graph_of(lambda: o1.check(o1.o1_chunk_attend(lstate, gl, lscratch, lq, lk, lv, lg, LROWS, lout),
+                                       "long"))
+    long_ms = timed_replays([lgraph], lambda i: lstate.copy_(lpristine), steps_big)
+    long_flops = window_flops(lsh, LROWS)
+    assert o1.o1_state_flags(lstate, gl) == 0, "state flags raised"
+    del lgraph, lscratch, lq, lk, lv, lg, lout, lstate, lpristine
+
+    # ---- the 24-layer stack's prefill, chunk-major as a model runs it: for
+    # each 64-row chunk every layer in turn. Each layer is first brought to
+    # its steady state (the ring full: 1088 rows in one untimed call); then
+    # STACK_CHUNKS chunks go through all layers, captured once in a CUDA
+    # graph, the states restored before each replay outside the timed region.
+    STACK_CHUNKS = 16
+    ss = synth.STACK_LAYER
+    gs = o1.geom(ss.groups, ss.heads_per_group, ss.d, ss.dv, ss.sinks, ss.window, ss.landmarks,
+                 rope_base=ss.rope_base)
+    sbytes_s = o1.o1_state_bytes(gs)
+    pscr = torch.empty(o1.o1_scratch_bytes(gs, 1088), dtype=torch.uint8, device=dev)
+    cscr = torch.empty(o1.o1_scratch_bytes(gs, 64), dtype=torch.uint8, device=dev)
+    warm_states, live_states, layer_rows = [], [], []
+    for layer in range(STACK_LAYERS):
+        cl = synth.layer_constants(ss, 1000 + layer)
+        cst = [up(cl.sink_k), up(cl.sink_v), up(cl.k_tilde), up(cl.q_tilde), up(cl.mu)]
+        st_ = torch.empty(sbytes_s, dtype=torch.uint8, device=dev)
+        o1.check(o1.o1_state_init(st_, gs, None, *cst, 0), "init")
+        rq, rk, rv, rg = device_rows(torch, ss, 1000 + layer, 1088 + 64 * STACK_CHUNKS, dev)
+        pout = torch.empty((1088, ss.nh, ss.dv), dtype=torch.float32, device=dev)
+        o1.check(o1.o1_chunk_attend(st_, gs, pscr, rq[:1088], rk[:1088], rv[:1088], rg[:1088], 1088, pout),
+                 "prefill")
+        warm_states.append(st_)
+        live_states.append(torch.empty_like(st_))
+        layer_rows.append((rq[1088:], rk[1088:], rv[1088:], rg[1088:],
+                           torch.empty((64 * STACK_CHUNKS, ss.nh, ss.dv), dtype=torch.float32, device=dev)))
+    del pscr, pout
+
+    def restore_stack(i):
+        for a_, b_ in zip(live_states, warm_states):
+            a_.copy_(b_)
+
+    def stack_chunks():
+        for c in range(STACK_CHUNKS):
+            r0 = 64 * c
+            for layer in range(STACK_LAYERS):
+                q_, k_, v_, g_, o_ = layer_rows[layer]
+                o1.check(o1.o1_chunk_attend(live_states[layer], gs, cscr, q_[r0:r0 + 64], k_[r0:r0 + 64],
+                                            v_[r0:r0 + 64], g_[r0:r0 + 64], 64, o_[r0:r0 + 64]), "chunk")
+    restore_stack(0)
+    sgraph_p = graph_of(stack_chunks)
+    stack_ms = timed_replays([sgraph_p], restore_stack, steps_big)
+    stack_rows = 64 * STACK_CHUNKS
+    stack_flops = STACK_LAYERS * window_flops(ss, stack_rows, len0=ss.window)
+    for st_ in live_states:
+        assert o1.o1_state_flags(st_, gs) == 0, "state flags raised"
+    del sgraph_p, warm_states, live_states, layer_rows, cscr
+
+    # ---- roofline of the dominant kernel (the window attention)
     names = [o1.o1_stage_name(j) for j in range(nst)]
     near_ms = float(stage_avg[names.index("near")])
     flops = window_flops(sh, ROWS)
@@ -565,14 +715,43 @@ def our_arm(args, rank, world, local_rank):
             "decode_stack": {"metric": "sealed-layer decode us per 24-layer token (stack shape, states larger than "
                                        "L2)", "value": stack_us, "unit": "us/token", "higher_is_better": False,
                              "config": f"{STACK_LAYERS} independent layers G=4 x 4 heads, d=dv=128, 4 sinks, "
-                                       f"window 1024, 64 landmarks, each prefilled with {STACK_PREFILL} rows; "
-                                       f"{STACK_STEPS} steps through all layers captured once in a CUDA graph",
+                                       f"window 1024, 64 landmarks (per-layer constants and rows from seeds "
+                                       f"1000 + layer, rows drawn on the device), each prefilled with "
+                                       f"{STACK_PREFILL} rows; {STACK_STEPS} steps through all layers captured once "
+                                       f"in a CUDA graph",
                              "states_mb": stack_state_mb,
-                             "gpu_launches_per_step": 2 * STACK_LAYERS,
+                             "gpu_launches_per_step": STACK_LAYERS,
                              "algorithmic_bytes_per_step": stack_bytes,
                              "achieved_gbs": stack_bytes / (stack_us * 1e-6) / 1e9,
                              "hbm_peak_gbs": pk_["hbm_gbs"],
                              "frac_of_hbm": stack_bytes / (stack_us * 1e-6) / 1e9 / pk_["hbm_gbs"]},
+            "prefill_chunked": {"metric": "sealed-layer prefill rows/s, the 4096-row prompt as 64 calls of 64 rows",
+                                "value": ROWS / (c64_ms * 1e-3), "unit": "rows/s", "ms_per_prompt": c64_ms,
+                                "algorithmic_tflops": c64_flops / (c64_ms * 1e-3) / 1e12,
+                                "frac_of_bf16_peak": c64_flops / (c64_ms * 1e-3) / 1e12 / pk_["bf16_tflops"],
+                                "config": "same layer and inputs as the prefill steps; 64 o1_chunk_attend calls of "
+                                          "64 rows each, per input set captured once in a CUDA graph; the fresh "
+                                          "state restored before each replay, untimed"},
+            "long_prompt": {"metric": "sealed-layer prefill rows/s, 32768-row prompt, group windows 1024 / 2048",
+                            "value": LROWS / (long_ms * 1e-3), "unit": "rows/s", "ms_per_prompt": long_ms,
+                            "algorithmic_tflops": long_flops / (long_ms * 1e-3) / 1e12,
+                            "frac_of_bf16_peak": long_flops / (long_ms * 1e-3) / 1e12 / pk_["bf16_tflops"],
+                            "config": "Qwen3.5-0.8B-shaped layer with group windows 1024 and 2048 (meta slot 3), "
+                                      "one o1_chunk_attend of 32768 rows from a fresh state (inputs drawn on the "
+                                      "device, seed 3); state restored before each run, untimed"},
+            "stack_prefill": {"metric": "24-layer stack prefill rows/s (64-row chunks, chunk-major, steady state)",
+                              "value": stack_rows / (stack_ms * 1e-3), "unit": "rows/s",
+                              "ms_per_chunk_through_24_layers": stack_ms / STACK_CHUNKS,
+                              "projected_65536_row_prompt_s": 65536 / (stack_rows / (stack_ms * 1e-3)),
+                              "algorithmic_tflops": stack_flops / (stack_ms * 1e-3) / 1e12,
+                              "frac_of_bf16_peak": stack_flops / (stack_ms * 1e-3) / 1e12 / pk_["bf16_tflops"],
+                              "config": f"{STACK_LAYERS} layers G=4 x 4 heads, d=dv=128, 4 sinks, window 1024, 64 "
+                                        f"landmarks (per-layer constants from seeds 1000 + layer, per-layer rows drawn "
+                                        f"on the device); each layer brought to its full ring by an untimed "
+                                        f"1088-row call, then {STACK_CHUNKS} chunks of 64 rows through every layer "
+                                        f"in turn ({STACK_CHUNKS * STACK_LAYERS} calls) in one CUDA graph; states "
+                                        f"restored before each replay, untimed. A stated subset of the 65536-row "
+                                        f"prompt: its rows past the first window cost the same per chunk"},
             "rewind": {"metric": "o1_state_back(1) + one-row o1_spec_commit us/pair", "value": back_us,
                        "unit": "us/pair", "higher_is_better": False,
                        "config": f"{SPEC_CYCLES} pairs on the decode state, captured once in a CUDA graph"},
@@ -588,7 +767,10 @@ def our_arm(args, rank, world, local_rank):
     if rank == 0 and world == 1:
         rate, dt, cores = oracle_prompt_rate(ROWS, SHAPE.groups)
         line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                                "sample": f"the whole 4096-row prompt once ({dt:.1f} s)"}
+                                "sample": f"the whole 4096-row prompt once ({dt:.1f} s), KV groups on "
+                                          f"{cores} threads (rows are serial)",
+                                "host_cores": os.cpu_count(), "threads_used": cores,
+                                "one_thread": oracle_one_thread_rates()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

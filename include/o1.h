@@ -22,8 +22,8 @@
  *    allocates no device or host memory for a call; a state buffer carries
  *    its own header. What it keeps itself: the second CUDA stream and two
  *    events of the chunk path (one set per host thread and device, made by
- *    the first chunk call; see O1_NUM_STAGES) and the static scratch array of
- *    o1_token_attend_noalloc.
+ *    the first chunk call and released when that thread exits; see
+ *    O1_NUM_STAGES) and the static scratch array of o1_token_attend_noalloc.
  *  - Pointers: "device" pointers are CUDA global memory of the current
  *    device, "host" pointers are ordinary process memory. Device buffers must
  *    be 16-byte aligned (a torch or cudaMalloc allocation always is); the
@@ -36,7 +36,8 @@
  *  - Errors: every call validates its arguments before launching anything
  *    and returns O1_OK or a negative status; nothing falls back to another
  *    implementation. O1_ERR_CUDA reports a failed launch or copy
- *    (cudaPeekAtLastError / the copy's status).
+ *    (cudaGetLastError after the launches, which also clears a launch
+ *    error so that it is reported once; or the copy's status).
  *  - State and geometry: the state's header (magic, geometry) lives on the
  *    device. The calls that synchronise anyway (o1_state_read, _write,
  *    _flags) check it against `geom` and return O1_ERR_STATE on a mismatch.
@@ -94,7 +95,8 @@ typedef struct o1_state_host {
     float *ring_k;     /* [G][window][d]: rotated keys by ring slot            */
     float *ring_v;     /* [G][window][dv]                                      */
     float *far_max;    /* M [G*hpg][m]; -inf while the far field is empty      */
-    float *far_mass;   /* Z [G*hpg][m]                                         */
+    float *far_mass;   /* Z [G*hpg][m], rounded to f32 (the state keeps a low
+                          part beside it; a write sets that part to zero)    */
     float *far_val;    /* T [G*hpg][m][dv]                                     */
 } o1_state_host;
 
@@ -218,7 +220,7 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
  * joined back into the caller's stream by events, so a stream capture of a
  * call captures both branches. The stream and its two events are created by
  * the first call on each host thread and device (make that call before a
- * stream capture) and live until the process exits. A stage that does not apply to the geometry
+ * stream capture) and live until that thread exits. A stage that does not apply to the geometry
  * (the fp16 panel gather outside the tensor-core window path) launches
  * nothing and times as empty. */
 #define O1_NUM_STAGES 8
@@ -259,8 +261,11 @@ O1_API const char *o1_stage_name(int32_t stage);
  * the GPU (other streams, other threads) race on it, so serialise them.
  * Nothing in it needs to start at zero: a call writes every scratch value
  * before reading it. The first call on each device looks the array's
- * device address up (cudaGetSymbolAddress, that device current); make that
- * first call before any stream capture. Returns O1_ERR_UNSUPPORTED when the
+ * device address up (cudaGetSymbolAddress, that device current) and keeps
+ * it for the life of the process; make that first call before any stream
+ * capture. The kept address does not survive cudaDeviceReset of that device
+ * (a new context holds the array elsewhere): do not reset a device and go on
+ * calling this entry point on it in the same process. Returns O1_ERR_UNSUPPORTED when the
  * geometry's one-row scratch exceeds O1_NOALLOC_SCRATCH_BYTES, else as
  * o1_token_attend. */
 O1_API int o1_token_attend_noalloc(void *state, const o1_geom *geom, const float *q, const float *k,
@@ -310,6 +315,19 @@ O1_API int o1_state_write(void *state, const o1_geom *geom, const o1_state_host 
  * state's meta lives on the device, so this call cannot see it). rows = 0
  * does nothing. One single-thread launch; asynchronous. */
 O1_API int o1_state_back(void *state, const o1_geom *geom, int32_t rows, void *stream);
+
+/* Limit, in SM clock cycles, of the kernels' waits (on their own copies and
+ * tensor-core work) for calls made from now on, in this process; a call
+ * captured in a CUDA graph keeps the limit it was captured with.
+ * cycles < 1, or above the default of 4e9 (about 2 s at the maximum SM
+ * clock), restores the default. A wait that runs out raises
+ * O1_FLAG_WAIT_EXPIRED and that call's output is not valid; the kernel still
+ * waits, with the default limit, for the work it had already issued before
+ * it exits. A tiny limit makes the first waits run out on purpose, which is
+ * how that path is tested; in use the default is meant to stay. Host-only,
+ * no CUDA call; always O1_OK. (The pages' kernels wait on no barrier of
+ * this kind, so there is no counterpart to cite.) */
+O1_API int o1_set_wait_limit(int64_t cycles);
 
 /* Read the state's flags into *flags (host) and, if `clear` is non-zero,
  * reset them to 0. Synchronises `stream`.

@@ -4,7 +4,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "o1_common.cuh"
 
@@ -15,6 +17,10 @@ static __device__ __align__(256) unsigned char o1_noalloc_scratch[O1_NOALLOC_SCR
 extern const char *const o1_stage_names[O1_NUM_STAGES];
 
 namespace {
+
+// Limit of the kernels' first waits for calls launched from now on
+// (o1_set_wait_limit); drains of work already in flight keep the full limit.
+std::atomic<long long> g_wait_cycles{O1_WAIT_CYCLES_FULL};
 
 bool geom_ok(const o1_geom *g) {
     if (!g) return false;
@@ -51,6 +57,7 @@ O1Args state_args(void *state, const o1_geom &g) {
     O1Args a;
     memset(&a, 0, sizeof(a));
     a.commit = 1;
+    a.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
     a.G = g.groups;
     a.hpg = g.heads_per_group;
     a.nh = g.groups * g.heads_per_group;
@@ -73,7 +80,9 @@ O1Args state_args(void *state, const o1_geom &g) {
     a.mu = (const float *)(b + L.mu);
     a.M = (float *)(b + L.M);
     a.Z = (float *)(b + L.Z);
+    a.Zlo = (float *)(b + L.Zlo);
     a.T = (float *)(b + L.T);
+    a.tick = (uint32_t *)(b + L.tick);
     return a;
 }
 
@@ -95,6 +104,21 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.nxp = S.nxp;
     a.tc = S.nxp > 0;
     a.Sp = S.cap >= 2 ? (float *)(b + S.Sp) : nullptr;
+}
+
+// The state the last one-row step on each stream was launched on. A step on
+// the same state right after it would find the copies it issues before its
+// wait stale (the kernel checks and fetches again), so it issues them after
+// the wait instead. Only a choice of timing: the kernel's own check of the
+// position is what keeps the copies correct.
+int tok_prefetch_for(cudaStream_t st, const void *state) {
+    static std::mutex mu;
+    static std::unordered_map<const void *, const void *> last;
+    std::lock_guard<std::mutex> lock(mu);
+    const void *&prev = last[(const void *)st];
+    const int prefetch = prev != state;
+    prev = state;
+    return prefetch;
 }
 
 int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes, const float *q,
@@ -140,6 +164,10 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
             a.kcur = (float *)(sb + T.kcur);
             a.KC = T.KC;
             a.NC = T.NC;
+            a.NF = T.NF;
+            a.MB = T.MB;
+            a.tok_smem = T.smem;
+            a.tok_prefetch = tok_prefetch_for(st, state);
             a.q = q + (size_t)r0 * nh * g.d;
             a.k = k + (size_t)r0 * g.groups * g.d;
             a.v = v + (size_t)r0 * g.groups * g.dv;
@@ -394,6 +422,8 @@ int o1_state_write(void *state, const o1_geom *geom, const o1_state_host *src, v
     cp(src->far_max, L.M, nh * m * 4);
     cp(src->far_mass, L.Z, nh * m * 4);
     cp(src->far_val, L.T, nh * m * g.dv * 4);
+    // a written far mass is exact as given: its low part is zero
+    if (e == cudaSuccess && src->far_mass) e = cudaMemsetAsync(b + L.Zlo, 0, nh * m * 4, st);
     if (e != cudaSuccess) return O1_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return O1_ERR_CUDA;
     return O1_OK;
@@ -409,6 +439,12 @@ int o1_state_flags(void *state, const o1_geom *geom, uint32_t *flags, int32_t cl
     if (cudaMemcpyAsync(flags, b, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) return O1_ERR_CUDA;
     if (clear && cudaMemsetAsync(b, 0, sizeof(uint32_t), st) != cudaSuccess) return O1_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return O1_ERR_CUDA;
+    return O1_OK;
+}
+
+int o1_set_wait_limit(int64_t cycles) {
+    g_wait_cycles.store(cycles < 1 || cycles > O1_WAIT_CYCLES_FULL ? O1_WAIT_CYCLES_FULL : (long long)cycles,
+                        std::memory_order_relaxed);
     return O1_OK;
 }
 

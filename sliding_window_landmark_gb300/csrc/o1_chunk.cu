@@ -253,9 +253,10 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
             a.Fb[(O1_FB_LSUM * nm + wid) * a.nsub + c] = p1;
         }
         if (c == 0 && lane == 0) {
-            // the entering (M, Z), which k_far_tscan reads while it replaces the state's
+            // the entering (M, Z, Zlo), which k_far_tscan reads while it replaces the state's
             a.Fb[O1_FB_PLANES * nm * a.nsub + wid] = a.M[wid];
             a.Fb[O1_FB_PLANES * nm * a.nsub + nm + wid] = a.Z[wid];
+            a.Fb[O1_FB_PLANES * nm * a.nsub + 2 * nm + wid] = a.Zlo[wid];
         }
     }
     if (!any) return;   // k_far_tscan adds no increment for a block without evictions
@@ -327,11 +328,12 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
 // max M_c = max(M_{c-1}, m_c), the rescale R_c = e^{M_{c-1} - M_c} (1 when
 // the max stays, so an empty field stays empty) and the block factor
 // f_c = e^{m_c - M_c} (0 for a block without evictions). The value sum
-// entering block c, R_c T_{c-1}, goes to Tp[c] and T_c = R_c T_{c-1} + f_c dT_c;
-// the mass likewise, Z_c = R_c Z_{c-1} + f_c s_c. Column 0's thread records
-// M_c, R_c Z_{c-1} and f_c for the side readout; the last M, Z, T are the new
-// state (o1b_far_e's max / rescale and o1b_far_commit's recurrence, taken as
-// a scan over the blocks).
+// entering block c, R_c T_{c-1}, goes to Tp[c] and T_c = R_c T_{c-1} + f_c dT_c.
+// Column 0's thread also carries the mass, Z_c = R_c Z_{c-1} + f_c s_c, in
+// float-float (the state keeps Z as a high and a low f32 part), and records M_c,
+// R_c Z_{c-1} (high and low) and f_c for the side readout; the last M, Z, T
+// are the new state (o1b_far_e's max / rescale and o1b_far_commit's
+// recurrence, taken as a scan over the blocks).
 __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
     const size_t n = (size_t)a.nh * a.m * a.dv, nm = (size_t)a.nh * a.m;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -342,19 +344,21 @@ __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
     const float *lsum = a.Fb + (O1_FB_LSUM * nm + wid) * a.nsub;
     float *Mc = a.Fb + (O1_FB_MC * nm + wid) * a.nsub;
     float *Bc = a.Fb + (O1_FB_BASE * nm + wid) * a.nsub;
+    float *Bl = a.Fb + (O1_FB_BASELO * nm + wid) * a.nsub;
     float *Fc = a.Fb + (O1_FB_FAC * nm + wid) * a.nsub;
+    const float *enter = a.Fb + O1_FB_PLANES * nm * a.nsub;
     float T = a.T[idx];
-    float Mo = a.Fb[O1_FB_PLANES * nm * a.nsub + wid], Zo = a.Fb[O1_FB_PLANES * nm * a.nsub + nm + wid];
+    const float M0 = enter[wid];
+    float Mo = M0;
     // 8 blocks' loads issued before their stores (the compiler cannot
     // reorder them itself: the stores may alias later loads for all it knows);
     // few enough registers for the scan to sit beside a window CTA
     for (int c0 = 0; c0 < a.nsub; c0 += 8) {
-        float lm[8], ls[8], dT[8];
+        float lm[8], dT[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int c = c0 + i;
             lm[i] = c < a.nsub ? lmax[c] : -INFINITY;
-            ls[i] = c < a.nsub ? lsum[c] : 0.f;
             dT[i] = c < a.nsub ? a.Tp[(size_t)c * n + idx] : 0.f;
         }
 #pragma unroll
@@ -367,23 +371,36 @@ __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
                 const float Ts = Rf * T;
                 a.Tp[(size_t)c * n + idx] = Ts;
                 T = f != 0.f ? fmaf(f, dT[i], Ts) : Ts;
-                const float base = Rf * Zo;
-                if (col0) {
-                    Mc[c] = Mn;
-                    Bc[c] = base;
-                    Fc[c] = f;
-                }
-                Zo = fmaf(f, ls[i], base);
                 Mo = Mn;
             }
         }
     }
+    if (col0) {
+        // the running max again, with the mass in float-float: M_c, R_c Z_{c-1}
+        // (high, low) and f_c per block for the side readout
+        o1_ff Zo = ff_make(enter[nm + wid], enter[2 * nm + wid]);
+        float Mr = M0;
+        for (int c = 0; c < a.nsub; ++c) {
+            const float lm = lmax[c];
+            const float Mn = fmaxf(Mr, lm);
+            const float Rf = Mn == Mr ? 1.f : expf(Mr - Mn);
+            const float f = lm == -INFINITY ? 0.f : expf(lm - Mn);
+            const o1_ff base = ff_mul_f(Zo, Rf);
+            Mc[c] = Mn;
+            Bc[c] = base.hi;
+            Bl[c] = base.lo;
+            Fc[c] = f;
+            Zo = ff_fma_f(base, f, lsum[c]);
+            Mr = Mn;
+        }
+        if (a.commit) {
+            a.M[wid] = Mr;
+            a.Z[wid] = Zo.hi;
+            a.Zlo[wid] = Zo.lo;
+        }
+    }
     if (!a.commit) return;   // attend only: the state keeps its far field
     a.T[idx] = T;
-    if (col0) {
-        a.M[wid] = Mo;
-        a.Z[wid] = Zo;
-    }
 }
 
 // The side part of every row of block c for head gh: the sinks and the far
@@ -421,8 +438,8 @@ __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
     off[1] = off[0] + (size_t)K6 * SR_LDA;                   // R1: score chunks, then B6 chunks (2 stages)
     off[2] = off[1] + (r1a > r1b ? r1a : r1b);               // sS [64][64 nbt + 1]
     off[3] = off[2] + (size_t)64 * (64 * nbt + 1);           // R3: mu, then E [64][65]
-    off[4] = off[3] + 64 * 65;                               // F, M_c, R_c Z_{c-1}, f_c [64] each
-    off[5] = off[4] + 4 * 64;                                // total (floats)
+    off[4] = off[3] + 64 * 65;                               // F, M_c, R_c Z_{c-1} (hi), f_c, (lo) [64] each
+    off[5] = off[4] + 5 * 64;                                // total (floats)
 }
 
 
@@ -447,9 +464,10 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     float *sS = sm + off[2];
     float *sR3 = sm + off[3];
     float *sRow = sm + off[4];
-    float *sMc = sRow + 64;    // M_c, R_c Z_{c-1}, f_c per landmark
+    float *sMc = sRow + 64;    // M_c, R_c Z_{c-1} (high, low), f_c per landmark
     float *sBc = sRow + 128;
     float *sFc = sRow + 192;
+    float *sBl = sRow + 256;
 
     // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks. A block
     //    without far field needs only the few sink columns: a warp per row.
@@ -565,6 +583,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             const size_t wid = (size_t)gh * m + b;
             sMc[b] = b < m ? a.Fb[(O1_FB_MC * nm + wid) * a.nsub + c] : 0.f;
             sBc[b] = b < m ? a.Fb[(O1_FB_BASE * nm + wid) * a.nsub + c] : 0.f;
+            sBl[b] = b < m ? a.Fb[(O1_FB_BASELO * nm + wid) * a.nsub + c] : 0.f;
             sFc[b] = b < m ? a.Fb[(O1_FB_FAC * nm + wid) * a.nsub + c] : 0.f;
         }
         __syncthreads();
@@ -619,12 +638,24 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             cf = warp_max(fmaxf(cb0, cb1));
             g0 = lane < m ? u0 * expf(cb0 - cf) : 0.f;
             g1 = lane + 32 < m ? u1 * expf(cb1 - cf) : 0.f;
-            // far mass P_b(row) = R_c Z_{c-1} + f_c (in-block prefix)
-            const float p0 = lane < m ? fmaf(sFc[lane], a.P[((size_t)gh * m + lane) * a.cap + r], sBc[lane]) : 0.f;
-            const float p1 =
-                lane + 32 < m ? fmaf(sFc[lane + 32], a.P[((size_t)gh * m + lane + 32) * a.cap + r], sBc[lane + 32]) : 0.f;
-            D = warp_sum(g0 * p0 + g1 * p1);
-            have = D >= 0.f;
+            // far mass P_b(row) = R_c Z_{c-1} + f_c (in-block prefix), and
+            // D = sum_b gain_b P_b, in float-float (the terms can cancel to
+            // a small fraction of their size)
+            auto pmass = [&](int b) -> o1_ff {
+                return ff_fma_f(ff_make(sBc[b], sBl[b]), sFc[b], a.P[((size_t)gh * m + b) * a.cap + r]);
+            };
+            o1_ff Dd = ff_make(0.f, 0.f);
+            if (lane < m) {
+                const o1_ff p0 = pmass(lane);
+                Dd = ff_add(ff_mul_f(p0, g0), Dd);
+            }
+            if (lane + 32 < m) {
+                const o1_ff p1 = pmass(lane + 32);
+                Dd = ff_add(ff_mul_f(p1, g1), Dd);
+            }
+            Dd = warp_sum(Dd);
+            have = ff_nonneg(Dd);
+            D = Dd.hi + Dd.lo;
         }
         const float sx0 = (i < nr && lane < ns) ? sS[i * ldS + m + lane] : -INFINITY;
         const float sx1 = (i < nr && lane + 32 < ns) ? sS[i * ldS + m + lane + 32] : -INFINITY;
@@ -1257,6 +1288,14 @@ namespace {
 struct O1Aux {
     cudaStream_t st = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    // Released when the host thread exits, so that short-lived or pooled
+    // threads leave nothing behind. (Should the runtime already be unloading,
+    // these calls return an error and change nothing.)
+    ~O1Aux() {
+        if (join) cudaEventDestroy(join);
+        if (fork) cudaEventDestroy(fork);
+        if (st) cudaStreamDestroy(st);
+    }
 };
 
 cudaError_t o1_aux(O1Aux **out) {
@@ -1352,7 +1391,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     const int live = R < a.w ? R : a.w;
     if (a.commit) k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
     end(7, st);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }
 
 // The state-advancing stages of a pass, without the attention: keys
@@ -1371,7 +1410,7 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }
 
 // Fresh far field and ring: M = -inf, Z = 0, T = 0, ring zeros.
@@ -1380,11 +1419,14 @@ __global__ void k_init_state(O1Args a) {
     const size_t nT = nM * a.dv;
     const size_t nK = (size_t)a.G * a.w * a.d, nV = (size_t)a.G * a.w * a.dv;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t nTick = (size_t)a.nh + a.G + 1;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nT + nK + nV + nM; i += stride) {
         if (i < nM) {
             a.M[i] = -INFINITY;
             a.Z[i] = 0.f;
+            a.Zlo[i] = 0.f;
         }
+        if (i < nTick) a.tick[i] = 0u;
         if (i < nT) a.T[i] = 0.f;
         else if (i < nT + nK) a.ring_k[i - nT] = 0.f;
         else if (i < nT + nK + nV) a.ring_v[i - nT - nK] = 0.f;
@@ -1393,7 +1435,7 @@ __global__ void k_init_state(O1Args a) {
 
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st) {
     k_init_state<<<304, 256, 0, st>>>(a);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }
 
 // One thread: check that every group can rewind `rows` pushes (dory.rs
@@ -1425,5 +1467,5 @@ __global__ void k_back(O1Args a, int rows) {
 
 cudaError_t o1_launch_back(const O1Args &a, int rows, cudaStream_t st) {
     k_back<<<1, 1, 0, st>>>(a, rows);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }

@@ -22,7 +22,8 @@
 #define O1_FB_MC 2
 #define O1_FB_BASE 3
 #define O1_FB_FAC 4
-#define O1_FB_PLANES 5
+#define O1_FB_BASELO 5
+#define O1_FB_PLANES 6
 #define O1_MAX_D 256
 #define O1_MAX_DV 256
 #define O1_MAX_M 64
@@ -31,6 +32,10 @@
 #define O1_MAX_W (1 << 20)
 #define O1_TC_BN 128           // keys per tile of the tensor-core window path
 #define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
+// Clock cycles an in-kernel wait may spin before the kernel gives up (about
+// 2 s at the maximum SM clock). Drains of copies or MMAs already in flight
+// always use this limit; the first waits of a call use O1Args::wait_cycles.
+#define O1_WAIT_CYCLES_FULL 4000000000LL
 
 // First bytes of a state buffer.
 struct O1Header {
@@ -46,9 +51,17 @@ struct O1Header {
 static inline size_t o1_al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Byte offsets of a state's parts. Per group: meta, ring, sinks, landmark
-// keys; per head: landmark queries, mu and the far field (M, Z, T).
+// keys; per head: landmark queries, mu and the far field (M, Z, T). The far
+// mass Z is a sum over every evicted key and grows for as long as the layer
+// runs, so it is kept as an unevaluated pair Z + Zlo (Zlo the rounding error
+// of Z, |Zlo| <= ulp(Z) / 2) and its recurrence is taken in float-float: an f32
+// running sum drifts by about one rounding per update, and signed landmark
+// coefficients can cancel the far mass D = sum_b gain_b Z_b down to a small
+// fraction of its terms, which magnifies that drift in the output.
+// Last come the one-row path's arrival counters (one per head, then one for
+// the whole step; G more are kept free), zero between calls.
 struct O1Layout {
-    size_t hdr, meta, ring_k, ring_v, sink_k, sink_v, kt, qt, mu, M, Z, T, total;
+    size_t hdr, meta, ring_k, ring_v, sink_k, sink_v, kt, qt, mu, M, Z, Zlo, T, tick, total;
 };
 
 static inline O1Layout o1_layout(const o1_geom &g) {
@@ -67,7 +80,9 @@ static inline O1Layout o1_layout(const o1_geom &g) {
     L.mu = off;     off += o1_al256(nh * m * m * 4);
     L.M = off;      off += o1_al256(nh * m * 4);
     L.Z = off;      off += o1_al256(nh * m * 4);
+    L.Zlo = off;    off += o1_al256(nh * m * 4);
     L.T = off;      off += o1_al256(nh * m * dv * 4);
+    L.tick = off;   off += o1_al256((nh + G + 1) * 4);
     L.total = off;
     return L;
 }
@@ -79,8 +94,9 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   P  [nh][m][cap]  per row, the in-block prefix of E
 //   Fb [O1_FB_PLANES][nh][m][nsub] per block: local max, local mass (from
 //                    the block kernel), running max M_c, R_c Z_{c-1} and
-//                    the factor exp(local max - M_c) (from the scan); then
-//                    [2][nh][m] the far (M, Z) entering the pass
+//                    the factor exp(local max - M_c) (from the scan), and
+//                    the low part of R_c Z_{c-1}; then [3][nh][m] the far
+//                    (M, Z, Zlo) entering the pass
 //   Tp [nsub][nh][m][dv]  far value sums: increments relative to the block
 //                         max, then the value sum entering each block,
 //                         rescaled to its running max
@@ -124,7 +140,7 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     S.kr = off; off += o1_al256(c * G * d * 4);
     S.E = off;  off += o1_al256(nh * m * c * 4);
     S.P = off;  off += o1_al256(nh * m * c * 4);
-    S.Fb = off; off += o1_al256((O1_FB_PLANES * ns + 2) * nh * m * 4);
+    S.Fb = off; off += o1_al256((O1_FB_PLANES * ns + 3) * nh * m * 4);
     S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
     S.fh = off; off += o1_al256(c * nh * 4 * 4);
     S.sh = off; off += o1_al256(c * nh * 4 * 4);
@@ -141,45 +157,96 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     return S;
 }
 
-// Far blocks of the one-row path per head, each over dv / O1_TOK_FS value
-// columns (rounded up to a multiple of 4). More than one block per head
-// measured slower: each recomputes the landmark part, and the shares of T are
-// strided rows that a bulk copy cannot bring in whole.
-#define O1_TOK_FS 1
-__host__ __device__ inline int o1_tok_far_cols(int dv) { return (dv + 4 * O1_TOK_FS - 1) / (4 * O1_TOK_FS) * 4; }
-// The far record per head: (c_f, D, have, evicted, numerator [dv], M' [m], Z' [m]).
-static inline size_t o1_tok_far_stride(const o1_geom &g) { return 4 + (size_t)g.dv + 2 * (size_t)g.landmarks; }
+// The one-row path runs as one launch of about one wave of CTAs
+// (O1_TOK_CTAS): far chunks, one per (head, MB landmarks), NF per head, and
+// near slices, one per (group, KC keys of the near set), NC per group, sized
+// so that their bytes are about even. Each CTA's shared memory stays under
+// O1_TOK_SMEM_CAP, so that the next step's CTAs fit beside a running step's
+// and can start loading under its tail.
+#define O1_TOK_CTAS 148
+#define O1_TOK_SMEM_CAP (100 * 1024)
+#define O1_TOK_MB_MAX 32   // landmarks of a far chunk: one per lane of a warp
 
-// Scratch of the one-row path: near partials per (group, key slice, head),
-// the value sums [dv] in `part` and (max, sum) in `pml`; the far record per
-// head; the row's rotated key per group.
-// KC keys per slice (a multiple of 8), NC slices per group, sized for the
-// longest near set (sinks + window) so that all groups' slices make about
-// 136 blocks (one wave with the far blocks), and capped so that a slice fits
-// in shared memory.
+// Shared memory (floats) of a near slice and of a far chunk, and of the
+// merge scratch that follows either; the kernel carves the same offsets.
+// The merge of up to hpg heads: per head NF far record factors and 8
+// scalars, then (16-byte aligned) 256 float4 partials for combining slice
+// groups; nothing per near slice. The step's commit reuses it for one slot
+// index per group.
+__host__ __device__ inline size_t o1_tok_merge_floats(int hpg, int NF, int G) {
+    const size_t mg = (size_t)hpg * (NF + 8) + 4 + 4 * 256;
+    return mg > (size_t)G ? mg : (size_t)G;
+}
+__host__ __device__ inline size_t o1_tok_near_floats(int d, int dv, int hpg, int KC, int NF, int G) {
+    return 4 + (size_t)hpg * d + d + dv + (size_t)hpg * dv + (size_t)KC * (d + dv) + (size_t)KC * hpg +
+           (size_t)8 * KC * hpg + o1_tok_merge_floats(hpg, NF, G);
+}
+// (the merge scratch of a far chunk starts 4-aligned: 4 + m MB + 8 m + 2 m
+// rounds up to a multiple of 4 through the 3 floats of slack after it)
+__host__ __device__ inline size_t o1_tok_far_floats(int d, int dv, int hpg, int m, int MB, int NF, int G) {
+    return 4 + 3 * (size_t)d + 2 * (size_t)dv + (size_t)hpg * dv + (size_t)MB * d + (size_t)m * d +
+           (size_t)MB * dv + (size_t)m * MB + 8 * (size_t)m + 8 * (size_t)MB + 2 * (size_t)m + 8 * (size_t)MB +
+           256 + 3 + o1_tok_merge_floats(hpg, NF, G);
+}
+
+// Scratch of the one-row path: near partials per (group, slice, head), the
+// value sums [dv] in `part` and (max, sum) in `pml`; far records per (head,
+// chunk): (c_f of the chunk, -, D high, D low, numerator [dv]); the row's
+// rotated key per group, for the commit.
 struct O1TokScratch {
     size_t part, pml, farp, kcur, total;
-    int KC, NC;
+    int KC, NC, NF, MB;
+    size_t smem;   // bytes of dynamic shared memory per CTA
 };
 
 static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
-    const size_t G = g.groups, nh = (size_t)g.groups * g.heads_per_group, dv = g.dv, d = g.d;
-    const long long nmax = (long long)g.sinks + g.window;
-    long long kc = (nmax * (long long)G + 135) / 136;
-    kc = kc < 8 ? 8 : (kc + 7) / 8 * 8;
-    // a slice's keys, values, scores and partial dots (8 per key and head)
-    // stay within 227 KB of shared memory, rows padded by 4 floats
-    const long long kmax = ((227 * 1024 / 4) - (long long)(g.heads_per_group + 1) * (g.d + 4) - 2 * g.heads_per_group) /
-                           ((long long)g.d + 4 + g.dv + 9 * g.heads_per_group) / 8 * 8;
-    if (kc > kmax) kc = kmax;
+    const long long G = g.groups, hpg = g.heads_per_group, nh = G * hpg, d = g.d, dv = g.dv, m = g.landmarks;
+    const long long nnear = (long long)g.sinks + g.window;
+    const double near_bytes = 4.0 * G * nnear * (d + dv);
+    const double far_head = 4.0 * m * (d + 2 * dv + m);
+    const double beta = (near_bytes + nh * far_head) / O1_TOK_CTAS;
+    long long NF = (long long)(far_head / beta + 0.999);
+    // every chunk also reads all m landmark keys (m d floats): more chunks
+    // than the far bytes over that share only repeat it
+    const long long nf_max = (d + 2 * dv + m + d - 1) / d;
+    NF = NF > nf_max ? nf_max : NF;
+    NF = NF < 1 ? 1 : (NF > m ? m : NF);
+    long long MB = (m + NF - 1) / NF;
+    if (MB > O1_TOK_MB_MAX) MB = O1_TOK_MB_MAX;
+    const long long cap = O1_TOK_SMEM_CAP / 4;
+    // the merge scratch depends on NC, which is not known yet: size the far
+    // chunk with a bound on it (at most O1_TOK_CTAS slices a group). Chunks
+    // stay at 8 landmarks or more: below that the parts every chunk holds
+    // whole (landmark keys, gate, merge scratch) dominate, and more chunks
+    // only repeat them; such a CTA just takes more than the cap.
+    while (MB > 8 && (long long)o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB,
+                                                   (int)((m + MB - 1) / MB), (int)G) > cap)
+        MB = (MB + 1) / 2;
+    NF = (m + MB - 1) / MB;
+    long long near_ctas = O1_TOK_CTAS - nh * NF;
+    if (near_ctas < G) near_ctas = G;
+    const long long nc0 = (near_ctas + G - 1) / G;
+    long long KC = (nnear + nc0 - 1) / nc0;
+    KC = KC < 8 ? 8 : (KC + 7) / 8 * 8;
+    if (KC > 256) KC = 256;   // a slice's keys sit in a warp's registers, 8 per lane
+    long long NC = (nnear + KC - 1) / KC;
+    while (KC > 8 && (long long)o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NF, (int)G) > cap) {
+        KC -= 8;
+        NC = (nnear + KC - 1) / KC;
+    }
     O1TokScratch S;
-    S.KC = (int)kc;
-    S.NC = (int)((nmax + kc - 1) / kc);
+    S.KC = (int)KC;
+    S.NC = (int)NC;
+    S.NF = (int)NF;
+    S.MB = (int)MB;
+    const size_t nf = o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB, (int)NF, (int)G);
+    const size_t nn = o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NF, (int)G);
+    S.smem = 4 * (nf > nn ? nf : nn);
     size_t off = 0;
-    S.part = off; off += o1_al256(G * S.NC * g.heads_per_group * dv * 4);
-    S.pml = off;  off += o1_al256(G * S.NC * g.heads_per_group * 2 * 4);
-    S.farp = off; off += o1_al256(nh * o1_tok_far_stride(g) * 4);
-    S.kcur = off; off += o1_al256(G * d * 4);
+    S.part = off; off += o1_al256((size_t)G * NC * hpg * dv * 4);
+    S.pml = off;  off += o1_al256((size_t)G * NC * hpg * 2 * 4);
+    S.farp = off; off += o1_al256((size_t)nh * NF * (4 + dv) * 4);
+    S.kcur = off; off += o1_al256((size_t)G * d * 4);
     S.total = off;
     return S;
 }
@@ -201,11 +268,13 @@ struct O1Args {
     uint32_t *meta;
     float *ring_k, *ring_v;
     const float *sink_k, *sink_v, *kt, *qt, *mu;
-    float *M, *Z, *T;
+    float *M, *Z, *Zlo, *T;
+    uint32_t *tick;   // one-row path: arrival counters [nh + G + 1]
     // this pass's rows
     const float *q, *k, *v, *gate;
     float *out;
     int R, nsub;
+    long long wait_cycles;   // limit of the first waits (o1_set_wait_limit); drains use O1_WAIT_CYCLES_FULL
     int commit;   // 0: attend only, the state is left as it was (speculative verify)
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     // scratch
@@ -215,9 +284,11 @@ struct O1Args {
     unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;
     float *Sp;   // short-pass window partials (null when the layout has none)
-    // one-row path scratch
+    // one-row path scratch and work split
     float *part, *pml, *farp, *kcur;
-    int KC, NC;
+    int KC, NC, NF, MB;
+    size_t tok_smem;
+    int tok_prefetch;   // issue the state copies before waiting on the previous kernel
 };
 
 // ---------------------------------------------------------------- helpers
@@ -250,6 +321,57 @@ __device__ __forceinline__ float warp_sum(float x) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
+
+// Float-float arithmetic: a value as the unevaluated sum hi + lo of two f32
+// (|lo| <= ulp(hi) / 2), about 48 significant bits, from f32 operations only
+// (FP64 runs at a small fraction of the f32 rate on this part). The error-free
+// transformations are Knuth's TwoSum and the fma-based TwoProduct (Dekker;
+// Ogita, Rump and Oishi, "Accurate sum and dot product", 2005); the _rn
+// intrinsics keep the compiler from contracting or reordering them.
+struct o1_ff {
+    float hi, lo;
+};
+__device__ __forceinline__ o1_ff ff_make(float hi, float lo) {
+    o1_ff r;
+    r.hi = hi;
+    r.lo = lo;
+    return r;
+}
+__device__ __forceinline__ o1_ff ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b), bb = __fsub_rn(s, a);
+    return ff_make(s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb)));
+}
+__device__ __forceinline__ o1_ff ff_fast_two_sum(float a, float b) {   // |a| >= |b| or a == 0
+    const float s = __fadd_rn(a, b);
+    return ff_make(s, __fsub_rn(b, __fsub_rn(s, a)));
+}
+__device__ __forceinline__ o1_ff ff_norm(float hi, float lo) { return ff_two_sum(hi, lo); }
+__device__ __forceinline__ o1_ff ff_add(o1_ff a, o1_ff b) {
+    const o1_ff s = ff_two_sum(a.hi, b.hi);
+    return ff_norm(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ o1_ff ff_add_f(o1_ff a, float b) {
+    const o1_ff s = ff_two_sum(a.hi, b);
+    return ff_norm(s.hi, __fadd_rn(s.lo, a.lo));
+}
+// a * b for a float-float a and an f32 b
+__device__ __forceinline__ o1_ff ff_mul_f(o1_ff a, float b) {
+    const float p = __fmul_rn(a.hi, b);
+    const float e = fmaf(a.hi, b, -p);
+    return ff_norm(p, fmaf(a.lo, b, e));
+}
+// acc + a * b for f32 a and b, the product taken exactly
+__device__ __forceinline__ o1_ff ff_fma_f(o1_ff acc, float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return ff_add(acc, ff_make(p, fmaf(a, b, -p)));
+}
+__device__ __forceinline__ o1_ff warp_sum(o1_ff x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x = ff_add(x, ff_make(__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)));
+    return x;
+}
+__device__ __forceinline__ bool ff_nonneg(o1_ff x) { return x.hi > 0.f || (x.hi == 0.f && x.lo >= 0.f); }
 
 // The ring window of group g at the start of a pass: len0 keys in logical
 // order from slot head0; wg = the group's window (meta slot 3).
@@ -342,7 +464,7 @@ static inline void o1_attrs_done(unsigned long long *mask, unsigned long long bi
     __atomic_fetch_or(mask, bit, __ATOMIC_RELEASE);
 }
 
-// Launchers (o1_chunk.cu). Each returns cudaPeekAtLastError() after its launches.
+// Launchers (o1_chunk.cu). Each returns cudaGetLastError() after its launches.
 // `ev` may be null; otherwise 2 * O1_NUM_STAGES events, one before and one after each stage.
 cudaError_t o1_launch_pass(const O1Args &a, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 cudaError_t o1_launch_init(const O1Args &a, cudaStream_t st);

@@ -39,7 +39,9 @@
 // Roles: warps 0-3 softmax / epilogue (thread = TMEM lane = query row),
 // warp 4 TMA producer, warp 5 MMA issuer (and TMEM owner). Every wait is
 // bounded by a clock limit; on expiry the kernel raises a flag in the state
-// header, stops issuing work and still releases its TMEM.
+// header and stops issuing work, then waits (with the full limit) for the
+// MMAs and copies it has already issued before it releases its TMEM and
+// shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -56,7 +58,6 @@ constexpr int TC_THREADS = 192;
 constexpr int TC_O_COL = 0;        // O accumulator: TMEM columns [0, dv)
 constexpr int TC_S_COL = 256;      // S / P buffers: [256, 384) and [384, 512)
 constexpr float TC_RESCALE = 8.f;  // log2-units headroom before O is rescaled
-constexpr long long TC_WAIT_CYCLES = 4000000000LL;
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -70,18 +71,25 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: false (and the shared abort flag raised) after the limit or
-// once another thread has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// Bounded wait: false (and the shared abort flag raised) after `limit`
+// cycles or once another thread has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, long long limit) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > TC_WAIT_CYCLES) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             return false;
         }
+    }
+}
+// Drain: wait, with the full limit, for a phase whose operations are already
+// in flight (copies or MMAs that write this block's shared memory or TMEM).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity) && clock64() - t0 < O1_WAIT_CYCLES_FULL) {
     }
 }
 
@@ -318,6 +326,8 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
     __syncthreads();
     tc_after();
     const uint32_t tmem = *tslot;
+    const long long wl = a.wait_cycles;   // limit of every wait but the final drains
+    int issued = 0;                      // ring items the producer has issued (its lane 0)
 
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer
@@ -333,7 +343,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             const int ybase = pl.g * NXp;
             auto next = [&](uint32_t bytes) -> int {
                 const int s = it % nslot;
-                if (!mbar_wait(&empty[s], ((it / nslot) & 1) ^ 1, abort)) return -1;
+                if (!mbar_wait(&empty[s], ((it / nslot) & 1) ^ 1, abort, wl)) return -1;
                 mbar_expect_tx(&full[s], bytes);
                 ++it;
                 return s;
@@ -362,15 +372,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 if (j + 1 < pl.nt) ok = load_k(j + 1);
                 if (ok) ok = load_v(j);
             }
-
-            if (!ok && it > 0) {
-                // drain: wait (bounded) for this thread's copies still in flight
-                for (int i = max(0, it - nslot); i < it; ++i) {
-                    const long long t0 = clock64();
-                    while (!mbar_try(&full[i % nslot], (i / nslot) & 1) && clock64() - t0 < TC_WAIT_CYCLES) {
-                    }
-                }
-            }
+            issued = it;   // copies still in flight after an abort are drained at the end
         }
     } else if (warp == 5) {
         // ------------------------------------------------------ MMA issuer
@@ -378,14 +380,14 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             const uint32_t id_s = idesc_f16(TC_BM, TC_BN), id_o = idesc_f16(TC_BM, dv);
             const uint32_t qh0 = su32(sQh), ql0 = su32(sQl), ra = su32(sR);
             int it = 0;
-            bool ok = mbar_wait(q_ready, 0, abort);
+            bool ok = mbar_wait(q_ready, 0, abort, wl);
             tc_after();
             // S = Q_hi.K_hi + Q_hi.K_lo + Q_lo.K_hi, one ring slot per d-chunk
             auto issue_s = [&](int j) -> bool {
                 const uint32_t dcol = tmem + TC_S_COL + TC_BN * (j & 1);
                 for (int c = 0; c < pl.nkc; ++c) {
                     const int s = it % nslot;
-                    if (!mbar_wait(&full[s], (it / nslot) & 1, abort)) return false;
+                    if (!mbar_wait(&full[s], (it / nslot) & 1, abort, wl)) return false;
                     tc_after();
                     const uint32_t kh = ra + s * TC_SLOT, kl = kh + TC_BN * 128, qh = qh0 + c * 16384,
                                    ql = ql0 + c * 16384;
@@ -405,8 +407,8 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 const uint32_t pcol = tmem + TC_S_COL + TC_BN * (j & 1);
                 for (int kh = 0; kh < 2; ++kh) {
                     const int sh = it % nslot, sl = (it + 1) % nslot;
-                    if (!mbar_wait(&full[sh], (it / nslot) & 1, abort)) return false;
-                    if (!mbar_wait(&full[sl], ((it + 1) / nslot) & 1, abort)) return false;
+                    if (!mbar_wait(&full[sh], (it / nslot) & 1, abort, wl)) return false;
+                    if (!mbar_wait(&full[sl], ((it + 1) / nslot) & 1, abort, wl)) return false;
                     tc_after();
                     const uint32_t vh = ra + sh * TC_SLOT, vl = ra + sl * TC_SLOT;
                     for (int k = 0; k < 4; ++k) {
@@ -426,7 +428,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             for (int j = 0; ok && j < pl.nt; ++j) {
                 if (j + 1 < pl.nt) ok = issue_s(j + 1);
                 if (!ok) break;
-                ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort);
+                ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort, wl);
                 tc_after();
                 if (ok) ok = issue_pv(j);
             }
@@ -446,7 +448,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         bool ok = true;
         uint32_t v[64];
         for (int j = 0; j < pl.nt && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort, wl));
             if (!ok) break;
             tc_after();
             const uint32_t scol = lane_base + TC_S_COL + TC_BN * (j & 1);
@@ -482,7 +484,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                 const float mnew = fmaxf(mref, mt);
                 if (j > 0) {
                     // O holds PV_0 .. PV_{j-1}: wait for the last of them, then rescale
-                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort));
+                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort, wl));
                     if (!ok) break;
                     tc_after();
                     const float f = mref > -INFINITY ? ex2(mref - mnew) : 0.f;
@@ -547,7 +549,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             tc_before();
             mbar_arrive(&p_full[j & 1]);
         }
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, 0, abort));
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, 0, abort, wl));
         tc_after();
         if (ok) {
             // the window part of each row: its header (reference, mass, true
@@ -580,14 +582,19 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
         }
     }
     // everyone waits for the MMA thread's final commit before TMEM is released
-    if (warp == 5 && lane == 0) {
-        const long long t0 = clock64();
-        while (!mbar_try(o_done, 0) && clock64() - t0 < TC_WAIT_CYCLES) {
-        }
-    }
+    if (warp == 5 && lane == 0) mbar_drain(o_done, 0);
     tc_before();
     __syncthreads();
     tc_after();
+    // After an abort (every role has stopped by now, so the flag no longer
+    // changes): the producer waits, with the full limit, for its copies that
+    // may still be in flight (the Q tile and the last nslot ring items) before
+    // the block's shared memory is given up.
+    if (warp == 4 && lane == 0 && *abort) {
+        mbar_drain(q_ready, 0);
+        for (int i = max(0, issued - nslot); i < issued; ++i) mbar_drain(&full[i % nslot], (i / nslot) & 1);
+    }
+    __syncthreads();
     if (warp == 5) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
     if (tid == 0 && *abort) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_WAIT_EXPIRED);
 }
@@ -639,7 +646,7 @@ size_t tc_smem(int d, int *nslot) {
 
 cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st) {
     k_gather_tc<<<dim3((a.nxp + 31) / 32, a.G), 256, 0, st>>>(a, a.Xk, a.XvT, a.nxp);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }
 
 cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
@@ -671,5 +678,5 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
             return cudaErrorInvalidValue;
     }
     k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh), TC_THREADS, smem, st>>>(a, mk, mv, mq, NXp, nslot);
-    return cudaPeekAtLastError();
+    return cudaGetLastError();
 }

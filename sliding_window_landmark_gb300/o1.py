@@ -91,7 +91,30 @@ def _load(path: str | None = None):
     lib.o1_state_flags.restype = ctypes.c_int
     lib.o1_status_string.argtypes = [ctypes.c_int]
     lib.o1_status_string.restype = ctypes.c_char_p
+    lib.o1_set_wait_limit.argtypes = [ctypes.c_int64]
+    lib.o1_set_wait_limit.restype = ctypes.c_int
     return lib
+
+
+def _header_defines(names):
+    """Integer #defines of include/o1.h (unsigned suffixes dropped), so that
+    the binding's constants are the header's and cannot drift from them."""
+    import re
+    text = open(os.path.join(_build.INCLUDE, "o1.h")).read()
+    out = {}
+    for n in names:
+        m = re.search(r"^#define\s+" + n + r"\s+(.+?)\s*(/\*.*)?$", text, re.M)
+        if not m:
+            raise RuntimeError(f"{n} is not defined in include/o1.h")
+        expr = re.sub(r"(\d+)[uU]", r"\1", m.group(1))
+        if not re.fullmatch(r"[\d\s()<>|+*x]+", expr):
+            raise RuntimeError(f"{n}: unexpected definition {expr!r}")
+        out[n] = int(eval(expr, {"__builtins__": {}}))
+    return out
+
+
+_DEF = _header_defines(["O1_NUM_STAGES", "O1_NOALLOC_SCRATCH_BYTES", "O1_FLAG_WAIT_EXPIRED",
+                        "O1_FLAG_FP16_RANGE", "O1_FLAG_BACK_REFUSED"])
 
 
 LIB = _load()
@@ -204,7 +227,7 @@ def o1_state_back(state, g: o1_geom, rows: int, stream=None) -> int:
     return LIB.o1_state_back(_dev(state, None, "state", dtype=None), ctypes.byref(g), int(rows), _stream(stream))
 
 
-O1_NUM_STAGES = 8
+O1_NUM_STAGES = _DEF["O1_NUM_STAGES"]
 
 
 def o1_stage_name(stage: int):
@@ -235,7 +258,7 @@ def o1_token_attend(state, g: o1_geom, scratch, q, k, v, gate, out, stream=None)
         _dev(gate, nh * g.dv, "gate"), _dev(out, nh * g.dv, "out"), _stream(stream))
 
 
-O1_NOALLOC_SCRATCH_BYTES = 4 << 20
+O1_NOALLOC_SCRATCH_BYTES = _DEF["O1_NOALLOC_SCRATCH_BYTES"]
 
 
 def o1_token_attend_noalloc(state, g: o1_geom, q, k, v, gate, out, stream=None) -> int:
@@ -280,9 +303,14 @@ def o1_state_write(state, g: o1_geom, src: dict, stream=None) -> int:
                               ctypes.byref(hv), _stream(stream))
 
 
-O1_FLAG_WAIT_EXPIRED = 1
-O1_FLAG_FP16_RANGE = 2
-O1_FLAG_BACK_REFUSED = 4
+O1_FLAG_WAIT_EXPIRED = _DEF["O1_FLAG_WAIT_EXPIRED"]
+O1_FLAG_FP16_RANGE = _DEF["O1_FLAG_FP16_RANGE"]
+O1_FLAG_BACK_REFUSED = _DEF["O1_FLAG_BACK_REFUSED"]
+
+
+def o1_set_wait_limit(cycles: int) -> int:
+    """Limit of the kernels' first waits for later calls (cycles < 1: the default)."""
+    return LIB.o1_set_wait_limit(int(cycles))
 
 
 def o1_state_flags(state, g: o1_geom, clear: bool = False, stream=None) -> int:

@@ -1,15 +1,18 @@
 """The one-row (decode) path's decomposition, restated in numpy (fp64) and
 checked against the serial oracle on the CPU.
 
-The decode kernels do not attend in one sequence. The near set after the
+The decode kernel does not attend in one sequence. The near set after the
 push (sinks, then the ring in logical order, with the pushed slot served
 from the row's own key and value) is cut into slices of KC keys, each with
-a slice-local softmax (max, mass, value sum), merged by an online max. The
-far part applies the evicted key's insert to (M, Z, T) and reads the
-updated value sums through the gains. The two meet under one exponent with
-the 1e-30 floor, and then the gate. This test takes one step that way from a
-snapshot of the oracle's state and compares it with the oracle's own next
-row, to fp64 rounding.
+a slice-local softmax (max, mass, value sum); the merge takes every slice
+against the largest slice max. The far part is cut into chunks of MB
+landmark queries: each applies the evicted key's insert to its (M, Z, T)
+and forms its share of the readout under its own exponent (the largest
+F + M'_b of the chunk): far mass and numerator; the merge moves the chunks
+to their largest exponent and sums them before the sign decision. The two
+parts meet under one exponent with the 1e-30 floor, and then the gate. This
+test takes one step that way from a snapshot of the oracle's state and
+compares it with the oracle's own next row, to fp64 rounding.
 """
 import numpy as np
 import pytest
@@ -19,7 +22,7 @@ from sliding_window_landmark_gb300 import synth
 import test_oracle_pins as pins
 
 
-def _token_step(shape, c, snap, q, k, v, gate, scale, KC):
+def _token_step(shape, c, snap, q, k, v, gate, scale, KC, MB):
     G, hpg, m, ns = shape.groups, shape.heads_per_group, shape.landmarks, shape.sinks
     p = snap["pos"]
     out = np.zeros((shape.nh, shape.dv))
@@ -44,16 +47,16 @@ def _token_step(shape, c, snap, q, k, v, gate, scale, KC):
         for hl in range(hpg):
             h = gi * hpg + hl
             qv = pins._rot(q[h], p, shape.rope_base)
-            # slices and their online merge
-            Mw, Lw, Aw = -np.inf, 0.0, np.zeros(shape.dv)
+            # slices: (max, mass, value sum) each, merged against the largest max
+            parts = []
             for i0 in range(0, len(keys), KC):
                 s = scale * keys[i0:i0 + KC] @ qv
                 ms = s.max()
                 e = np.exp(s - ms)
-                Mn = max(Mw, ms)
-                Lw = Lw * np.exp(Mw - Mn) + e.sum() * np.exp(ms - Mn)
-                Aw = Aw * np.exp(Mw - Mn) + (e @ vals[i0:i0 + KC]) * np.exp(ms - Mn)
-                Mw = Mn
+                parts.append((ms, e.sum(), e @ vals[i0:i0 + KC]))
+            Mw = max(pt[0] for pt in parts)
+            Lw = sum(pt[1] * np.exp(pt[0] - Mw) for pt in parts)
+            Aw = sum(pt[2] * np.exp(pt[0] - Mw) for pt in parts)
             # the far part: insert of the evicted key, then the readout
             cf, Df, have, num = -np.inf, 0.0, False, 0.0
             if farl + (1 if evict else 0) > 0:
@@ -71,11 +74,17 @@ def _token_step(shape, c, snap, q, k, v, gate, scale, KC):
                 F = f.max()
                 u = np.exp(f - F) @ mu[h]
                 cb = F + Mn
-                cf = cb.max()
-                gain = u * np.exp(cb - cf)
-                Df = gain @ Zn
+                # chunks of MB landmark queries, each under its own exponent
+                recs = []
+                for b0 in range(0, m, MB):
+                    sl = slice(b0, b0 + MB)
+                    cl = cb[sl].max()
+                    gl = u[sl] * np.exp(cb[sl] - cl)
+                    recs.append((cl, gl @ Zn[sl], gl @ Tn[sl]))
+                cf = max(r[0] for r in recs)
+                Df = sum(r[1] * np.exp(r[0] - cf) for r in recs)
                 have = Df >= 0
-                num = gain @ Tn
+                num = sum(r[2] * np.exp(r[0] - cf) for r in recs)
             cc = max(Mw, cf)
             al = np.exp(Mw - cc)
             be = np.exp(cf - cc) if have else 0.0
@@ -85,19 +94,20 @@ def _token_step(shape, c, snap, q, k, v, gate, scale, KC):
 
 
 @pytest.mark.parametrize("case", [
-    # (G, hpg, d, dv, ns, window, m, prompt rows, KC, rope base, seed)
-    (2, 2, 16, 8, 3, 24, 4, 60, 8, 1e6, 1),    # full ring: each step evicts
-    (1, 3, 8, 4, 2, 40, 3, 17, 8, 1e4, 2),     # ring still filling: no eviction, no far field yet
-    (1, 2, 8, 6, 0, 12, 2, 12, 16, 0.0, 3),    # the first eviction, no sinks, one slice
+    # (G, hpg, d, dv, ns, window, m, prompt rows, KC, MB, rope base, seed)
+    (2, 2, 16, 8, 3, 24, 4, 60, 8, 4, 1e6, 1),    # full ring: each step evicts; one far chunk
+    (2, 2, 16, 8, 3, 24, 7, 60, 8, 3, 1e6, 4),    # far chunks of 3, 3 and 1 landmarks
+    (1, 3, 8, 4, 2, 40, 3, 17, 8, 1, 1e4, 2),     # ring still filling: no eviction, no far field yet
+    (1, 2, 8, 6, 0, 12, 2, 12, 16, 1, 0.0, 3),    # the first eviction, no sinks, one slice
 ])
 def test_token_decomposition_equals_serial(case):
-    G, hpg, d, dv, ns, w, m, prompt, KC, base, seed = case
+    G, hpg, d, dv, ns, w, m, prompt, KC, MB, base, seed = case
     sh = synth.Shape(groups=G, heads_per_group=hpg, d=d, dv=dv, sinks=ns, window=w, landmarks=m, rope_base=base)
     lay, c, g = pins._layer(sh, seed)
     q, k, v, gt = synth.layer_rows(sh, seed, 0, prompt + 3)
     lay.rows(q[:prompt], k[:prompt], v[:prompt], gt[:prompt])
     for t in range(prompt, prompt + 3):
         snap = lay.snapshot()
-        got = _token_step(sh, c, snap, q[t], k[t], v[t], gt[t], g.scale_f32(), KC)
+        got = _token_step(sh, c, snap, q[t], k[t], v[t], gt[t], g.scale_f32(), KC, MB)
         want = lay.rows(q[t:t + 1], k[t:t + 1], v[t:t + 1], gt[t:t + 1])[0]
         np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-11)

@@ -348,18 +348,19 @@ __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
     float *Fc = a.Fb + (O1_FB_FAC * nm + wid) * a.nsub;
     const float *enter = a.Fb + O1_FB_PLANES * nm * a.nsub;
     float T = a.T[idx];
-    const float M0 = enter[wid];
-    float Mo = M0;
+    float Mo = enter[wid];
+    o1_ff Zo = ff_make(col0 ? enter[nm + wid] : 0.f, col0 ? enter[2 * nm + wid] : 0.f);
     // 8 blocks' loads issued before their stores (the compiler cannot
     // reorder them itself: the stores may alias later loads for all it knows);
     // few enough registers for the scan to sit beside a window CTA
     for (int c0 = 0; c0 < a.nsub; c0 += 8) {
-        float lm[8], dT[8];
+        float lm[8], dT[8], ls[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int c = c0 + i;
             lm[i] = c < a.nsub ? lmax[c] : -INFINITY;
             dT[i] = c < a.nsub ? a.Tp[(size_t)c * n + idx] : 0.f;
+            ls[i] = (col0 && c < a.nsub) ? lsum[c] : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -371,36 +372,27 @@ __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
                 const float Ts = Rf * T;
                 a.Tp[(size_t)c * n + idx] = Ts;
                 T = f != 0.f ? fmaf(f, dT[i], Ts) : Ts;
+                if (col0) {
+                    // the mass in float-float; M_c, R_c Z_{c-1} (high, low)
+                    // and f_c for the side readout
+                    const o1_ff base = ff_mul_f(Zo, Rf);
+                    Mc[c] = Mn;
+                    Bc[c] = base.hi;
+                    Bl[c] = base.lo;
+                    Fc[c] = f;
+                    Zo = ff_fma_f(base, f, ls[i]);
+                }
                 Mo = Mn;
             }
         }
     }
-    if (col0) {
-        // the running max again, with the mass in float-float: M_c, R_c Z_{c-1}
-        // (high, low) and f_c per block for the side readout
-        o1_ff Zo = ff_make(enter[nm + wid], enter[2 * nm + wid]);
-        float Mr = M0;
-        for (int c = 0; c < a.nsub; ++c) {
-            const float lm = lmax[c];
-            const float Mn = fmaxf(Mr, lm);
-            const float Rf = Mn == Mr ? 1.f : expf(Mr - Mn);
-            const float f = lm == -INFINITY ? 0.f : expf(lm - Mn);
-            const o1_ff base = ff_mul_f(Zo, Rf);
-            Mc[c] = Mn;
-            Bc[c] = base.hi;
-            Bl[c] = base.lo;
-            Fc[c] = f;
-            Zo = ff_fma_f(base, f, lsum[c]);
-            Mr = Mn;
-        }
-        if (a.commit) {
-            a.M[wid] = Mr;
-            a.Z[wid] = Zo.hi;
-            a.Zlo[wid] = Zo.lo;
-        }
-    }
     if (!a.commit) return;   // attend only: the state keeps its far field
     a.T[idx] = T;
+    if (col0) {
+        a.M[wid] = Mo;
+        a.Z[wid] = Zo.hi;
+        a.Zlo[wid] = Zo.lo;
+    }
 }
 
 // The side part of every row of block c for head gh: the sinks and the far

@@ -110,9 +110,11 @@ __device__ __forceinline__ void tok_cs(const O1Args &a, float inv, long long p, 
 
 // Dot products of shared-memory rows (d floats each) with `nq` vectors (d
 // floats, `qstride` apart), lane = row, warp = a contiguous share of d in
-// float4 units, visited from a lane-dependent start so that the 8 lanes of a
-// quarter warp read 8 different bank groups. Returns the warp's partial dots
-// in acc[0 .. nq-1] (0 for an invalid row).
+// float4 units (U = d / 32 of them, at most 8), visited from a lane-dependent
+// start so that the lanes of a quarter warp read different bank groups.
+// Returns the warp's partial dots in acc[0 .. nq-1] (0 for an invalid row).
+// A runtime loop over the warp's units keeps the code short: the kernel is
+// latency-bound and its instruction fetch shows.
 template <int NQ>
 __device__ __forceinline__ void tok_dots(const float *rows, int row, bool valid, const float *qs, int qstride,
                                          int nq, int d, float (&acc)[NQ]) {
@@ -123,28 +125,19 @@ __device__ __forceinline__ void tok_dots(const float *rows, int row, bool valid,
     for (int h = 0; h < NQ; ++h) acc[h] = 0.f;
     if (!valid) return;
     const float4 *kr = (const float4 *)(rows + (size_t)row * d);
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 kv[8];
-    int us[8];
-    int s = lane % U;
+    int sidx = lane % U;
+#pragma unroll 2
+    for (int t = 0; t < U; ++t) {
+        const int u = ub + sidx;
+        if (++sidx == U) sidx = 0;
+        if (u >= nu) continue;
+        const float4 kv = kr[u];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        us[t] = ub + s;
-        kv[t] = (t < U && us[t] < nu) ? kr[us[t]] : z;
-        if (++s == U) s = 0;
-    }
-#pragma unroll
-    for (int h = 0; h < NQ; ++h) {
-        if (h >= nq) break;
-        const float4 *qh = (const float4 *)(qs + (size_t)h * qstride);
-        float4 qv[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) qv[t] = (t < U && us[t] < nu) ? qh[us[t]] : z;
-        float a0 = 0.f;
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            a0 = fmaf(qv[t].x, kv[t].x, fmaf(qv[t].y, kv[t].y, fmaf(qv[t].z, kv[t].z, fmaf(qv[t].w, kv[t].w, a0))));
-        acc[h] = a0;
+        for (int h = 0; h < NQ; ++h) {
+            if (h >= nq) break;
+            const float4 qv = ((const float4 *)(qs + (size_t)h * qstride))[u];
+            acc[h] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[h]))));
+        }
     }
 }
 
@@ -303,15 +296,17 @@ __device__ __forceinline__ void tok_cp_wait() {
 // the push and the commit), the gate logits of the group's heads (for a
 // merge), and the rotated queries of `nq` heads from head q0. Issued right
 // after the wait (tok_inputs_load), finished once the position is known.
+template <int HPG>
 struct TokIn {
-    float x0[O1_MAX_HPG + 1], x1[O1_MAX_HPG + 1];
+    float x0[HPG + 1], x1[HPG + 1];
 };
-__device__ __forceinline__ void tok_inputs_load(const O1Args &a, int g, int q0, int nq, TokIn &in, float *svr,
+template <int HPG>
+__device__ __forceinline__ void tok_inputs_load(const O1Args &a, int g, int q0, int nq, TokIn<HPG> &in, float *svr,
                                                 float *sgt) {
     const int tid = threadIdx.x, d = a.d, dv = a.dv, half = d >> 1;
     const bool rj = tid < half;
 #pragma unroll
-    for (int h = 0; h <= O1_MAX_HPG; ++h) {
+    for (int h = 0; h <= HPG; ++h) {
         const float *src = h < nq ? a.q + (size_t)(q0 + h) * d : a.k + (size_t)g * d;
         const bool ok = rj && h <= nq;
         in.x0[h] = ok ? src[tid] : 0.f;
@@ -322,12 +317,13 @@ __device__ __forceinline__ void tok_inputs_load(const O1Args &a, int g, int q0, 
         for (int t = tid; t < ((a.hpg * dv) >> 2); t += blockDim.x)
             tok_cp16(sgt + 4 * t, a.gate + (size_t)g * a.hpg * dv + 4 * t);
 }
-__device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int nq, float cs, float sn, const TokIn &in,
+template <int HPG>
+__device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int nq, float cs, float sn, const TokIn<HPG> &in,
                                                   float *sq, float *sk) {
     const int tid = threadIdx.x, d = a.d, half = d >> 1;
     if (tid < half) {
 #pragma unroll
-        for (int h = 0; h <= O1_MAX_HPG; ++h) {
+        for (int h = 0; h <= HPG; ++h) {
             if (h > nq) break;
             float *dst = h < nq ? sq + h * d : sk;
             dst[tid] = in.x0[h] * cs - in.x1[h] * sn;
@@ -338,6 +334,7 @@ __device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int nq, float
 
 // A near slice: scores of every head of the group over the slice's keys, a
 // slice-local softmax and the value sums -> partial (max, sum, value sum).
+template <int HPG>
 __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Meta &mt, const TokNearSm &s) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.d, dv = a.dv, hpg = a.hpg, KC = a.KC;
@@ -365,44 +362,35 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
     __syncthreads();
     // scores: partial dots per warp (lane = key) over the warp's share of d
     for (int k0 = 0; k0 < cnt; k0 += 32) {
-        float acc[O1_MAX_HPG];
+        float acc[HPG];
         const int key = k0 + lane;
         tok_dots(s.sK, key, key < cnt, s.sq, d, hpg, d, acc);
         if (key < cnt)
 #pragma unroll
-            for (int h = 0; h < O1_MAX_HPG; ++h) {
+            for (int h = 0; h < HPG; ++h) {
                 if (h >= hpg) break;
                 s.sP[((size_t)warp * KC + key) * hpg + h] = acc[h];
             }
     }
     __syncthreads();
-    // per head (a warp each): the partials' sums, the slice max, the weights
-    // e^{s - max} and their sum, in one pass over the keys held in registers
+    // per head (a warp each): the partials' sums and the slice max, then the
+    // weights e^{s - max} and their sum
     for (int h = warp; h < hpg; h += blockDim.x >> 5) {
-        float sc[8];
         float mx = -INFINITY;
+        for (int i = lane; i < cnt; i += 32) {
+            float acc = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = lane + 32 * u;
-            sc[u] = -INFINITY;
-            if (i < cnt) {
-                float acc = 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) acc += s.sP[((size_t)w * KC + i) * hpg + h];
-                sc[u] = acc * a.scale;
-                mx = fmaxf(mx, sc[u]);
-            }
+            for (int w = 0; w < 8; ++w) acc += s.sP[((size_t)w * KC + i) * hpg + h];
+            acc *= a.scale;
+            s.sS[i * hpg + h] = acc;
+            mx = fmaxf(mx, acc);
         }
         mx = warp_max(mx);
         float l = 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = lane + 32 * u;
-            if (i < cnt) {
-                const float e = expf(sc[u] - mx);
-                s.sS[i * hpg + h] = e;
-                l += e;
-            }
+        for (int i = lane; i < cnt; i += 32) {
+            const float e = expf(s.sS[i * hpg + h] - mx);
+            s.sS[i * hpg + h] = e;
+            l += e;
         }
         l = warp_sum(l);
         if (lane == 0) {
@@ -582,10 +570,11 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
 // flight at once, the threads split over slice groups when there are more
 // threads than (head, 4 columns); nothing in shared memory grows with the
 // number of slices.
+template <int HPG>
 __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, const float *sgt, float *smg) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv, dv4 = dv >> 2;
-    int heads[O1_MAX_HPG];
+    int heads[HPG];
     int nS = 0;
     for (int hl = 0; hl < hpg; ++hl)
         if (mine & (1u << hl)) heads[nS++] = hl;
@@ -750,6 +739,7 @@ __device__ void tok_commit(const O1Args &a, long long p, float *smg) {
 
 }  // namespace
 
+template <int HPG>
 __global__ __launch_bounds__(256) void k_tok(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     __shared__ long long s_pos;
@@ -808,9 +798,9 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
     // The row's inputs and the position check go out in one round.
     tok_wait_primary();
     tok_allow_dependents();
-    TokIn in;
-    if (ro.far) tok_inputs_load(a, ro.g, ro.h, 1, in, svr, sgt);
-    else tok_inputs_load(a, ro.g, ro.g * a.hpg, a.hpg, in, svr, sgt);
+    TokIn<HPG> in;
+    if (ro.far) tok_inputs_load<HPG>(a, ro.g, ro.h, 1, in, svr, sgt);
+    else tok_inputs_load<HPG>(a, ro.g, ro.g * a.hpg, a.hpg, in, svr, sgt);
     float Mo = -INFINITY;
     o1_ff Zo = ff_make(0.f, 0.f);
     const int b0 = ro.fc * a.MB, nbf = ro.far ? max(0, min(a.MB, a.m - b0)) : 0;
@@ -853,27 +843,27 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
     const bool evict = mt.len0 == mt.wg;
     const int farl1 = mt.farl0 + (evict ? 1 : 0);
     if (p != pguess && tid < (a.d >> 1)) tok_cs(a, inv, p, cs, sn);
-    tok_inputs_finish(a, ro.far ? 1 : a.hpg, cs, sn, in, sq, sk);
+    tok_inputs_finish<HPG>(a, ro.far ? 1 : a.hpg, cs, sn, in, sq, sk);
     tok_cp_wait();
     tok_wait_copies(a, bar, (uint32_t)s_parity);
     __syncthreads();
     if (ro.far) tok_far_compute(a, ro, mt, fs, Mo, Zo);
-    else tok_near_compute(a, ro, mt, ns);
+    else tok_near_compute<HPG>(a, ro, mt, ns);
 
     // ---- arrival: the last CTA for a head merges it; the last of all commits
     __syncthreads();   // every partial and record of this CTA is written
     if (tid == 0) {
         __threadfence();
         const unsigned total = (unsigned)(a.NC + a.NF);
-        unsigned r[O1_MAX_HPG];
+        unsigned r[HPG];
         const int nt = ro.far ? 1 : a.hpg;
         const unsigned base = ro.far ? (unsigned)ro.h : (unsigned)(ro.g * a.hpg);
 #pragma unroll
-        for (int i = 0; i < O1_MAX_HPG; ++i) r[i] = i < nt ? atomicAdd(a.tick + base + i, 1u) : 0u;
+        for (int i = 0; i < HPG; ++i) r[i] = i < nt ? atomicAdd(a.tick + base + i, 1u) : 0u;
         const unsigned ra = atomicAdd(a.tick + a.nh + a.G, 1u);
         unsigned mine = 0;
 #pragma unroll
-        for (int i = 0; i < O1_MAX_HPG; ++i)
+        for (int i = 0; i < HPG; ++i)
             if (i < nt && r[i] == total - 1) mine |= 1u << (ro.far ? ro.hl : i);
         const bool last = ra == gridDim.x - 1;
         if (mine || last) __threadfence();
@@ -883,23 +873,26 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
         s_last = last;
     }
     __syncthreads();
-    if (s_mine) tok_merge(a, ro.g, s_mine, farl1, sgt, smg);
+    if (s_mine) tok_merge<HPG>(a, ro.g, s_mine, farl1, sgt, smg);
     if (s_last) {
         __syncthreads();
         tok_commit(a, p, smg);
     }
 }
 
-cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
+// One instance of the kernel per power of two of heads per group (the
+// smallest at least hpg), so that nothing is unrolled to the largest count.
+template <int HPG>
+static cudaError_t tok_launch(const O1Args &a, cudaStream_t st) {
     static unsigned long long done = 0;
     static size_t dyn_max = 0;   // the kernel's static shared memory taken off the 227 KB a block may hold
     unsigned long long bit = 0;
     if (o1_attrs_needed(&done, &bit)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, k_tok);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_tok<HPG>);
         if (e != cudaSuccess) return e;
         const size_t dmax = 227 * 1024 - fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(k_tok, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
+        e = cudaFuncSetAttribute(k_tok<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
         if (e != cudaSuccess) return e;
         __atomic_store_n(&dyn_max, dmax, __ATOMIC_RELAXED);
         o1_attrs_done(&done, bit);
@@ -915,6 +908,14 @@ cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, k_tok, a);
+    cudaLaunchKernelEx(&cfg, k_tok<HPG>, a);
     return cudaGetLastError();
+}
+
+cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
+    if (a.hpg <= 1) return tok_launch<1>(a, st);
+    if (a.hpg <= 2) return tok_launch<2>(a, st);
+    if (a.hpg <= 4) return tok_launch<4>(a, st);
+    if (a.hpg <= 8) return tok_launch<8>(a, st);
+    return tok_launch<16>(a, st);
 }

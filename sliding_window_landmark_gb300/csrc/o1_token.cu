@@ -423,7 +423,7 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
 // readout's share: F and e^{f - F} over every landmark key, u_b, the chunk's
 // exponent c_f = max_b (F + M'_b), gains, the chunk's far mass (float-float) and
 // numerator -> the far record (c_f, D, numerator), all relative to c_f.
-// Warp 2, lane b, holds the chunk's entering M and Z (Mo, Zo).
+// Warp 1, lane b, holds the chunk's entering M and Z (Mo, Zo).
 __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta &mt, const TokFarSm &s, float Mo,
                                 o1_ff Zo) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -432,7 +432,7 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
     const int farl1 = mt.farl0 + (evict ? 1 : 0);
     const int b0 = ro.fc * MB, nb = max(0, min(MB, m - b0));
     float *fp = a.farp + ((size_t)h * a.NF + ro.fc) * (4 + dv);
-    __shared__ float s_F, s_cf, s_Dh, s_Dl;
+    __shared__ float s_Dh, s_Dl;
     if (farl1 == 0 || nb == 0) {   // no far field, or no landmark here: an empty record
         for (int t = tid; t < dv; t += blockDim.x) fp[4 + t] = 0.f;
         if (tid == 0) {
@@ -455,8 +455,12 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
         if (lane < nb) s.sPl[warp * MB + lane] = l1[0];
     }
     __syncthreads();
-    if (warp == 0) {
-        // the readout's landmark scores: F = max_a f_a and e^{f_a - F}
+    // Every warp: F = max_a f_a and e^{f_a - F} for a = lane, lane + 32 (the
+    // same in each warp, so that no warp waits for another); then u_b for its
+    // share of the chunk's landmarks (b = warp, warp + 8, ...), a warp sum
+    // over a each. Warp 1 also takes the insert, lane = b.
+    float F;
+    {
         float f0 = -INFINITY, f1 = -INFINITY;
         if (lane < m) {
             float acc = 0.f;
@@ -470,11 +474,18 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
             for (int w = 0; w < 8; ++w) acc += s.sPf[w * m + lane + 32];
             f1 = acc * a.scale;
         }
-        const float F = warp_max(fmaxf(f0, f1));
-        if (lane < m) s.sF[lane] = expf(f0 - F);
-        if (lane + 32 < m) s.sF[lane + 32] = expf(f1 - F);
-        if (lane == 0) s_F = F;
-    } else if (warp == 2 && lane < nb) {
+        F = warp_max(fmaxf(f0, f1));
+        const float e0 = lane < m ? expf(f0 - F) : 0.f, e1 = lane + 32 < m ? expf(f1 - F) : 0.f;
+        for (int b = warp; b < nb; b += 8) {
+            float part = 0.f;
+            if (lane < m) part = e0 * s.smu[lane * MB + b];
+            if (lane + 32 < m) part = fmaf(e1, s.smu[(lane + 32) * MB + b], part);
+            float u = warp_sum(part);
+            if (a.rect) u = fmaxf(u, 0.f);
+            if (lane == 0) s.sG[b] = u;   // u_b here; the gain is formed from it below
+        }
+    }
+    if (warp == 1 && lane < nb) {
         // the insert of the evicted key for landmark query b = b0 + lane
         float Mn = Mo, rho = 1.f, e = 0.f;
         o1_ff Zn = Zo;
@@ -499,40 +510,20 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
         s.sZl[lane] = Zn.lo;
     }
     __syncthreads();
-    // u_b = sum_a e^{f_a - F} mu[a][b]: thread (k, b) sums a = k, k + 8, ...
-    {
-        const int b = tid % MB, k = tid / MB;
-        if (k < 8 && b < nb) {
-            float acc = 0.f;
-            for (int aa = k; aa < m; aa += 8) acc = fmaf(s.sF[aa], s.smu[aa * MB + b], acc);
-            s.sPl[k * MB + b] = acc;
-        }
-    }
-    __syncthreads();
+    // Every warp: the chunk's exponent c_f = max_b (F + M'_b). Gains
+    // g_b = u_b e^{F + M'_b - c_f}; warp 0 sums the chunk's far mass
+    // D = sum_b g_b Z_b in float-float (its terms can cancel to a small
+    // fraction of their size); every thread inserts the evicted value into
+    // its share of T, writes T back and forms partial far numerators.
+    const float cf = warp_max(lane < nb ? F + s.sMn[lane] : -INFINITY);
     if (warp == 0) {
-        const bool in = lane < nb;
-        float u = 0.f;
-        if (in) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) u += s.sPl[k * MB + lane];
-            if (a.rect) u = fmaxf(u, 0.f);
-        }
-        const float cb = in ? s_F + s.sMn[lane] : -INFINITY;
-        const float cf = warp_max(cb);
-        const float gn = in ? u * expf(cb - cf) : 0.f;
-        if (in) s.sG[lane] = gn;
-        // the chunk's far mass in float-float: the terms can cancel to a
-        // small fraction of their size
-        const o1_ff D = warp_sum(in ? ff_mul_f(ff_make(s.sZh[lane], s.sZl[lane]), gn) : ff_make(0.f, 0.f));
+        const float gn = lane < nb ? s.sG[lane] * expf(F + s.sMn[lane] - cf) : 0.f;
+        const o1_ff D = warp_sum(lane < nb ? ff_mul_f(ff_make(s.sZh[lane], s.sZl[lane]), gn) : ff_make(0.f, 0.f));
         if (lane == 0) {
-            s_cf = cf;
             s_Dh = D.hi;
             s_Dl = D.lo;
         }
     }
-    __syncthreads();
-    // the value sums: thread = (column t, landmark group lg); insert the
-    // evicted value, write T back, partial far numerators, then their sum
     const int nlg = blockDim.x / dv, t = tid % dv, lg = tid / dv;
     if (lg < nlg) {
         const float vt = evict ? s.sve[t] : 0.f;
@@ -543,7 +534,7 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
                 x = s.sRho[b] * x + s.sE[b] * vt;
                 a.T[((size_t)h * m + b0 + b) * dv + t] = x;
             }
-            acc = fmaf(s.sG[b], x, acc);
+            acc = fmaf(s.sG[b] * expf(F + s.sMn[b] - cf), x, acc);
         }
         s.sNum[lg * dv + t] = acc;
     }
@@ -554,7 +545,7 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
         fp[4 + c] = acc;
     }
     if (tid == 0) {
-        fp[0] = s_cf;
+        fp[0] = cf;
         fp[2] = s_Dh;
         fp[3] = s_Dl;
     }
@@ -804,7 +795,7 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
     float Mo = -INFINITY;
     o1_ff Zo = ff_make(0.f, 0.f);
     const int b0 = ro.fc * a.MB, nbf = ro.far ? max(0, min(a.MB, a.m - b0)) : 0;
-    if (warp == 2 && lane < nbf) {   // the far chunk's entering max and mass
+    if (warp == 1 && lane < nbf) {   // the far chunk's entering max and mass (the insert's warp)
         const size_t at = (size_t)ro.h * a.m + b0 + lane;
         Mo = a.M[at];
         Zo = ff_make(a.Z[at], a.Zlo[at]);

@@ -171,6 +171,7 @@ __device__ __forceinline__ TokRole tok_role(const O1Args &a) {
 struct TokNear {
     bool evict;
     int len1, head1, n, i0, cnt;
+    int ipush;   // the slice's index of the pushed key (the near set's last), or -1
 };
 
 __device__ __forceinline__ TokNear tok_near_plan(const O1Args &a, const O1Meta &mt, int c) {
@@ -181,6 +182,7 @@ __device__ __forceinline__ TokNear tok_near_plan(const O1Args &a, const O1Meta &
     p.n = a.ns + p.len1;
     p.i0 = c * a.KC;
     p.cnt = max(0, min(a.KC, p.n - p.i0));
+    p.ipush = (p.cnt > 0 && p.i0 + p.cnt == p.n) ? p.cnt - 1 : -1;
     return p;
 }
 
@@ -245,13 +247,17 @@ __device__ void tok_issue(const O1Args &a, const TokRole &ro, const O1Meta &mt, 
         const TokNearSm s = tok_near_sm(a, sm);
         const TokNear p = tok_near_plan(a, mt, ro.c);
         // sinks, then ring logical indices as at most two contiguous runs
-        // (to the ring's end, from slot 0), one bulk copy each for K and V
-        const int nsk = max(0, min(p.cnt, a.ns - p.i0));
+        // (to the ring's end, from slot 0), one bulk copy each for K and V.
+        // The pushed key (the near set's last, always a ring key) is not
+        // copied: this row overwrites its slot, and tok_inputs_finish puts
+        // the row's own rotated key and value in its place.
+        const int ccopy = p.ipush >= 0 ? p.cnt - 1 : p.cnt;
+        const int nsk = max(0, min(ccopy, a.ns - p.i0));
         if (nsk > 0) {
             tok_bulk(s.sK, a.sink_k + ((size_t)ro.g * a.ns + p.i0) * d, (uint32_t)nsk * d * 4, s.bar);
             tok_bulk(s.sV, a.sink_v + ((size_t)ro.g * a.ns + p.i0) * dv, (uint32_t)nsk * dv * 4, s.bar);
         }
-        const int nr = p.cnt - nsk;
+        const int nr = ccopy - nsk;
         if (nr > 0) {
             const int L0 = p.i0 + nsk - a.ns;
             const int s0 = (p.head1 + L0) % mt.wg;
@@ -317,19 +323,30 @@ __device__ __forceinline__ void tok_inputs_load(const O1Args &a, int g, int q0, 
         for (int t = tid; t < ((a.hpg * dv) >> 2); t += blockDim.x)
             tok_cp16(sgt + 4 * t, a.gate + (size_t)g * a.hpg * dv + 4 * t);
 }
+// A near slice holding the pushed key gets the row's rotated key and value
+// in that key's place (kpush, vpush; null otherwise). Called after the
+// copies of a stale prefetch have landed, so that none overwrites them.
 template <int HPG>
-__device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int nq, float cs, float sn, const TokIn<HPG> &in,
-                                                  float *sq, float *sk) {
+__device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int g, int nq, float cs, float sn,
+                                                  const TokIn<HPG> &in, float *sq, float *sk, float *kpush,
+                                                  float *vpush) {
     const int tid = threadIdx.x, d = a.d, half = d >> 1;
     if (tid < half) {
 #pragma unroll
         for (int h = 0; h <= HPG; ++h) {
             if (h > nq) break;
             float *dst = h < nq ? sq + h * d : sk;
-            dst[tid] = in.x0[h] * cs - in.x1[h] * sn;
-            dst[tid + half] = in.x1[h] * cs + in.x0[h] * sn;
+            const float y0 = in.x0[h] * cs - in.x1[h] * sn, y1 = in.x1[h] * cs + in.x0[h] * sn;
+            dst[tid] = y0;
+            dst[tid + half] = y1;
+            if (h == nq && kpush) {
+                kpush[tid] = y0;
+                kpush[tid + half] = y1;
+            }
         }
     }
+    if (vpush)
+        for (int t = tid; t < (a.dv >> 2); t += blockDim.x) tok_cp16(vpush + 4 * t, a.v + (size_t)g * a.dv + 4 * t);
 }
 
 // A near slice: scores of every head of the group over the slice's keys, a
@@ -352,14 +369,7 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
         }
         return;
     }
-    // the last logical key is the pushed one: its ring slot is overwritten
-    // by this row, so it is served from the row's own rotated key and value
-    const int ipush = a.ns + p.len1 - 1 - p.i0;
-    if (ipush >= 0 && ipush < cnt) {
-        for (int j = tid; j < d; j += blockDim.x) s.sK[(size_t)ipush * d + j] = s.sk[j];
-        for (int j = tid; j < dv; j += blockDim.x) s.sV[(size_t)ipush * dv + j] = s.svr[j];
-    }
-    __syncthreads();
+    // (the pushed key's row holds the row's own rotated key and value)
     // scores: partial dots per warp (lane = key) over the warp's share of d
     for (int k0 = 0; k0 < cnt; k0 += 32) {
         float acc[HPG];
@@ -834,7 +844,15 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
     const bool evict = mt.len0 == mt.wg;
     const int farl1 = mt.farl0 + (evict ? 1 : 0);
     if (p != pguess && tid < (a.d >> 1)) tok_cs(a, inv, p, cs, sn);
-    tok_inputs_finish<HPG>(a, ro.far ? 1 : a.hpg, cs, sn, in, sq, sk);
+    float *kpush = nullptr, *vpush = nullptr;
+    if (!ro.far) {
+        const int ip = tok_near_plan(a, mt, ro.c).ipush;
+        if (ip >= 0) {
+            kpush = ns.sK + (size_t)ip * a.d;
+            vpush = ns.sV + (size_t)ip * a.dv;
+        }
+    }
+    tok_inputs_finish<HPG>(a, ro.g, ro.far ? 1 : a.hpg, cs, sn, in, sq, sk, kpush, vpush);
     tok_cp_wait();
     tok_wait_copies(a, bar, (uint32_t)s_parity);
     __syncthreads();

@@ -169,24 +169,34 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
 
 // Shared memory (floats) of a near slice and of a far chunk, and of the
 // merge scratch that follows either; the kernel carves the same offsets.
-// The merge of up to hpg heads: per head NF far record factors and 8
-// scalars, then (16-byte aligned) 256 float4 partials for combining slice
-// groups; nothing per near slice. The step's commit reuses it for one slot
-// index per group.
-__host__ __device__ inline size_t o1_tok_merge_floats(int hpg, int NF, int G) {
-    const size_t mg = (size_t)hpg * (NF + 8) + 4 + 4 * 256;
-    return mg > (size_t)G ? mg : (size_t)G;
+// After its own work a CTA may merge heads and commit the step: the merge
+// stages the rows it reads (the near partials and far numerators, NC + NF
+// rows of dv floats per head) in the part of shared memory the work used
+// (from the near slice's keys, or the far chunk's landmark queries, up to
+// the merge scratch), after their factors [heads][NC + NF]. That part is
+// made at least one row per head plus the factors (o1_tok_stage_min). The
+// merge scratch holds 8 scalars per head and one slot index per group.
+__host__ __device__ inline size_t o1_tok_merge_floats(int hpg, int G) { return (size_t)8 * hpg + G + 4; }
+__host__ __device__ inline size_t o1_tok_stage_min(int hpg, int NC, int NF, int dv) {
+    return ((size_t)hpg * (NC + NF) + 3) / 4 * 4 + (size_t)hpg * dv;
 }
-__host__ __device__ inline size_t o1_tok_near_floats(int d, int dv, int hpg, int KC, int NF, int G) {
-    return 4 + (size_t)hpg * d + d + dv + (size_t)hpg * dv + (size_t)KC * (d + dv) + (size_t)KC * hpg +
-           (size_t)8 * KC * hpg + o1_tok_merge_floats(hpg, NF, G);
+__host__ __device__ inline size_t o1_tok_near_region(int d, int dv, int hpg, int KC) {
+    return (size_t)KC * (d + dv) + (size_t)KC * hpg + (size_t)8 * KC * hpg;
 }
-// (the merge scratch of a far chunk starts 4-aligned: 4 + m MB + 8 m + 2 m
-// rounds up to a multiple of 4 through the 3 floats of slack after it)
-__host__ __device__ inline size_t o1_tok_far_floats(int d, int dv, int hpg, int m, int MB, int NF, int G) {
-    return 4 + 3 * (size_t)d + 2 * (size_t)dv + (size_t)hpg * dv + (size_t)MB * d + (size_t)m * d +
-           (size_t)MB * dv + (size_t)m * MB + 8 * (size_t)m + 8 * (size_t)MB + 2 * (size_t)m + 8 * (size_t)MB +
-           256 + 3 + o1_tok_merge_floats(hpg, NF, G);
+__host__ __device__ inline size_t o1_tok_near_floats(int d, int dv, int hpg, int KC, int NC, int NF, int G) {
+    const size_t r = o1_tok_near_region(d, dv, hpg, KC), st = o1_tok_stage_min(hpg, NC, NF, dv);
+    return 4 + (size_t)hpg * d + d + dv + (size_t)hpg * dv + (r > st ? r : st) + o1_tok_merge_floats(hpg, G);
+}
+// (from the landmark queries to the end of the numerator partials; the
+// merge scratch after it starts 16-byte aligned, through 3 floats of slack)
+__host__ __device__ inline size_t o1_tok_far_region(int d, int dv, int m, int MB) {
+    return (size_t)MB * d + (size_t)m * d + (size_t)MB * dv + (size_t)m * MB + 8 * (size_t)m + 8 * (size_t)MB +
+           2 * (size_t)m + 8 * (size_t)MB + 256;
+}
+__host__ __device__ inline size_t o1_tok_far_floats(int d, int dv, int hpg, int m, int MB, int NC, int NF, int G) {
+    const size_t r = o1_tok_far_region(d, dv, m, MB), st = o1_tok_stage_min(hpg, NC, NF, dv);
+    return 4 + 3 * (size_t)d + 2 * (size_t)dv + (size_t)hpg * dv + (r > st ? r : st) + 3 +
+           o1_tok_merge_floats(hpg, G);
 }
 
 // Scratch of the one-row path: near partials per (group, slice, head), the
@@ -214,12 +224,12 @@ static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     long long MB = (m + NF - 1) / NF;
     if (MB > O1_TOK_MB_MAX) MB = O1_TOK_MB_MAX;
     const long long cap = O1_TOK_SMEM_CAP / 4;
-    // the merge scratch depends on NC, which is not known yet: size the far
-    // chunk with a bound on it (at most O1_TOK_CTAS slices a group). Chunks
+    // the merge's staging depends on NC, which is not known yet: size the
+    // far chunk with a bound on it (at most O1_TOK_CTAS slices a group). Chunks
     // stay at 8 landmarks or more: below that the parts every chunk holds
     // whole (landmark keys, gate, merge scratch) dominate, and more chunks
     // only repeat them; such a CTA just takes more than the cap.
-    while (MB > 8 && (long long)o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB,
+    while (MB > 8 && (long long)o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB, O1_TOK_CTAS,
                                                    (int)((m + MB - 1) / MB), (int)G) > cap)
         MB = (MB + 1) / 2;
     NF = (m + MB - 1) / MB;
@@ -230,7 +240,7 @@ static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     KC = KC < 8 ? 8 : (KC + 7) / 8 * 8;
     if (KC > 256) KC = 256;   // a slice's keys sit in a warp's registers, 8 per lane
     long long NC = (nnear + KC - 1) / KC;
-    while (KC > 8 && (long long)o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NF, (int)G) > cap) {
+    while (KC > 8 && (long long)o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NC, (int)NF, (int)G) > cap) {
         KC -= 8;
         NC = (nnear + KC - 1) / KC;
     }
@@ -239,8 +249,8 @@ static inline O1TokScratch o1_tok_layout(const o1_geom &g) {
     S.NC = (int)NC;
     S.NF = (int)NF;
     S.MB = (int)MB;
-    const size_t nf = o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB, (int)NF, (int)G);
-    const size_t nn = o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NF, (int)G);
+    const size_t nf = o1_tok_far_floats((int)d, (int)dv, (int)hpg, (int)m, (int)MB, (int)NC, (int)NF, (int)G);
+    const size_t nn = o1_tok_near_floats((int)d, (int)dv, (int)hpg, (int)KC, (int)NC, (int)NF, (int)G);
     S.smem = 4 * (nf > nn ? nf : nn);
     size_t off = 0;
     S.part = off; off += o1_al256((size_t)G * NC * hpg * dv * 4);

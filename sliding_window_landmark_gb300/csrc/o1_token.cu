@@ -202,7 +202,9 @@ __device__ __forceinline__ TokNearSm tok_near_sm(const O1Args &a, float *sm) {
     s.sV = s.sK + (size_t)a.KC * a.d;       // [KC][dv]
     s.sS = s.sV + (size_t)a.KC * a.dv;      // [KC][hpg]  scores, then weights
     s.sP = s.sS + (size_t)a.KC * a.hpg;     // [8][KC][hpg] partial dots
-    s.smg = s.sP + (size_t)8 * a.KC * a.hpg;
+    // the merge's staging reuses sK onwards; the merge scratch follows it
+    const size_t r = o1_tok_near_region(a.d, a.dv, a.hpg, a.KC), st = o1_tok_stage_min(a.hpg, a.NC, a.NF, a.dv);
+    s.smg = s.sK + (r > st ? r : st);
     return s;
 }
 
@@ -236,7 +238,10 @@ __device__ __forceinline__ TokFarSm tok_far_sm(const O1Args &a, float *sm) {
     s.sZh = s.sMn + MB;                     // [MB]      far mass after the insert, high part
     s.sZl = s.sZh + MB;                     // [MB]      and low part
     s.sNum = s.sG + 8 * MB;                 // [256]     numerator partials
-    s.smg = (float *)(((uintptr_t)(s.sNum + 256) + 15) & ~(uintptr_t)15);   // 16-byte aligned
+    // the merge's staging reuses sqt onwards; the merge scratch follows it,
+    // 16-byte aligned
+    const size_t r = o1_tok_far_region(d, dv, m, MB), st = o1_tok_stage_min(a.hpg, a.NC, a.NF, dv);
+    s.smg = (float *)(((uintptr_t)(s.sqt + (r > st ? r : st)) + 15) & ~(uintptr_t)15);
     return s;
 }
 
@@ -362,11 +367,13 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
     float *pml = a.pml + slot * 2;    // [hpg][2]
     if (ro.c == 0)   // the group's rotated key, for the commit
         for (int j = tid; j < d; j += blockDim.x) a.kcur[(size_t)ro.g * d + j] = s.sk[j];
-    if (cnt == 0) {
+    if (cnt == 0) {   // an empty slice: zero weight, and zero sums (the merge reads every row)
         for (int h = tid; h < hpg; h += blockDim.x) {
             pml[2 * h] = -INFINITY;
             pml[2 * h + 1] = 0.f;
         }
+        for (int i = tid; i < ((hpg * dv) >> 2); i += blockDim.x)
+            ((float4 *)pv)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
     // (the pushed key's row holds the row's own rotated key and value)
@@ -561,34 +568,105 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
     }
 }
 
+// Bulk copy without its own expect-tx: the bytes of a batch of them are
+// announced once on the barrier (tok_merge_issue).
+__device__ __forceinline__ void tok_bulk_nx(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     tok_su32(dst)),
+                 "l"((uint64_t)src), "r"(bytes), "r"(tok_su32(bar))
+                 : "memory");
+}
+// Barrier 1 over the first `nthr` threads (the merge's; barrier 0 is the CTA's).
+__device__ __forceinline__ void tok_bar_merge(int nthr) { asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory"); }
+// The si-th head (0-based, in order) of the set `mine`.
+__device__ __forceinline__ int tok_nth_head(unsigned mine, int si) {
+    for (int k = 0; k < si; ++k) mine &= mine - 1;
+    return __ffs(mine) - 1;
+}
+
+// Warp 0: the bulk copies of rows [r0, r1) of a merge (row c < NC: near
+// slice c's value sums; row NC + r: far record r's numerator) for every head
+// of `mine`, to buf[(c - r0) nS + si][dv]. When every head of the group
+// merges, the near rows are one contiguous copy.
+__device__ void tok_merge_issue(const O1Args &a, int g, unsigned mine, int nS, int r0, int r1, float *buf,
+                                uint64_t *bar) {
+    const int lane = threadIdx.x & 31, hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv;
+    // the rows were written by generic stores (other CTAs', ordered before
+    // the arrival's acquire) and the buffer last held this CTA's own generic
+    // accesses: order both before the async proxy's copies
+    asm volatile("fence.proxy.async;" ::: "memory");
+    if (lane == 0) {
+        const uint32_t bytes = (uint32_t)(r1 - r0) * nS * dv * 4;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tok_su32(bar)), "r"(bytes)
+                     : "memory");
+    }
+    __syncwarp();
+    const int nn = max(0, min(r1, NC) - r0);
+    if (nS == hpg) {
+        if (nn > 0 && lane == 0)
+            tok_bulk_nx(buf, a.part + (size_t)(g * NC + r0) * hpg * dv, (uint32_t)nn * hpg * dv * 4, bar);
+    } else {
+        for (int j = lane; j < nn * nS; j += 32) {
+            const int c = r0 + j / nS, si = j % nS;
+            tok_bulk_nx(buf + (size_t)j * dv, a.part + ((size_t)(g * NC + c) * hpg + tok_nth_head(mine, si)) * dv,
+                        (uint32_t)dv * 4, bar);
+        }
+    }
+    const int f0 = max(r0, NC), nfr = max(0, r1 - f0);
+    for (int j = lane; j < nfr * nS; j += 32) {
+        const int r = f0 - NC + j / nS, si = j % nS;
+        const int h = g * hpg + tok_nth_head(mine, si);
+        tok_bulk_nx(buf + ((size_t)(f0 - r0) * nS + j) * dv, a.farp + ((size_t)h * NF + r) * (4 + dv) + 4,
+                    (uint32_t)dv * 4, bar);
+    }
+}
+
 // The merge of the heads in `mine` (bits hl of group g), by the CTA that
-// arrived last for them: per head, the near slices' (max, sum) -> the window
-// max M_w and mass L; the far records -> c_f and D (float-float, sign decision);
-// then per (head, 4 columns) the slices' value sums (each moved to M_w), the
-// far numerator, one exponent c = max(M_w, c_f) (the far max counts even
-// when the far part is dropped, as the pages' c_all does), the 1e-30 floor
-// and the gate. The value sums are read as float4, a thread's 16 slices in
-// flight at once, the threads split over slice groups when there are more
-// threads than (head, 4 columns); nothing in shared memory grows with the
-// number of slices.
+// arrived last for them, on its first `nthr` threads: per head, the near
+// slices' (max, sum) -> the window max M_w and mass L; the far records ->
+// c_f and D (float-float, sign decision); then per (head, 4 columns) the
+// slices' value sums (each moved to M_w), the far numerator, one exponent
+// c = max(M_w, c_f) (the far max counts even when the far part is dropped,
+// as the pages' c_all does), the 1e-30 floor and the gate.
+// The rows summed (NC near value sums and NF far numerators a head) come
+// into shared memory by bulk copies: all at once when they fit, else in
+// rounds through two buffers; the statistics are formed from global memory
+// while the first copies fly. `stage` is shared memory the CTA's own work is
+// done with (at least o1_tok_stage_min floats), `shd` the merge scratch,
+// `bars` two mbarriers (phases counted in `*phase`, one bit per barrier).
 template <int HPG>
-__device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, const float *sgt, float *smg) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv, dv4 = dv >> 2;
-    int heads[HPG];
-    int nS = 0;
-    for (int hl = 0; hl < hpg; ++hl)
-        if (mine & (1u << hl)) heads[nS++] = hl;
-    float *shd = smg;                       // [nS][8]  M_w, L, c_f, have, D
-    float *sff = shd + 8 * nS;              // [nS][NF] far record factors e^{c_r - c_f}
-    float4 *sacc = (float4 *)(((uintptr_t)(smg + (size_t)hpg * (NF + 8)) + 15) & ~(uintptr_t)15);   // [256]
+__device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, const float *sgt, float *shd,
+                          float *stage, size_t stage_floats, uint64_t *bars, int nthr) {
+    constexpr int MAXP = (HPG * 64 + 223) / 224;   // passes over the (head, 4 columns) items
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv, dv4 = dv >> 2, RT = NC + NF;
+    const int nS = __popc(mine);
+    float *fac = stage;   // [nS][RT] row factors
+    const size_t ffl = ((size_t)nS * RT + 3) / 4 * 4;
+    float *rows = stage + ffl;
+    const size_t row_floats = (size_t)nS * dv, avail = stage_floats - ffl;
+    int nbuf = 1, R = RT;
+    if ((size_t)RT * row_floats > avail) {
+        R = (int)(avail / (2 * row_floats));
+        nbuf = 2;
+        if (R < 1) {
+            R = (int)(avail / row_floats);
+            nbuf = 1;
+        }
+    }
+    const int nr = (RT + R - 1) / R;
+    if (warp == 0)
+        for (int k = 0; k < nbuf && k < nr; ++k)
+            tok_merge_issue(a, g, mine, nS, k * R, min(RT, (k + 1) * R), rows + (size_t)k * R * row_floats,
+                            bars + k);
+
+    // statistics, a warp per head, from global memory
     const float *pml = a.pml + (size_t)g * NC * hpg * 2;   // slice c, head hl: pml[(c hpg + hl) 2]
-    for (int si = warp; si < nS; si += blockDim.x >> 5) {
-        const int hl = heads[si];
+    for (int si = warp; si < nS; si += nwarps) {
+        const int hl = tok_nth_head(mine, si);
         const int h = g * hpg + hl;
-        // the far records (c_r, -, D high, D low) and the slices' (max, sum),
-        // every load of the lane issued before any is used: NF <= 64, and a
-        // lane takes the slices lane, lane + 32, ... with an online max
+        float *fs = fac + (size_t)si * RT;
+        // far record headers (c_r, -, D high, D low): NF <= 64
         float4 fr4[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -599,6 +677,7 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
         float mx = -INFINITY, L = 0.f;
         for (int c = lane; c < NC; c += 32) {
             const float2 v = __ldcg((const float2 *)(pml + ((size_t)c * hpg + hl) * 2));
+            fs[c] = v.x;
             if (v.x == -INFINITY) continue;
             const float mn = fmaxf(mx, v.x);
             L = L * expf(mx - mn) + v.y * expf(v.x - mn);
@@ -606,132 +685,162 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
         }
         const float Mw = warp_max(mx);
         L = warp_sum(mx == -INFINITY ? 0.f : L * expf(mx - Mw));
+        for (int c = lane; c < NC; c += 32) {   // the lane's own entries: no sync needed
+            const float mc = fs[c];
+            fs[c] = mc == -INFINITY ? 0.f : expf(mc - Mw);
+        }
         const float cf = warp_max(fmaxf(fr4[0].x, fr4[1].x));
         o1_ff D = ff_make(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int r = lane + 32 * k;
             const float fr = (fr4[k].x == -INFINITY) ? 0.f : expf(fr4[k].x - cf);
-            if (r < NF) sff[si * NF + r] = fr;
+            if (r < NF) fs[NC + r] = fr;
             D = ff_add(D, ff_mul_f(ff_make(fr4[k].z, fr4[k].w), fr));
         }
         D = warp_sum(D);
-        const float mx_ = Mw;
         if (lane == 0) {
             const bool have = farl1 > 0 && ff_nonneg(D);
-            shd[si * 8 + 0] = mx_;
+            shd[si * 8 + 0] = Mw;
             shd[si * 8 + 1] = L;
             shd[si * 8 + 2] = farl1 > 0 ? cf : -INFINITY;
             shd[si * 8 + 3] = have ? 1.f : 0.f;
             shd[si * 8 + 4] = have ? D.hi + D.lo : 0.f;
         }
     }
-    __syncthreads();
+    tok_bar_merge(nthr);
+
+    // rows: a thread per (head, 4 columns) item and slice group sg (lanes
+    // that differ in their high bits), summed over the rows of its group
     const int items = nS * dv4;
-    int nsg = items >= (int)blockDim.x ? 1 : (int)blockDim.x / items;
-    if (nsg > 8) nsg = 8;
-    for (int it0 = 0; it0 < items; it0 += blockDim.x / nsg) {
-        const int it = it0 + tid % (blockDim.x / nsg), sg = tid / (blockDim.x / nsg);
-        const bool act = it < items && sg < nsg;
-        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        int si = 0, c4 = 0;
-        if (act) {
-            si = it / dv4;
-            c4 = it - si * dv4;
-            const int hl = heads[si];
-            const float Mw = shd[si * 8 + 0];
-            const float4 *pv = (const float4 *)(a.part + ((size_t)g * NC * hpg + hl) * dv) + c4;   // slice c: + c hpg dv4
-            for (int c0 = sg; c0 < NC; c0 += 16 * nsg) {
-                float4 v[16];
-                float mc[16];
+    int nsg = 1;
+    while (nsg < 8 && items * nsg * 2 <= nthr) nsg *= 2;
+    const int lpi = 32 / nsg, sg = lane / lpi, ipp = nthr / nsg;
+    const int P = (items + ipp - 1) / ipp;
+    float4 A[MAXP], FN[MAXP];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int c = c0 + u * nsg;
-                    const bool in = c < NC;
-                    mc[u] = in ? __ldcg(pml + ((size_t)c * hpg + hl) * 2) : -INFINITY;
-                    v[u] = in ? __ldcg(pv + (size_t)c * hpg * dv4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+    for (int q = 0; q < MAXP; ++q) A[q] = FN[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nr; ++k) {
+        const int r0 = k * R, r1 = min(RT, r0 + R), b = k % nbuf;
+        tok_wait_copies(a, bars + b, (uint32_t)((k / nbuf) & 1));
+        const float4 *buf = (const float4 *)(rows + (size_t)b * R * row_floats);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (mc[u] == -INFINITY) continue;
-                    const float f = expf(mc[u] - Mw);
-                    A.x = fmaf(f, v[u].x, A.x);
-                    A.y = fmaf(f, v[u].y, A.y);
-                    A.z = fmaf(f, v[u].z, A.z);
-                    A.w = fmaf(f, v[u].w, A.w);
-                }
+        for (int q = 0; q < MAXP; ++q) {
+            if (q >= P) break;
+            const int it = q * ipp + warp * lpi + (lane % lpi);
+            if (it >= items) continue;
+            const int si = it / dv4, c4 = it - si * dv4;
+            const float *fs = fac + (size_t)si * RT;
+            float4 acc = A[q];
+            int j = r0 + sg;
+            for (; j < min(r1, NC); j += nsg) {
+                const float f = fs[j];
+                const float4 v = buf[((size_t)(j - r0) * nS + si) * dv4 + c4];
+                acc.x = fmaf(f, v.x, acc.x);
+                acc.y = fmaf(f, v.y, acc.y);
+                acc.z = fmaf(f, v.z, acc.z);
+                acc.w = fmaf(f, v.w, acc.w);
             }
-        }
-        if (nsg > 1) {
-            sacc[tid] = A;
-            __syncthreads();
-            if (act && sg == 0)
-                for (int q = 1; q < nsg; ++q) {
-                    const float4 o = sacc[q * (blockDim.x / nsg) + tid];
-                    A.x += o.x;
-                    A.y += o.y;
-                    A.z += o.z;
-                    A.w += o.w;
-                }
-            __syncthreads();
-        }
-        if (act && sg == 0) {
-            const int hl = heads[si], h = g * hpg + hl;
-            float4 FN = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r = 0; r < NF; ++r) {
-                const float fr = sff[si * NF + r];
-                const float4 n = __ldcg((const float4 *)(a.farp + ((size_t)h * NF + r) * (4 + dv) + 4) + c4);
-                FN.x = fmaf(fr, n.x, FN.x);
-                FN.y = fmaf(fr, n.y, FN.y);
-                FN.z = fmaf(fr, n.z, FN.z);
-                FN.w = fmaf(fr, n.w, FN.w);
+            A[q] = acc;
+            acc = FN[q];
+            for (; j < r1; j += nsg) {
+                const float f = fs[j];
+                const float4 v = buf[((size_t)(j - r0) * nS + si) * dv4 + c4];
+                acc.x = fmaf(f, v.x, acc.x);
+                acc.y = fmaf(f, v.y, acc.y);
+                acc.z = fmaf(f, v.z, acc.z);
+                acc.w = fmaf(f, v.w, acc.w);
             }
-            const float Mw = shd[si * 8 + 0], L = shd[si * 8 + 1], cf = shd[si * 8 + 2];
-            const bool have = shd[si * 8 + 3] > 0.5f;
-            const float c = cf > -INFINITY ? fmaxf(Mw, cf) : Mw;
-            const float al = expf(Mw - c);
-            const float be = have ? expf(cf - c) : 0.f;
-            const float rden = 1.f / fmaxf(be * shd[si * 8 + 4] + al * L, 1e-30f);
-            float y[4] = {(be * FN.x + al * A.x) * rden, (be * FN.y + al * A.y) * rden, (be * FN.z + al * A.z) * rden,
-                          (be * FN.w + al * A.w) * rden};
-            if (a.gate)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) y[j] = y[j] / (1.f + expf(-sgt[hl * dv + 4 * c4 + j]));
-            *((float4 *)(a.out + (size_t)h * dv) + c4) = make_float4(y[0], y[1], y[2], y[3]);
+            FN[q] = acc;
         }
+        if (k + nbuf < nr) {   // every thread is done with buffer b: refill it
+            tok_bar_merge(nthr);
+            if (warp == 0)
+                tok_merge_issue(a, g, mine, nS, (k + nbuf) * R, min(RT, (k + nbuf + 1) * R),
+                                rows + (size_t)b * R * row_floats, bars + b);
+        }
+    }
+    // slice groups -> lane sg = 0, then the output
+#pragma unroll
+    for (int q = 0; q < MAXP; ++q) {
+        if (q >= P) break;
+        for (int off = 16; off >= lpi; off >>= 1) {
+            A[q].x += __shfl_xor_sync(0xffffffffu, A[q].x, off);
+            A[q].y += __shfl_xor_sync(0xffffffffu, A[q].y, off);
+            A[q].z += __shfl_xor_sync(0xffffffffu, A[q].z, off);
+            A[q].w += __shfl_xor_sync(0xffffffffu, A[q].w, off);
+            FN[q].x += __shfl_xor_sync(0xffffffffu, FN[q].x, off);
+            FN[q].y += __shfl_xor_sync(0xffffffffu, FN[q].y, off);
+            FN[q].z += __shfl_xor_sync(0xffffffffu, FN[q].z, off);
+            FN[q].w += __shfl_xor_sync(0xffffffffu, FN[q].w, off);
+        }
+        const int it = q * ipp + warp * lpi + (lane % lpi);
+        if (sg != 0 || it >= items) continue;
+        const int si = it / dv4, c4 = it - si * dv4;
+        const int hl = tok_nth_head(mine, si), h = g * hpg + hl;
+        const float Mw = shd[si * 8 + 0], L = shd[si * 8 + 1], cf = shd[si * 8 + 2];
+        const bool have = shd[si * 8 + 3] > 0.5f;
+        const float c = cf > -INFINITY ? fmaxf(Mw, cf) : Mw;
+        const float al = expf(Mw - c);
+        const float be = have ? expf(cf - c) : 0.f;
+        const float rden = 1.f / fmaxf(be * shd[si * 8 + 4] + al * L, 1e-30f);
+        float y[4] = {(be * FN[q].x + al * A[q].x) * rden, (be * FN[q].y + al * A[q].y) * rden,
+                      (be * FN[q].z + al * A[q].z) * rden, (be * FN[q].w + al * A[q].w) * rden};
+        if (a.gate)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) y[jj] = y[jj] / (1.f + expf(-sgt[hl * dv + 4 * c4 + jj]));
+        *((float4 *)(a.out + (size_t)h * dv) + c4) = make_float4(y[0], y[1], y[2], y[3]);
     }
 }
 
-// The commit of the step, by the CTA that arrived last of all (every CTA has
-// read the ring, meta and far state by then): each group's ring slot gets
-// the row's rotated key and value and its meta moves (o1b_ring_commit /
-// o1b_meta for one row); then the position, the step's last write, released
-// after every state write of the step.
-__device__ void tok_commit(const O1Args &a, long long p, float *smg) {
-    const int tid = threadIdx.x;
-    int *sslot = (int *)smg;   // [G] the slot each group pushes to
-    for (int g = tid; g < a.G; g += blockDim.x) {
-        const int len0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 0), head0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 1);
-        const int farl0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 2), wg = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 3);
-        sslot[g] = (head0 + len0) % wg;
-        if (len0 == wg) {
-            a.meta[g * 4 + 1] = (uint32_t)((head0 + 1) % wg);
-            a.meta[g * 4 + 2] = (uint32_t)(farl0 + 1);
-        } else {
-            a.meta[g * 4 + 0] = (uint32_t)(len0 + 1);
+// The commit of the step, by one warp of the CTA that arrived last of all
+// (every CTA has read the ring, meta and far state by then): each group's
+// ring slot gets the row's rotated key and value and its meta moves
+// (o1b_ring_commit / o1b_meta for one row); then the position, the step's
+// last write, released after every state write of the step. The values and
+// the metas are read in one round; `sslot` holds a slot index per group.
+__device__ void tok_commit_warp(const O1Args &a, long long p, int *sslot) {
+    const int lane = threadIdx.x & 31, G = a.G, d4 = a.d >> 2, dv4 = a.dv >> 2;
+    const int nk = G * d4, nt = nk + G * dv4;
+    const float4 *kc4 = (const float4 *)a.kcur, *v4 = (const float4 *)a.v;
+    float4 *rk4 = (float4 *)a.ring_k, *rv4 = (float4 *)a.ring_v;
+    for (int base = 0; base < nt; base += 32 * 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + 32 * u + lane;
+            x[u] = i < nk ? __ldcg(kc4 + i) : (i < nt ? __ldcg(v4 + (i - nk)) : make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+        if (base == 0) {
+            for (int g = lane; g < G; g += 32) {
+                const int len0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 0);
+                const int head0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 1);
+                const int farl0 = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 2);
+                const int wg = (int)tok_ld_relaxed_u32(a.meta + g * 4 + 3);
+                sslot[g] = (head0 + len0) % wg;
+                if (len0 == wg) {
+                    a.meta[g * 4 + 1] = (uint32_t)((head0 + 1) % wg);
+                    a.meta[g * 4 + 2] = (uint32_t)(farl0 + 1);
+                } else {
+                    a.meta[g * 4 + 0] = (uint32_t)(len0 + 1);
+                }
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + 32 * u + lane;
+            if (i < nk) {
+                const int g = i / d4, j = i - g * d4;
+                rk4[((size_t)g * a.w + sslot[g]) * d4 + j] = x[u];
+            } else if (i < nt) {
+                const int i2 = i - nk, g = i2 / dv4, j = i2 - g * dv4;
+                rv4[((size_t)g * a.w + sslot[g]) * dv4 + j] = x[u];
+            }
         }
     }
-    __syncthreads();
-    for (size_t i = tid; i < (size_t)a.G * a.d; i += blockDim.x) {
-        const int g = (int)(i / a.d), j = (int)(i - (size_t)g * a.d);
-        a.ring_k[((size_t)g * a.w + sslot[g]) * a.d + j] = __ldcg(a.kcur + i);
-    }
-    for (size_t i = tid; i < (size_t)a.G * a.dv; i += blockDim.x) {
-        const int g = (int)(i / a.dv), j = (int)(i - (size_t)g * a.dv);
-        a.ring_v[((size_t)g * a.w + sslot[g]) * a.dv + j] = a.v[i];
-    }
-    __syncthreads();
-    if (tid == 0) {
+    __syncwarp();
+    if (lane == 0) {
         a.tick[a.nh + a.G] = 0u;
         __threadfence();
         tok_st_release((long long *)&a.hdr->pos, p + 1);
@@ -741,13 +850,14 @@ __device__ void tok_commit(const O1Args &a, long long p, float *smg) {
 }  // namespace
 
 template <int HPG>
-__global__ __launch_bounds__(256) void k_tok(O1Args a) {
+__global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     __shared__ long long s_pos;
     __shared__ int s_meta[4];
     __shared__ int s_parity;
     __shared__ unsigned s_mine;
     __shared__ int s_last;
+    __shared__ uint64_t s_mbar[2];   // the merge's copies
     const TokRole ro = tok_role(a);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint64_t *bar = (uint64_t *)sm;
@@ -766,6 +876,8 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
         for (int i = 0; i < 4; ++i) s_meta[i] = (int)tok_ld_relaxed_u32(a.meta + ro.g * 4 + i);
         s_pos = p0;
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tok_su32(bar)) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tok_su32(&s_mbar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tok_su32(&s_mbar[1])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (a.tok_prefetch) {
             // the copies read global memory through the async proxy: order
@@ -882,10 +994,15 @@ __global__ __launch_bounds__(256) void k_tok(O1Args a) {
         s_last = last;
     }
     __syncthreads();
-    if (s_mine) tok_merge<HPG>(a, ro.g, s_mine, farl1, sgt, smg);
-    if (s_last) {
-        __syncthreads();
-        tok_commit(a, p, smg);
+    // the commit (last of all) on warp 7, beside the merge on the other
+    // warps; the merge reuses the shared memory the CTA's work is done with
+    const unsigned mine = s_mine;
+    const bool last = s_last;
+    if (last && warp == 7) {
+        tok_commit_warp(a, p, (int *)(smg + 8 * a.hpg));
+    } else if (mine) {
+        float *stage = ro.far ? fs.sqt : ns.sK;
+        tok_merge<HPG>(a, ro.g, mine, farl1, sgt, smg, stage, (size_t)(smg - stage), s_mbar, last ? 224 : 256);
     }
 }
 

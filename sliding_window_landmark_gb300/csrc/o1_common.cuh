@@ -170,15 +170,16 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
 // Shared memory (floats) of a near slice and of a far chunk, and of the
 // merge scratch that follows either; the kernel carves the same offsets.
 // After its own work a CTA may merge heads and commit the step: the merge
-// stages the rows it reads (the near partials and far numerators, NC + NF
-// rows of dv floats per head) in the part of shared memory the work used
+// stages what it reads (per head, the NC near value sums of dv floats and
+// the NF far records of 4 + dv) in the part of shared memory the work used
 // (from the near slice's keys, or the far chunk's landmark queries, up to
-// the merge scratch), after their factors [heads][NC + NF]. That part is
-// made at least one row per head plus the factors (o1_tok_stage_min). The
-// merge scratch holds 8 scalars per head and one slot index per group.
+// the merge scratch), after the rows' factors [heads][NC + NF]. That part is
+// made to hold at least the factors, the far records and one near row per
+// head (o1_tok_stage_min). The merge scratch holds 8 scalars per head and
+// one slot index per group.
 __host__ __device__ inline size_t o1_tok_merge_floats(int hpg, int G) { return (size_t)8 * hpg + G + 4; }
 __host__ __device__ inline size_t o1_tok_stage_min(int hpg, int NC, int NF, int dv) {
-    return ((size_t)hpg * (NC + NF) + 3) / 4 * 4 + (size_t)hpg * dv;
+    return ((size_t)hpg * (NC + NF) + 3) / 4 * 4 + (size_t)hpg * NF * (4 + dv) + (size_t)hpg * dv;
 }
 __host__ __device__ inline size_t o1_tok_near_region(int d, int dv, int hpg, int KC) {
     return (size_t)KC * (d + dv) + (size_t)KC * hpg + (size_t)8 * KC * hpg;
@@ -199,8 +200,9 @@ __host__ __device__ inline size_t o1_tok_far_floats(int d, int dv, int hpg, int 
            o1_tok_merge_floats(hpg, G);
 }
 
-// Scratch of the one-row path: near partials per (group, slice, head), the
-// value sums [dv] in `part` and (max, sum) in `pml`; far records per (head,
+// Scratch of the one-row path: near partials per (group, head, slice), the
+// value sums [dv] in `part` and (max, sum) in `pml` (a head's slices are
+// contiguous, for the merge's copies); far records per (head,
 // chunk): (c_f of the chunk, -, D high, D low, numerator [dv]); the row's
 // rotated key per group, for the commit.
 struct O1TokScratch {

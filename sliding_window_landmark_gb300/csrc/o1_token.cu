@@ -362,18 +362,22 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
     const int d = a.d, dv = a.dv, hpg = a.hpg, KC = a.KC;
     const TokNear p = tok_near_plan(a, mt, ro.c);
     const int cnt = p.cnt;
-    const size_t slot = (size_t)(ro.g * a.NC + ro.c) * hpg;
-    float *pv = a.part + slot * dv;   // [hpg][dv]
-    float *pml = a.pml + slot * 2;    // [hpg][2]
+    // head h's partial: pv + h NC dv (value sums), pml + h NC 2 (max, sum)
+    const size_t slot = (size_t)ro.g * hpg * a.NC + ro.c, hs = (size_t)a.NC;
+    float *pv = a.part + slot * dv;
+    float *pml = a.pml + slot * 2;
     if (ro.c == 0)   // the group's rotated key, for the commit
         for (int j = tid; j < d; j += blockDim.x) a.kcur[(size_t)ro.g * d + j] = s.sk[j];
     if (cnt == 0) {   // an empty slice: zero weight, and zero sums (the merge reads every row)
         for (int h = tid; h < hpg; h += blockDim.x) {
-            pml[2 * h] = -INFINITY;
-            pml[2 * h + 1] = 0.f;
+            pml[h * hs * 2] = -INFINITY;
+            pml[h * hs * 2 + 1] = 0.f;
         }
-        for (int i = tid; i < ((hpg * dv) >> 2); i += blockDim.x)
-            ((float4 *)pv)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int dv4 = dv >> 2;
+        for (int i = tid; i < hpg * dv4; i += blockDim.x) {
+            const int h = i / dv4;
+            ((float4 *)(pv + h * hs * dv))[i - h * dv4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         return;
     }
     // (the pushed key's row holds the row's own rotated key and value)
@@ -411,8 +415,8 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
         }
         l = warp_sum(l);
         if (lane == 0) {
-            pml[2 * h] = mx;
-            pml[2 * h + 1] = l;
+            pml[h * hs * 2] = mx;
+            pml[h * hs * 2 + 1] = l;
         }
     }
     __syncthreads();
@@ -430,7 +434,7 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
             acc.z = fmaf(w, v.z, acc.z);
             acc.w = fmaf(w, v.w, acc.w);
         }
-        ((float4 *)(pv + (size_t)h * dv))[c4] = acc;
+        ((float4 *)(pv + h * hs * dv))[c4] = acc;
     }
 }
 
@@ -584,40 +588,28 @@ __device__ __forceinline__ int tok_nth_head(unsigned mine, int si) {
     return __ffs(mine) - 1;
 }
 
-// Warp 0: the bulk copies of rows [r0, r1) of a merge (row c < NC: near
-// slice c's value sums; row NC + r: far record r's numerator) for every head
-// of `mine`, to buf[(c - r0) nS + si][dv]. When every head of the group
-// merges, the near rows are one contiguous copy.
-__device__ void tok_merge_issue(const O1Args &a, int g, unsigned mine, int nS, int r0, int r1, float *buf,
-                                uint64_t *bar) {
-    const int lane = threadIdx.x & 31, hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv;
-    // the rows were written by generic stores (other CTAs', ordered before
-    // the arrival's acquire) and the buffer last held this CTA's own generic
-    // accesses: order both before the async proxy's copies
-    asm volatile("fence.proxy.async;" ::: "memory");
-    if (lane == 0) {
-        const uint32_t bytes = (uint32_t)(r1 - r0) * nS * dv * 4;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tok_su32(bar)), "r"(bytes)
-                     : "memory");
-    }
-    __syncwarp();
-    const int nn = max(0, min(r1, NC) - r0);
-    if (nS == hpg) {
-        if (nn > 0 && lane == 0)
-            tok_bulk_nx(buf, a.part + (size_t)(g * NC + r0) * hpg * dv, (uint32_t)nn * hpg * dv * 4, bar);
-    } else {
-        for (int j = lane; j < nn * nS; j += 32) {
-            const int c = r0 + j / nS, si = j % nS;
-            tok_bulk_nx(buf + (size_t)j * dv, a.part + ((size_t)(g * NC + c) * hpg + tok_nth_head(mine, si)) * dv,
-                        (uint32_t)dv * 4, bar);
-        }
-    }
-    const int f0 = max(r0, NC), nfr = max(0, r1 - f0);
-    for (int j = lane; j < nfr * nS; j += 32) {
-        const int r = f0 - NC + j / nS, si = j % nS;
-        const int h = g * hpg + tok_nth_head(mine, si);
-        tok_bulk_nx(buf + ((size_t)(f0 - r0) * nS + j) * dv, a.farp + ((size_t)h * NF + r) * (4 + dv) + 4,
-                    (uint32_t)dv * 4, bar);
+// One thread: the bulk copies of a merge's round, for every head si of
+// `mine`: near rows [r0, r1) of its slices (contiguous in `part`) to
+// buf[si][R][dv], and in the first round its NF far records (contiguous in
+// `farp`, 4 + dv floats each) to far[si][NF][4 + dv].
+__device__ void tok_merge_issue(const O1Args &a, int g, unsigned mine, int nS, int r0, int r1, int R, float *buf,
+                                float *far, uint64_t *bar) {
+    const int hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv;
+    // the data were written by generic stores (other CTAs', ordered before
+    // the arrival's acquire) and the buffers last held this CTA's own
+    // generic accesses: order both before the async proxy's copies
+    asm volatile("fence.proxy.async.global;\nfence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t near_b = (uint32_t)(r1 - r0) * dv * 4, far_b = far ? (uint32_t)NF * (4 + dv) * 4 : 0u;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tok_su32(bar)),
+                 "r"((uint32_t)nS * (near_b + far_b))
+                 : "memory");
+    unsigned left = mine;
+    for (int si = 0; si < nS; ++si) {
+        const int hl = __ffs(left) - 1;
+        left &= left - 1;
+        tok_bulk_nx(buf + (size_t)si * R * dv, a.part + ((size_t)(g * hpg + hl) * NC + r0) * dv, near_b, bar);
+        if (far)
+            tok_bulk_nx(far + (size_t)si * NF * (4 + dv), a.farp + (size_t)(g * hpg + hl) * NF * (4 + dv), far_b, bar);
     }
 }
 
@@ -628,12 +620,12 @@ __device__ void tok_merge_issue(const O1Args &a, int g, unsigned mine, int nS, i
 // slices' value sums (each moved to M_w), the far numerator, one exponent
 // c = max(M_w, c_f) (the far max counts even when the far part is dropped,
 // as the pages' c_all does), the 1e-30 floor and the gate.
-// The rows summed (NC near value sums and NF far numerators a head) come
-// into shared memory by bulk copies: all at once when they fit, else in
+// The rows summed come into shared memory by bulk copies (two a head, issued
+// by the last warp's first thread): all at once when they fit, else in
 // rounds through two buffers; the statistics are formed from global memory
 // while the first copies fly. `stage` is shared memory the CTA's own work is
 // done with (at least o1_tok_stage_min floats), `shd` the merge scratch,
-// `bars` two mbarriers (phases counted in `*phase`, one bit per barrier).
+// `bars` two mbarriers.
 template <int HPG>
 __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, const float *sgt, float *shd,
                           float *stage, size_t stage_floats, uint64_t *bars, int nthr) {
@@ -641,12 +633,14 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int hpg = a.hpg, NC = a.NC, NF = a.NF, dv = a.dv, dv4 = dv >> 2, RT = NC + NF;
     const int nS = __popc(mine);
+    const bool issuer = tid == nthr - 32;
     float *fac = stage;   // [nS][RT] row factors
     const size_t ffl = ((size_t)nS * RT + 3) / 4 * 4;
-    float *rows = stage + ffl;
-    const size_t row_floats = (size_t)nS * dv, avail = stage_floats - ffl;
-    int nbuf = 1, R = RT;
-    if ((size_t)RT * row_floats > avail) {
+    float *far = stage + ffl;   // [nS][NF][4 + dv]
+    float *rows = far + (size_t)nS * NF * (4 + dv);
+    const size_t row_floats = (size_t)nS * dv, avail = stage_floats - ffl - (size_t)nS * NF * (4 + dv);
+    int nbuf = 1, R = NC;
+    if ((size_t)NC * row_floats > avail) {
         R = (int)(avail / (2 * row_floats));
         nbuf = 2;
         if (R < 1) {
@@ -654,17 +648,17 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
             nbuf = 1;
         }
     }
-    const int nr = (RT + R - 1) / R;
-    if (warp == 0)
+    const int nr = (NC + R - 1) / R;
+    if (issuer)
         for (int k = 0; k < nbuf && k < nr; ++k)
-            tok_merge_issue(a, g, mine, nS, k * R, min(RT, (k + 1) * R), rows + (size_t)k * R * row_floats,
-                            bars + k);
+            tok_merge_issue(a, g, mine, nS, k * R, min(NC, (k + 1) * R), R, rows + (size_t)k * R * row_floats,
+                            k == 0 ? far : nullptr, bars + k);
 
     // statistics, a warp per head, from global memory
-    const float *pml = a.pml + (size_t)g * NC * hpg * 2;   // slice c, head hl: pml[(c hpg + hl) 2]
     for (int si = warp; si < nS; si += nwarps) {
         const int hl = tok_nth_head(mine, si);
         const int h = g * hpg + hl;
+        const float *pml = a.pml + (size_t)h * NC * 2;   // slice c: pml[2 c]
         float *fs = fac + (size_t)si * RT;
         // far record headers (c_r, -, D high, D low): NF <= 64
         float4 fr4[2];
@@ -676,7 +670,7 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
         }
         float mx = -INFINITY, L = 0.f;
         for (int c = lane; c < NC; c += 32) {
-            const float2 v = __ldcg((const float2 *)(pml + ((size_t)c * hpg + hl) * 2));
+            const float2 v = __ldcg((const float2 *)(pml + 2 * c));
             fs[c] = v.x;
             if (v.x == -INFINITY) continue;
             const float mn = fmaxf(mx, v.x);
@@ -684,12 +678,12 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
             mx = mn;
         }
         const float Mw = warp_max(mx);
+        const float cf = warp_max(fmaxf(fr4[0].x, fr4[1].x));
         L = warp_sum(mx == -INFINITY ? 0.f : L * expf(mx - Mw));
         for (int c = lane; c < NC; c += 32) {   // the lane's own entries: no sync needed
             const float mc = fs[c];
             fs[c] = mc == -INFINITY ? 0.f : expf(mc - Mw);
         }
-        const float cf = warp_max(fmaxf(fr4[0].x, fr4[1].x));
         o1_ff D = ff_make(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -717,11 +711,11 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
     while (nsg < 8 && items * nsg * 2 <= nthr) nsg *= 2;
     const int lpi = 32 / nsg, sg = lane / lpi, ipp = nthr / nsg;
     const int P = (items + ipp - 1) / ipp;
-    float4 A[MAXP], FN[MAXP];
+    float4 A[MAXP];
 #pragma unroll
-    for (int q = 0; q < MAXP; ++q) A[q] = FN[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < MAXP; ++q) A[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < nr; ++k) {
-        const int r0 = k * R, r1 = min(RT, r0 + R), b = k % nbuf;
+        const int r0 = k * R, r1 = min(NC, r0 + R), b = k % nbuf;
         tok_wait_copies(a, bars + b, (uint32_t)((k / nbuf) & 1));
         const float4 *buf = (const float4 *)(rows + (size_t)b * R * row_floats);
 #pragma unroll
@@ -731,50 +725,56 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
             if (it >= items) continue;
             const int si = it / dv4, c4 = it - si * dv4;
             const float *fs = fac + (size_t)si * RT;
+            const float4 *src = buf + (size_t)si * R * dv4 + c4;
             float4 acc = A[q];
-            int j = r0 + sg;
-            for (; j < min(r1, NC); j += nsg) {
+            for (int j = r0 + sg; j < r1; j += nsg) {
                 const float f = fs[j];
-                const float4 v = buf[((size_t)(j - r0) * nS + si) * dv4 + c4];
+                const float4 v = src[(size_t)(j - r0) * dv4];
                 acc.x = fmaf(f, v.x, acc.x);
                 acc.y = fmaf(f, v.y, acc.y);
                 acc.z = fmaf(f, v.z, acc.z);
                 acc.w = fmaf(f, v.w, acc.w);
             }
             A[q] = acc;
-            acc = FN[q];
-            for (; j < r1; j += nsg) {
-                const float f = fs[j];
-                const float4 v = buf[((size_t)(j - r0) * nS + si) * dv4 + c4];
-                acc.x = fmaf(f, v.x, acc.x);
-                acc.y = fmaf(f, v.y, acc.y);
-                acc.z = fmaf(f, v.z, acc.z);
-                acc.w = fmaf(f, v.w, acc.w);
-            }
-            FN[q] = acc;
         }
         if (k + nbuf < nr) {   // every thread is done with buffer b: refill it
             tok_bar_merge(nthr);
-            if (warp == 0)
-                tok_merge_issue(a, g, mine, nS, (k + nbuf) * R, min(RT, (k + nbuf + 1) * R),
-                                rows + (size_t)b * R * row_floats, bars + b);
+            if (issuer)
+                tok_merge_issue(a, g, mine, nS, (k + nbuf) * R, min(NC, (k + nbuf + 1) * R), R,
+                                rows + (size_t)b * R * row_floats, nullptr, bars + b);
         }
     }
-    // slice groups -> lane sg = 0, then the output
+    // the far numerators (staged with the first round), the slice groups ->
+    // lane sg = 0, then the output
+    const int rs4 = (4 + dv) >> 2;
 #pragma unroll
     for (int q = 0; q < MAXP; ++q) {
         if (q >= P) break;
+        const int it = q * ipp + warp * lpi + (lane % lpi);
+        float4 FN = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (it < items) {
+            const int si = it / dv4, c4 = it - si * dv4;
+            const float *fs = fac + (size_t)si * RT + NC;
+            const float4 *src = (const float4 *)far + (size_t)si * NF * rs4 + 1 + c4;
+            for (int r = sg; r < NF; r += nsg) {
+                const float f = fs[r];
+                const float4 v = src[(size_t)r * rs4];
+                FN.x = fmaf(f, v.x, FN.x);
+                FN.y = fmaf(f, v.y, FN.y);
+                FN.z = fmaf(f, v.z, FN.z);
+                FN.w = fmaf(f, v.w, FN.w);
+            }
+        }
         for (int off = 16; off >= lpi; off >>= 1) {
             A[q].x += __shfl_xor_sync(0xffffffffu, A[q].x, off);
             A[q].y += __shfl_xor_sync(0xffffffffu, A[q].y, off);
             A[q].z += __shfl_xor_sync(0xffffffffu, A[q].z, off);
             A[q].w += __shfl_xor_sync(0xffffffffu, A[q].w, off);
-            FN[q].x += __shfl_xor_sync(0xffffffffu, FN[q].x, off);
-            FN[q].y += __shfl_xor_sync(0xffffffffu, FN[q].y, off);
-            FN[q].z += __shfl_xor_sync(0xffffffffu, FN[q].z, off);
-            FN[q].w += __shfl_xor_sync(0xffffffffu, FN[q].w, off);
+            FN.x += __shfl_xor_sync(0xffffffffu, FN.x, off);
+            FN.y += __shfl_xor_sync(0xffffffffu, FN.y, off);
+            FN.z += __shfl_xor_sync(0xffffffffu, FN.z, off);
+            FN.w += __shfl_xor_sync(0xffffffffu, FN.w, off);
         }
-        const int it = q * ipp + warp * lpi + (lane % lpi);
         if (sg != 0 || it >= items) continue;
         const int si = it / dv4, c4 = it - si * dv4;
         const int hl = tok_nth_head(mine, si), h = g * hpg + hl;
@@ -784,8 +784,8 @@ __device__ void tok_merge(const O1Args &a, int g, unsigned mine, int farl1, cons
         const float al = expf(Mw - c);
         const float be = have ? expf(cf - c) : 0.f;
         const float rden = 1.f / fmaxf(be * shd[si * 8 + 4] + al * L, 1e-30f);
-        float y[4] = {(be * FN[q].x + al * A[q].x) * rden, (be * FN[q].y + al * A[q].y) * rden,
-                      (be * FN[q].z + al * A[q].z) * rden, (be * FN[q].w + al * A[q].w) * rden};
+        float y[4] = {(be * FN.x + al * A[q].x) * rden, (be * FN.y + al * A[q].y) * rden,
+                      (be * FN.z + al * A[q].z) * rden, (be * FN.w + al * A[q].w) * rden};
         if (a.gate)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) y[jj] = y[jj] / (1.f + expf(-sgt[hl * dv + 4 * c4 + jj]));

@@ -181,8 +181,10 @@ __host__ __device__ inline size_t o1_tok_merge_floats(int hpg, int G) { return (
 __host__ __device__ inline size_t o1_tok_stage_min(int hpg, int NC, int NF, int dv) {
     return ((size_t)hpg * (NC + NF) + 3) / 4 * 4 + (size_t)hpg * NF * (4 + dv) + (size_t)hpg * dv;
 }
+// (the key rows onwards also take the 8 warps' value-sum partials, 8 hpg dv)
 __host__ __device__ inline size_t o1_tok_near_region(int d, int dv, int hpg, int KC) {
-    return (size_t)KC * (d + dv) + (size_t)KC * hpg + (size_t)8 * KC * hpg;
+    const size_t r = (size_t)KC * (d + dv) + (size_t)KC * hpg + (size_t)8 * KC * hpg, v = (size_t)8 * hpg * dv;
+    return r > v ? r : v;
 }
 __host__ __device__ inline size_t o1_tok_near_floats(int d, int dv, int hpg, int KC, int NC, int NF, int G) {
     const size_t r = o1_tok_near_region(d, dv, hpg, KC), st = o1_tok_stage_min(hpg, NC, NF, dv);

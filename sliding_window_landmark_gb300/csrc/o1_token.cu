@@ -354,6 +354,136 @@ __device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int g, int nq
         for (int t = tid; t < (a.dv >> 2); t += blockDim.x) tok_cp16(vpush + 4 * t, a.v + (size_t)g * a.dv + 4 * t);
 }
 
+// A near slice for up to 4 heads a group: lanes across the vectors' columns
+// (the queries in registers, each key row read once and without bank
+// conflicts), warps across keys (key = warp + 8 i). A warp's per-lane partial
+// dots leave it through one reduce-scatter butterfly: at the step over lane
+// bit b a lane keeps the half of its values that the bit selects and adds
+// the partner's copy of it, so that after five steps (31 shuffles) lane l
+// holds the sum of value l, value i HPG + h being key i's score for head h.
+// The value sums go the same way round (warps across keys, lanes across
+// columns, every head in registers); the 8 warps' partials meet in the key
+// rows' shared memory, free by then.
+template <int HPG>
+__device__ void tok_near_small(const O1Args &a, const TokNearSm &s, int cnt, float *pv, float *pml, size_t hs) {
+    static_assert(HPG <= 4, "registers hold HPG queries and HPG value sums");
+    constexpr int KPB = 32 / HPG;   // a warp's keys per butterfly
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hpg = a.hpg, nu = a.d >> 2, nv = a.dv >> 2;   // float4 units of a key, of a value (<= 64)
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 *sq4 = (const float4 *)s.sq, *sK4 = (const float4 *)s.sK, *sV4 = (const float4 *)s.sV;
+    float4 qr[HPG][2];
+#pragma unroll
+    for (int h = 0; h < HPG; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int u = lane + 32 * j;
+            qr[h][j] = (h < hpg && u < nu) ? sq4[h * nu + u] : z4;
+        }
+    const int kpw = (cnt + 7) >> 3;   // keys of the busiest warp
+    for (int i0 = 0; i0 < kpw; i0 += KPB) {
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < KPB; ++i) {
+            const int key = warp + 8 * (i0 + i);
+            float4 k0 = z4, k1 = z4;
+            if (key < cnt) {
+                if (lane < nu) k0 = sK4[(size_t)key * nu + lane];
+                if (lane + 32 < nu) k1 = sK4[(size_t)key * nu + lane + 32];
+            }
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) {
+                float acc = qr[h][0].x * k0.x;
+                acc = fmaf(qr[h][0].y, k0.y, acc);
+                acc = fmaf(qr[h][0].z, k0.z, acc);
+                acc = fmaf(qr[h][0].w, k0.w, acc);
+                acc = fmaf(qr[h][1].x, k1.x, acc);
+                acc = fmaf(qr[h][1].y, k1.y, acc);
+                acc = fmaf(qr[h][1].z, k1.z, acc);
+                acc = fmaf(qr[h][1].w, k1.w, acc);
+                x[i * HPG + h] = acc;
+            }
+        }
+#pragma unroll
+        for (int i = KPB * HPG; i < 32; ++i) x[i] = 0.f;
+#pragma unroll
+        for (int b = 16; b >= 1; b >>= 1) {
+            const bool up = lane & b;
+#pragma unroll
+            for (int i = 0; i < b; ++i) {
+                const float send = up ? x[i] : x[i + b];
+                const float keep = up ? x[i + b] : x[i];
+                x[i] = keep + __shfl_xor_sync(0xffffffffu, send, b);
+            }
+        }
+        const int i = lane / HPG, h = lane - i * HPG, key = warp + 8 * (i0 + i);
+        if (i < KPB && h < hpg && key < cnt) s.sS[key * hpg + h] = x[0] * a.scale;
+    }
+    __syncthreads();
+    // per head (a warp each): the slice max, the weights e^{s - max} and their sum
+    for (int h = warp; h < hpg; h += 8) {
+        float mx = -INFINITY;
+        for (int i = lane; i < cnt; i += 32) mx = fmaxf(mx, s.sS[i * hpg + h]);
+        mx = warp_max(mx);
+        float l = 0.f;
+        for (int i = lane; i < cnt; i += 32) {
+            const float e = expf(s.sS[i * hpg + h] - mx);
+            s.sS[i * hpg + h] = e;
+            l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            pml[h * hs * 2] = mx;
+            pml[h * hs * 2 + 1] = l;
+        }
+    }
+    __syncthreads();
+    float4 acc[HPG][2];
+#pragma unroll
+    for (int h = 0; h < HPG; ++h) acc[h][0] = acc[h][1] = z4;
+    for (int key = warp; key < cnt; key += 8) {
+        float w[HPG];
+#pragma unroll
+        for (int h = 0; h < HPG; ++h) w[h] = h < hpg ? s.sS[key * hpg + h] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = lane + 32 * j;
+            if (c >= nv) continue;
+            const float4 v = sV4[(size_t)key * nv + c];
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) {
+                acc[h][j].x = fmaf(w[h], v.x, acc[h][j].x);
+                acc[h][j].y = fmaf(w[h], v.y, acc[h][j].y);
+                acc[h][j].z = fmaf(w[h], v.z, acc[h][j].z);
+                acc[h][j].w = fmaf(w[h], v.w, acc[h][j].w);
+            }
+        }
+    }
+    __syncthreads();   // every warp is done with the key and value rows
+    float4 *red = (float4 *)s.sK;   // [8][hpg][nv]: 8 hpg dv floats fit (o1_tok_near_floats)
+#pragma unroll
+    for (int h = 0; h < HPG; ++h)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = lane + 32 * j;
+            if (h < hpg && c < nv) red[((size_t)warp * hpg + h) * nv + c] = acc[h][j];
+        }
+    __syncthreads();
+    for (int idx = tid; idx < hpg * nv; idx += blockDim.x) {
+        const int h = idx / nv, c = idx - h * nv;
+        float4 t = red[(size_t)h * nv + c];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            const float4 o = red[((size_t)w * hpg + h) * nv + c];
+            t.x += o.x;
+            t.y += o.y;
+            t.z += o.z;
+            t.w += o.w;
+        }
+        ((float4 *)(pv + h * hs * a.dv))[c] = t;
+    }
+}
+
 // A near slice: scores of every head of the group over the slice's keys, a
 // slice-local softmax and the value sums -> partial (max, sum, value sum).
 template <int HPG>
@@ -381,60 +511,64 @@ __device__ void tok_near_compute(const O1Args &a, const TokRole &ro, const O1Met
         return;
     }
     // (the pushed key's row holds the row's own rotated key and value)
-    // scores: partial dots per warp (lane = key) over the warp's share of d
-    for (int k0 = 0; k0 < cnt; k0 += 32) {
-        float acc[HPG];
-        const int key = k0 + lane;
-        tok_dots(s.sK, key, key < cnt, s.sq, d, hpg, d, acc);
-        if (key < cnt)
+    if constexpr (HPG <= 4) {
+        tok_near_small<HPG>(a, s, cnt, pv, pml, hs);
+    } else {
+        // scores: partial dots per warp (lane = key) over the warp's share of d
+        for (int k0 = 0; k0 < cnt; k0 += 32) {
+            float acc[HPG];
+            const int key = k0 + lane;
+            tok_dots(s.sK, key, key < cnt, s.sq, d, hpg, d, acc);
+            if (key < cnt)
 #pragma unroll
-            for (int h = 0; h < HPG; ++h) {
-                if (h >= hpg) break;
-                s.sP[((size_t)warp * KC + key) * hpg + h] = acc[h];
+                for (int h = 0; h < HPG; ++h) {
+                    if (h >= hpg) break;
+                    s.sP[((size_t)warp * KC + key) * hpg + h] = acc[h];
+                }
+        }
+        __syncthreads();
+        // per head (a warp each): the partials' sums and the slice max, then the
+        // weights e^{s - max} and their sum
+        for (int h = warp; h < hpg; h += blockDim.x >> 5) {
+            float mx = -INFINITY;
+            for (int i = lane; i < cnt; i += 32) {
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) acc += s.sP[((size_t)w * KC + i) * hpg + h];
+                acc *= a.scale;
+                s.sS[i * hpg + h] = acc;
+                mx = fmaxf(mx, acc);
             }
-    }
-    __syncthreads();
-    // per head (a warp each): the partials' sums and the slice max, then the
-    // weights e^{s - max} and their sum
-    for (int h = warp; h < hpg; h += blockDim.x >> 5) {
-        float mx = -INFINITY;
-        for (int i = lane; i < cnt; i += 32) {
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) acc += s.sP[((size_t)w * KC + i) * hpg + h];
-            acc *= a.scale;
-            s.sS[i * hpg + h] = acc;
-            mx = fmaxf(mx, acc);
+            mx = warp_max(mx);
+            float l = 0.f;
+            for (int i = lane; i < cnt; i += 32) {
+                const float e = expf(s.sS[i * hpg + h] - mx);
+                s.sS[i * hpg + h] = e;
+                l += e;
+            }
+            l = warp_sum(l);
+            if (lane == 0) {
+                pml[h * hs * 2] = mx;
+                pml[h * hs * 2 + 1] = l;
+            }
         }
-        mx = warp_max(mx);
-        float l = 0.f;
-        for (int i = lane; i < cnt; i += 32) {
-            const float e = expf(s.sS[i * hpg + h] - mx);
-            s.sS[i * hpg + h] = e;
-            l += e;
-        }
-        l = warp_sum(l);
-        if (lane == 0) {
-            pml[h * hs * 2] = mx;
-            pml[h * hs * 2 + 1] = l;
-        }
-    }
-    __syncthreads();
-    // value sums: thread per (head, 4 columns)
-    const int dv4 = dv >> 2;
-    for (int idx = tid; idx < hpg * dv4; idx += blockDim.x) {
-        const int h = idx / dv4, c4 = idx - h * dv4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncthreads();
+        // value sums: thread per (head, 4 columns)
+        const int dv4 = dv >> 2;
+        for (int idx = tid; idx < hpg * dv4; idx += blockDim.x) {
+            const int h = idx / dv4, c4 = idx - h * dv4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int i = 0; i < cnt; ++i) {
-            const float w = s.sS[i * hpg + h];
-            const float4 v = ((const float4 *)(s.sV + (size_t)i * dv))[c4];
-            acc.x = fmaf(w, v.x, acc.x);
-            acc.y = fmaf(w, v.y, acc.y);
-            acc.z = fmaf(w, v.z, acc.z);
-            acc.w = fmaf(w, v.w, acc.w);
+            for (int i = 0; i < cnt; ++i) {
+                const float w = s.sS[i * hpg + h];
+                const float4 v = ((const float4 *)(s.sV + (size_t)i * dv))[c4];
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            ((float4 *)(pv + h * hs * dv))[c4] = acc;
         }
-        ((float4 *)(pv + h * hs * dv))[c4] = acc;
     }
 }
 

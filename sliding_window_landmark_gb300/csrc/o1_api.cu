@@ -97,7 +97,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.fh = (float *)(b + S.fh);
     a.sh = (float *)(b + S.sh);
     a.sn = (float *)(b + S.sn);
-    a.cap = S.cap;
+    a.cap = S.ldc;   // the row stride of E and P
     a.Xk = (unsigned short *)(b + S.Xk);
     a.XvT = (unsigned short *)(b + S.XvT);
     a.Qs = (unsigned short *)(b + S.Qs);

@@ -460,6 +460,21 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     float *sBc = sRow + 128;
     float *sFc = sRow + 192;
     float *sBl = sRow + 256;
+    if (far_any) {   // mu and the block's far records, in flight under the scores
+        float *sMu = sR3;   // [m][65]
+        for (int idx = tid; idx < m * m; idx += 256) {
+            const int aa = idx / m, b = idx % m;
+            sMu[aa * 65 + b] = a.mu[((size_t)gh * m + aa) * m + b];
+        }
+        const size_t nm = (size_t)nh * m;
+        for (int b = tid; b < 64; b += 256) {
+            const size_t wid = (size_t)gh * m + b;
+            sMc[b] = b < m ? a.Fb[(O1_FB_MC * nm + wid) * a.nsub + c] : 0.f;
+            sBc[b] = b < m ? a.Fb[(O1_FB_BASE * nm + wid) * a.nsub + c] : 0.f;
+            sBl[b] = b < m ? a.Fb[(O1_FB_BASELO * nm + wid) * a.nsub + c] : 0.f;
+            sFc[b] = b < m ? a.Fb[(O1_FB_FAC * nm + wid) * a.nsub + c] : 0.f;
+        }
+    }
 
     // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks. A block
     //    without far field needs only the few sink columns: a warp per row.
@@ -564,21 +579,20 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
                     for (int j = 0; j < 4; ++j) sS[(ty + 16 * i) * ldS + 64 * t + tx + 16 * j] = a.scale * acc[t][i][j];
     }
     __syncthreads();   // scores complete before any row reads them (step 2 or 4)
+    // the block's E and in-block prefix P [m][64] into the score staging
+    // (free now), in flight under steps 2 and 3
+    float *sEr = sR1, *sPr = sR1 + (size_t)m * 64;
     if (far_any) {
+        const int nr4 = (nr + 3) >> 2;
+        for (int idx = tid; idx < m * 16; idx += 256) {
+            const int b = idx >> 4, q = idx & 15;
+            const bool ok = q < nr4;   // a chunk of 4 rows from r0 (within the padded row stride)
+            const size_t at = ((size_t)gh * m + b) * a.cap + r0 + 4 * q;
+            cp_async16(sEr + b * 64 + 4 * q, ok ? a.E + at : a.E, ok);
+            cp_async16(sPr + b * 64 + 4 * q, ok ? a.P + at : a.P, ok);
+        }
+        cp_async_commit();
         float *sMu = sR3;   // [m][65]
-        for (int idx = tid; idx < m * m; idx += 256) {
-            const int aa = idx / m, b = idx % m;
-            sMu[aa * 65 + b] = a.mu[((size_t)gh * m + aa) * m + b];
-        }
-        const size_t nm = (size_t)nh * m;
-        for (int b = tid; b < 64; b += 256) {
-            const size_t wid = (size_t)gh * m + b;
-            sMc[b] = b < m ? a.Fb[(O1_FB_MC * nm + wid) * a.nsub + c] : 0.f;
-            sBc[b] = b < m ? a.Fb[(O1_FB_BASE * nm + wid) * a.nsub + c] : 0.f;
-            sBl[b] = b < m ? a.Fb[(O1_FB_BASELO * nm + wid) * a.nsub + c] : 0.f;
-            sFc[b] = b < m ? a.Fb[(O1_FB_FAC * nm + wid) * a.nsub + c] : 0.f;
-        }
-        __syncthreads();
         // 2. F per row and e^{f - F} (columns [0, m))
         for (int i = warp; i < 64; i += 8) {
             const float v0 = lane < m ? sS[i * ldS + lane] : -INFINITY;
@@ -588,6 +602,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             if (lane < m) sS[i * ldS + lane] = expf(v0 - F);
             if (lane + 32 < m) sS[i * ldS + lane + 32] = expf(v1 - F);
         }
+        cp_async_wait<0>();   // this thread's E and P chunks have landed
         __syncthreads();
         // 3. u = e mu, written back over columns [0, m)
         float acc[4][4];
@@ -605,7 +620,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
         for (int idx = tid; idx < m * 64; idx += 256) {
             const int b = idx >> 6, jj = idx & 63;
             const int r = r0 + jj;
-            sE[b * 65 + jj] = (jj < nr && r >= j0) ? sFc[b] * a.E[((size_t)gh * m + b) * a.cap + r] : 0.f;
+            sE[b * 65 + jj] = (jj < nr && r >= j0) ? sFc[b] * sEr[b * 64 + jj] : 0.f;
         }
     }
 
@@ -634,7 +649,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
             // D = sum_b gain_b P_b, in float-float (the terms can cancel to
             // a small fraction of their size)
             auto pmass = [&](int b) -> o1_ff {
-                return ff_fma_f(ff_make(sBc[b], sBl[b]), sFc[b], a.P[((size_t)gh * m + b) * a.cap + r]);
+                return ff_fma_f(ff_make(sBc[b], sBl[b]), sFc[b], sPr[b * 64 + i]);
             };
             o1_ff Dd = ff_make(0.f, 0.f);
             if (lane < m) {

@@ -90,8 +90,9 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 // A chunk call's scratch for up to `cap` rows per pass (nsub = reference
 // blocks of O1_SUB rows):
 //   qr [cap][nh][d]  rotated queries        kr [cap][G][d]  rotated keys
-//   E  [nh][m][cap]  per row, exp(l - block max) of the key it evicts
-//   P  [nh][m][cap]  per row, the in-block prefix of E
+//   E  [nh][m][ldc]  per row, exp(l - block max) of the key it evicts
+//   P  [nh][m][ldc]  per row, the in-block prefix of E
+//                    (ldc = cap rounded up to 4: rows of 16-byte multiples)
 //   Fb [O1_FB_PLANES][nh][m][nsub] per block: local max, local mass (from
 //                    the block kernel), running max M_c, R_c Z_{c-1} and
 //                    the factor exp(local max - M_c) (from the scan), and
@@ -113,7 +114,7 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   Sp  [G][O1_SMALL_NS][O1_SMALL_NQ][dv] value sums, then [..][2] (max, sum)
 struct O1Scratch {
     size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, Sp, total;
-    int cap, nsub, nxp;
+    int cap, ldc, nsub, nxp;
 };
 
 // The tensor-core window path: d in 64-wide chunks (one 128-byte swizzle row
@@ -134,12 +135,13 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
                  m = g.landmarks;
     O1Scratch S;
     S.cap = cap;
+    S.ldc = (cap + 3) & ~3;
     S.nsub = (cap + O1_SUB - 1) / O1_SUB;
     size_t c = (size_t)cap, ns = (size_t)S.nsub, off = 0;
     S.qr = off; off += o1_al256(c * nh * d * 4);
     S.kr = off; off += o1_al256(c * G * d * 4);
-    S.E = off;  off += o1_al256(nh * m * c * 4);
-    S.P = off;  off += o1_al256(nh * m * c * 4);
+    S.E = off;  off += o1_al256(nh * m * (size_t)S.ldc * 4);
+    S.P = off;  off += o1_al256(nh * m * (size_t)S.ldc * 4);
     S.Fb = off; off += o1_al256((O1_FB_PLANES * ns + 3) * nh * m * 4);
     S.Tp = off; off += o1_al256(ns * nh * m * dv * 4);
     S.fh = off; off += o1_al256(c * nh * 4 * 4);
@@ -293,7 +295,7 @@ struct O1Args {
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
-    int cap;
+    int cap;   // the row stride of E and P (a multiple of 4)
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
     unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;

@@ -479,20 +479,38 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     // 1. scores: columns [0, m) landmarks f_a, [m, m + ns) sinks. A block
     //    without far field needs only the few sink columns: a warp per row.
     if (!far_any && ns <= 8) {
-        for (int i = warp; i < nr; i += 8) {
-            const float *qrow = a.qr + ((size_t)(r0 + i) * nh + gh) * d;
-            float qv[O1_MAX_D / 32];
+        // the sink keys in shared memory; a warp takes 4 rows at a time
+        // (rows i0 + 8 rr), their queries loaded together, lanes across d,
+        // and one reduce-scatter leaves score (rr, sink s) in lane 8 rr + s
+        float *sSk = sR1;   // [ns][d]
+        for (int i = tid; i < ns * d; i += 256) sSk[i] = a.sink_k[(size_t)g * ns * d + i];
+        __syncthreads();
+        for (int i0 = warp; i0 < nr; i0 += 32) {
+            float qv[4][O1_MAX_D / 32];
 #pragma unroll
-            for (int t = 0; t < O1_MAX_D / 32; ++t) qv[t] = lane + 32 * t < d ? qrow[lane + 32 * t] : 0.f;
-            for (int x = 0; x < ns; ++x) {
-                const float *sk = a.sink_k + ((size_t)g * ns + x) * d;
-                float dot = 0.f;
+            for (int rr = 0; rr < 4; ++rr) {
+                const int i = i0 + 8 * rr;
+                const float *qrow = a.qr + ((size_t)(r0 + i) * nh + gh) * d;
 #pragma unroll
                 for (int t = 0; t < O1_MAX_D / 32; ++t)
-                    if (lane + 32 * t < d) dot = fmaf(qv[t], sk[lane + 32 * t], dot);
-                dot = warp_sum(dot);
-                if (lane == 0) sS[i * ldS + m + x] = a.scale * dot;
+                    qv[rr][t] = (i < nr && lane + 32 * t < d) ? qrow[lane + 32 * t] : 0.f;
             }
+            float x[32];
+#pragma unroll
+            for (int v = 0; v < 32; ++v) x[v] = 0.f;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                if (s >= ns) break;
+#pragma unroll
+                for (int t = 0; t < O1_MAX_D / 32; ++t) {
+                    const float kv = lane + 32 * t < d ? sSk[s * d + lane + 32 * t] : 0.f;
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) x[rr * 8 + s] = fmaf(qv[rr][t], kv, x[rr * 8 + s]);
+                }
+            }
+            warp_reduce_scatter32(x);
+            const int rr = lane >> 3, s = lane & 7, i = i0 + 8 * rr;
+            if (s < ns && i < nr) sS[i * ldS + m + s] = a.scale * x[0];
         }
     } else {
         // two stages of [query rows [64][SR_LDQ] | landmark and sink rows [64 nbt][SR_LDQ]]

@@ -332,6 +332,24 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
+// Reduce-scatter over a warp: every lane holds 32 partial values; at the
+// step over lane bit b a lane keeps the half of its values that its bit
+// selects and adds the partner's copy of that half. After five steps (31
+// shuffles) x[0] of lane l is the warp's sum of value l.
+__device__ __forceinline__ void warp_reduce_scatter32(float (&x)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int b = 16; b >= 1; b >>= 1) {
+        const bool up = lane & b;
+#pragma unroll
+        for (int i = 0; i < b; ++i) {
+            const float send = up ? x[i] : x[i + b];
+            const float keep = up ? x[i + b] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, b);
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

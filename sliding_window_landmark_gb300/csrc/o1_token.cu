@@ -357,10 +357,8 @@ __device__ __forceinline__ void tok_inputs_finish(const O1Args &a, int g, int nq
 // A near slice for up to 4 heads a group: lanes across the vectors' columns
 // (the queries in registers, each key row read once and without bank
 // conflicts), warps across keys (key = warp + 8 i). A warp's per-lane partial
-// dots leave it through one reduce-scatter butterfly: at the step over lane
-// bit b a lane keeps the half of its values that the bit selects and adds
-// the partner's copy of it, so that after five steps (31 shuffles) lane l
-// holds the sum of value l, value i HPG + h being key i's score for head h.
+// dots leave it through one reduce-scatter (warp_reduce_scatter32): lane l
+// ends with the sum of value l, value i HPG + h being key i's score for head h.
 // The value sums go the same way round (warps across keys, lanes across
 // columns, every head in registers); the 8 warps' partials meet in the key
 // rows' shared memory, free by then.
@@ -406,16 +404,7 @@ __device__ void tok_near_small(const O1Args &a, const TokNearSm &s, int cnt, flo
         }
 #pragma unroll
         for (int i = KPB * HPG; i < 32; ++i) x[i] = 0.f;
-#pragma unroll
-        for (int b = 16; b >= 1; b >>= 1) {
-            const bool up = lane & b;
-#pragma unroll
-            for (int i = 0; i < b; ++i) {
-                const float send = up ? x[i] : x[i + b];
-                const float keep = up ? x[i + b] : x[i];
-                x[i] = keep + __shfl_xor_sync(0xffffffffu, send, b);
-            }
-        }
+        warp_reduce_scatter32(x);
         const int i = lane / HPG, h = lane - i * HPG, key = warp + 8 * (i0 + i);
         if (i < KPB && h < hpg && key < cnt) s.sS[key * hpg + h] = x[0] * a.scale;
     }

@@ -141,6 +141,43 @@ __device__ __forceinline__ void tok_dots(const float *rows, int row, bool valid,
     }
 }
 
+// The same for one vector, its units held in registers: Q.q[t] is unit
+// ub + (lane % U + t) % U of the vector, the unit tok_dot1 reads of a row at
+// step t, so that a row costs one shared-memory load per unit.
+struct TokQ1 {
+    float4 q[8];
+};
+__device__ __forceinline__ void tok_q1_load(const float *qs, int d, TokQ1 &Q) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = d >> 2, U = (nu + 7) >> 3, ub = warp * U;
+    int sidx = lane % U;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const int u = ub + sidx;
+        Q.q[t] = (t < U && u < nu) ? ((const float4 *)qs)[u] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (++sidx == U) sidx = 0;
+    }
+}
+__device__ __forceinline__ float tok_dot1(const float *rows, int row, bool valid, const TokQ1 &Q, int d) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = d >> 2, U = (nu + 7) >> 3, ub = warp * U;
+    if (!valid) return 0.f;
+    const float4 *kr = (const float4 *)(rows + (size_t)row * d);
+    int sidx = lane % U;
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        if (t >= U) break;
+        const int u = ub + sidx;
+        if (++sidx == U) sidx = 0;
+        if (u < nu) {
+            const float4 kv = kr[u];
+            acc = fmaf(Q.q[t].x, kv.x, fmaf(Q.q[t].y, kv.y, fmaf(Q.q[t].z, kv.z, fmaf(Q.q[t].w, kv.w, acc))));
+        }
+    }
+    return acc;
+}
+
 // What a CTA of the step is.
 struct TokRole {
     bool far;
@@ -587,16 +624,17 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
     }
     // partial dots per warp, lane = landmark: kt_a . q' (every a), and
     // qt_b . k_e (the chunk's b, when a key is evicted)
-    for (int a0 = 0; a0 < m; a0 += 32) {
-        const int aa = a0 + lane;
-        float f1[1];
-        tok_dots(s.skt, aa, aa < m, s.sq, 0, 1, d, f1);
-        if (aa < m) s.sPf[warp * m + aa] = f1[0];
-    }
     {
-        float l1[1];
-        tok_dots(s.sqt, lane, evict && lane < nb, s.ske, 0, 1, d, l1);
-        if (lane < nb) s.sPl[warp * MB + lane] = l1[0];
+        TokQ1 Q;
+        tok_q1_load(s.sq, d, Q);
+        for (int a0 = 0; a0 < m; a0 += 32) {
+            const int aa = a0 + lane;
+            const float f = tok_dot1(s.skt, aa, aa < m, Q, d);
+            if (aa < m) s.sPf[warp * m + aa] = f;
+        }
+        if (evict) tok_q1_load(s.ske, d, Q);
+        const float l = tok_dot1(s.sqt, lane, evict && lane < nb, Q, d);
+        if (lane < nb) s.sPl[warp * MB + lane] = l;
     }
     __syncthreads();
     // Every warp: F = max_a f_a and e^{f_a - F} for a = lane, lane + 32 (the
@@ -1097,7 +1135,10 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
     // ---- arrival: the last CTA for a head merges it; the last of all commits
     __syncthreads();   // every partial and record of this CTA is written
     if (tid == 0) {
-        __threadfence();
+        // release: the CTA's partials, records and state writes (ordered
+        // before this thread by the barrier) before its counts; a merger or
+        // the committer takes the matching acquire after its count
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         const unsigned total = (unsigned)(a.NC + a.NF);
         unsigned r[HPG];
         const int nt = ro.far ? 1 : a.hpg;
@@ -1110,7 +1151,7 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
         for (int i = 0; i < HPG; ++i)
             if (i < nt && r[i] == total - 1) mine |= 1u << (ro.far ? ro.hl : i);
         const bool last = ra == gridDim.x - 1;
-        if (mine || last) __threadfence();
+        if (mine || last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
         for (int hl = 0; hl < a.hpg; ++hl)
             if (mine & (1u << hl)) a.tick[ro.g * a.hpg + hl] = 0u;   // every arrival for it is in
         s_mine = mine;

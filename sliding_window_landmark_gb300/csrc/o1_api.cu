@@ -324,6 +324,27 @@ int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scrat
     if (cap < 1 || scratch_bytes < o1_tok_layout(g).total) return O1_ERR_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     O1Args a = state_args(state, g);
+    if (rows == 1) {
+        // one row: the one-row kernel's far chunks insert the evicted key and
+        // the last of them commits; nothing attends
+        const O1TokScratch T = o1_tok_layout(g);
+        char *sb = (char *)scratch;
+        a.part = (float *)(sb + T.part);
+        a.pml = (float *)(sb + T.pml);
+        a.farp = (float *)(sb + T.farp);
+        a.kcur = (float *)(sb + T.kcur);
+        a.KC = T.KC;
+        a.NC = T.NC;
+        a.NF = T.NF;
+        a.MB = T.MB;
+        a.tok_smem = T.smem;
+        a.tok_prefetch = tok_prefetch_for(st, state);
+        a.tok_commit_only = 1;
+        a.k = k;
+        a.v = v;
+        a.R = 1;
+        return o1_launch_token(a, st) == cudaSuccess ? O1_OK : O1_ERR_CUDA;
+    }
     for (int r0 = 0; r0 < rows; r0 += cap) {
         const int R = rows - r0 < cap ? rows - r0 : cap;
         const O1Scratch S = o1_scratch_layout(g, R);

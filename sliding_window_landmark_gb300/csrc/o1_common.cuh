@@ -305,6 +305,7 @@ struct O1Args {
     int KC, NC, NF, MB;
     size_t tok_smem;
     int tok_prefetch;   // issue the state copies before waiting on the previous kernel
+    int tok_commit_only;   // push the row (rotation, far insert, ring, meta) without attending
 };
 
 // ---------------------------------------------------------------- helpers

@@ -283,6 +283,7 @@ __device__ __forceinline__ TokFarSm tok_far_sm(const O1Args &a, float *sm) {
 }
 
 // Thread 0: the copies of the state a CTA needs, for meta `mt`.
+template <bool CO>
 __device__ void tok_issue(const O1Args &a, const TokRole &ro, const O1Meta &mt, float *sm) {
     const int d = a.d, dv = a.dv;
     if (!ro.far) {
@@ -312,6 +313,16 @@ __device__ void tok_issue(const O1Args &a, const TokRole &ro, const O1Meta &mt, 
                 tok_bulk(s.sV + (size_t)(nsk + na) * dv, a.ring_v + (size_t)ro.g * a.w * dv,
                          (uint32_t)(nr - na) * dv * 4, s.bar);
             }
+        }
+    } else if constexpr (CO) {
+        // the insert's operands only: landmark queries, T rows, the evicted pair
+        const TokFarSm s = tok_far_sm(a, sm);
+        const int b0 = ro.fc * a.MB, nb = max(0, min(a.MB, a.m - b0));
+        if (mt.len0 == mt.wg && nb > 0) {
+            tok_bulk(s.sT, a.T + ((size_t)ro.h * a.m + b0) * dv, (uint32_t)nb * dv * 4, s.bar);
+            tok_bulk(s.sqt, a.qt + ((size_t)ro.h * a.m + b0) * d, (uint32_t)nb * d * 4, s.bar);
+            tok_bulk(s.ske, a.ring_k + ((size_t)ro.g * a.w + mt.head0) * d, (uint32_t)d * 4, s.bar);
+            tok_bulk(s.sve, a.ring_v + ((size_t)ro.g * a.w + mt.head0) * dv, (uint32_t)dv * 4, s.bar);
         }
     } else {
         const TokFarSm s = tok_far_sm(a, sm);
@@ -733,6 +744,45 @@ __device__ void tok_far_compute(const O1Args &a, const TokRole &ro, const O1Meta
     }
 }
 
+// A pushed row without attention (o1_spec_commit of one row): the far
+// chunk's insert of the evicted key only, with the same arithmetic as
+// tok_far_compute: l_b, M' = max(M, l_b), rho, e, Z in float-float, and T.
+__device__ void tok_far_insert(const O1Args &a, const TokRole &ro, const O1Meta &mt, const TokFarSm &s, float Mo,
+                               o1_ff Zo) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = a.d, dv = a.dv, m = a.m, MB = a.MB, h = ro.h;
+    const int b0 = ro.fc * MB, nb = max(0, min(MB, m - b0));
+    if (mt.len0 != mt.wg || nb == 0) return;   // nothing evicted, or no landmark here
+    {
+        TokQ1 Q;
+        tok_q1_load(s.ske, d, Q);
+        const float l = tok_dot1(s.sqt, lane, lane < nb, Q, d);
+        if (lane < nb) s.sPl[warp * MB + lane] = l;
+    }
+    __syncthreads();
+    if (warp == 1 && lane < nb) {
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) l += s.sPl[w * MB + lane];
+        l *= a.scale;
+        const float Mn = fmaxf(Mo, l);
+        const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
+        const float e = expf(l - Mn);
+        const o1_ff Zn = ff_add_f(ff_mul_f(Zo, rho), e);
+        const size_t at = (size_t)h * m + b0 + lane;
+        a.M[at] = Mn;
+        a.Z[at] = Zn.hi;
+        a.Zlo[at] = Zn.lo;
+        s.sRho[lane] = rho;
+        s.sE[lane] = e;
+    }
+    __syncthreads();
+    for (int i = tid; i < nb * dv; i += blockDim.x) {
+        const int b = i / dv, t = i - b * dv;
+        a.T[((size_t)h * m + b0 + b) * dv + t] = s.sRho[b] * s.sT[b * dv + t] + s.sE[b] * s.sve[t];
+    }
+}
+
 // Bulk copy without its own expect-tx: the bytes of a batch of them are
 // announced once on the barrier (tok_merge_issue).
 __device__ __forceinline__ void tok_bulk_nx(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -1010,7 +1060,10 @@ __device__ void tok_commit_warp(const O1Args &a, long long p, int *sslot) {
 
 }  // namespace
 
-template <int HPG>
+// CO: a pushed row without attention (o1_spec_commit of one row): only the
+// far chunks, which insert the evicted key; the last CTA commits. A
+// separate instance, so that the attending kernel's code does not carry it.
+template <int HPG, bool CO>
 __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     __shared__ long long s_pos;
@@ -1049,11 +1102,11 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
             mt.head0 = s_meta[1];
             mt.farl0 = s_meta[2];
             mt.wg = s_meta[3];
-            tok_issue(a, ro, mt, sm);
+            tok_issue<CO>(a, ro, mt, sm);
         }
     }
     const float inv = tid < (a.d >> 1) ? a.hdr->inv_freq[tid] : 0.f;   // a constant of the layer
-    if (ro.far) {   // mu's columns of the chunk: a constant of the layer
+    if (ro.far && !CO) {   // mu's columns of the chunk: a constant of the layer
         const int b0 = ro.fc * a.MB, nb = max(0, min(a.MB, a.m - b0));
         for (int i = tid; i < a.m * nb; i += blockDim.x) {
             const int aa = i / nb, j = i - aa * nb;
@@ -1073,7 +1126,7 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
     tok_wait_primary();
     tok_allow_dependents();
     TokIn<HPG> in;
-    if (ro.far) tok_inputs_load<HPG>(a, ro.g, ro.h, 1, in, svr, sgt);
+    if (ro.far) tok_inputs_load<HPG>(a, ro.g, ro.h, CO ? 0 : 1, in, svr, sgt);
     else tok_inputs_load<HPG>(a, ro.g, ro.g * a.hpg, a.hpg, in, svr, sgt);
     float Mo = -INFINITY;
     o1_ff Zo = ff_make(0.f, 0.f);
@@ -1103,7 +1156,7 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
             mt.head0 = mt1[1];
             mt.farl0 = mt1[2];
             mt.wg = mt1[3];
-            tok_issue(a, ro, mt, sm);
+            tok_issue<CO>(a, ro, mt, sm);
         }
         s_parity = parity;
     }
@@ -1125,12 +1178,19 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
             vpush = ns.sV + (size_t)ip * a.dv;
         }
     }
-    tok_inputs_finish<HPG>(a, ro.g, ro.far ? 1 : a.hpg, cs, sn, in, sq, sk, kpush, vpush);
+    tok_inputs_finish<HPG>(a, ro.g, ro.far ? (CO ? 0 : 1) : a.hpg, cs, sn, in, sq, sk, kpush, vpush);
     tok_cp_wait();
     tok_wait_copies(a, bar, (uint32_t)s_parity);
     __syncthreads();
-    if (ro.far) tok_far_compute(a, ro, mt, fs, Mo, Zo);
-    else tok_near_compute<HPG>(a, ro, mt, ns);
+    if constexpr (CO) {
+        if (ro.hl == 0 && ro.fc == 0)   // the group's rotated key, for the commit
+            for (int j = tid; j < a.d; j += blockDim.x) a.kcur[(size_t)ro.g * a.d + j] = sk[j];
+        tok_far_insert(a, ro, mt, fs, Mo, Zo);
+    } else if (ro.far) {
+        tok_far_compute(a, ro, mt, fs, Mo, Zo);
+    } else {
+        tok_near_compute<HPG>(a, ro, mt, ns);
+    }
 
     // ---- arrival: the last CTA for a head merges it; the last of all commits
     __syncthreads();   // every partial and record of this CTA is written
@@ -1141,7 +1201,7 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
         const unsigned total = (unsigned)(a.NC + a.NF);
         unsigned r[HPG];
-        const int nt = ro.far ? 1 : a.hpg;
+        const int nt = CO ? 0 : (ro.far ? 1 : a.hpg);   // no merges in a commit
         const unsigned base = ro.far ? (unsigned)ro.h : (unsigned)(ro.g * a.hpg);
 #pragma unroll
         for (int i = 0; i < HPG; ++i) r[i] = i < nt ? atomicAdd(a.tick + base + i, 1u) : 0u;
@@ -1171,25 +1231,26 @@ __global__ __launch_bounds__(256, 2) void k_tok(O1Args a) {
 }
 
 // One instance of the kernel per power of two of heads per group (the
-// smallest at least hpg), so that nothing is unrolled to the largest count.
-template <int HPG>
+// smallest at least hpg), so that nothing is unrolled to the largest count;
+// commits (no near slices, no merges) run the one-head instance of CO.
+template <int HPG, bool CO>
 static cudaError_t tok_launch(const O1Args &a, cudaStream_t st) {
     static unsigned long long done = 0;
     static size_t dyn_max = 0;   // the kernel's static shared memory taken off the 227 KB a block may hold
     unsigned long long bit = 0;
     if (o1_attrs_needed(&done, &bit)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, k_tok<HPG>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_tok<HPG, CO>);
         if (e != cudaSuccess) return e;
         const size_t dmax = 227 * 1024 - fa.sharedSizeBytes;
-        e = cudaFuncSetAttribute(k_tok<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
+        e = cudaFuncSetAttribute(k_tok<HPG, CO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dmax);
         if (e != cudaSuccess) return e;
         __atomic_store_n(&dyn_max, dmax, __ATOMIC_RELAXED);
         o1_attrs_done(&done, bit);
     }
     if (a.tok_smem > __atomic_load_n(&dyn_max, __ATOMIC_RELAXED)) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.nh * a.NF + a.G * a.NC, 1, 1);
+    cfg.gridDim = dim3(a.nh * a.NF + (CO ? 0 : a.G * a.NC), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = a.tok_smem;
     cfg.stream = st;
@@ -1198,14 +1259,15 @@ static cudaError_t tok_launch(const O1Args &a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, k_tok<HPG>, a);
+    cudaLaunchKernelEx(&cfg, k_tok<HPG, CO>, a);
     return cudaGetLastError();
 }
 
 cudaError_t o1_launch_token(const O1Args &a, cudaStream_t st) {
-    if (a.hpg <= 1) return tok_launch<1>(a, st);
-    if (a.hpg <= 2) return tok_launch<2>(a, st);
-    if (a.hpg <= 4) return tok_launch<4>(a, st);
-    if (a.hpg <= 8) return tok_launch<8>(a, st);
-    return tok_launch<16>(a, st);
+    if (a.tok_commit_only) return tok_launch<1, true>(a, st);
+    if (a.hpg <= 1) return tok_launch<1, false>(a, st);
+    if (a.hpg <= 2) return tok_launch<2, false>(a, st);
+    if (a.hpg <= 4) return tok_launch<4, false>(a, st);
+    if (a.hpg <= 8) return tok_launch<8, false>(a, st);
+    return tok_launch<16, false>(a, st);
 }

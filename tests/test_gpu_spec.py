@@ -175,3 +175,51 @@ def test_state_back_then_repush(case):
     torch.cuda.synchronize()
     assert o1.o1_state_flags(gpu.state, gpu.g, clear=True) == o1.O1_FLAG_BACK_REFUSED
     assert torch.equal(gpu.state, before)
+
+
+# (shape, prompt rows, rows committed one at a time, rewind + re-commit pairs)
+ONE_ROW_CASES = [
+    # the ring fills during the one-row commits, then every commit evicts
+    (synth.Shape(groups=2, heads_per_group=2, d=64, dv=64, sinks=4, window=24, landmarks=8), 10, 30, 6),
+    # the stack's landmark count and widths (m = 64, d = dv = 128), ring evicting
+    (synth.Shape(groups=2, heads_per_group=4, d=128, dv=128, sinks=4, window=64, landmarks=64), 80, 12, 6),
+]
+
+
+@pytest.mark.parametrize("case", range(len(ONE_ROW_CASES)))
+def test_one_row_commits_and_rewinds(case):
+    """o1_spec_commit of one row at a time (the one-row kernel's commit mode:
+    the far chunks insert the evicted key, the last CTA pushes the row) lands
+    on the oracle's state, across the ring filling and evicting; then one-row
+    rewinds each followed by a one-row commit of another row, as a looped
+    layer runs them; then attention over that state matches the oracle."""
+    import torch
+    from sliding_window_landmark_gb300 import o1
+    shape, prompt, n, pairs = ONE_ROW_CASES[case]
+    seed = 90 + case
+    c = synth.layer_constants(shape, seed)
+    orc = harness.oracle_layer(shape, c)
+    gpu = harness.GpuLayer(shape, c, max_rows=max(prompt, 16))
+    q, k, v, g = synth.layer_rows(shape, seed, 0, prompt + n + pairs + 16)
+    want, diag = orc.rows(q[:prompt], k[:prompt], v[:prompt], g[:prompt], diag=True)
+    harness.assert_outputs(gpu.rows(q[:prompt], k[:prompt], v[:prompt], g[:prompt]), want, diag, "prompt")
+    kd, vd = gpu.up(k), gpu.up(v)
+    for i in range(prompt, prompt + n):
+        orc.rows(q[i:i + 1], k[i:i + 1], v[i:i + 1], g[i:i + 1])   # the oracle's push (its output unused)
+        o1.check(o1.o1_spec_commit(gpu.state, gpu.g, gpu.scratch, kd[i:i + 1], vd[i:i + 1], 1), "commit")
+    torch.cuda.synchronize()
+    assert o1.o1_state_flags(gpu.state, gpu.g) == 0
+    harness.assert_state(gpu.read(), orc, f"after {n} one-row commits")
+    for j in range(prompt + n, prompt + n + pairs):
+        assert orc.back(1)
+        o1.check(o1.o1_state_back(gpu.state, gpu.g, 1), "back")
+        orc.rows(q[j:j + 1], k[j:j + 1], v[j:j + 1], g[j:j + 1])
+        o1.check(o1.o1_spec_commit(gpu.state, gpu.g, gpu.scratch, kd[j:j + 1], vd[j:j + 1], 1), "commit")
+    torch.cuda.synchronize()
+    assert o1.o1_state_flags(gpu.state, gpu.g) == 0
+    harness.assert_state(gpu.read(), orc, f"after {pairs} rewind + one-row commit pairs")
+    a = prompt + n + pairs
+    want, diag = orc.rows(q[a:a + 16], k[a:a + 16], v[a:a + 16], g[a:a + 16], diag=True)
+    harness.assert_outputs(gpu.tokens(q[a:a + 16], k[a:a + 16], v[a:a + 16], g[a:a + 16]), want, diag,
+                           "one-row steps after the commits")
+    harness.assert_state(gpu.read(), orc, "end")

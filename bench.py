@@ -754,7 +754,8 @@ def our_arm(args, rank, world, local_rank):
                                         f"prompt: its rows past the first window cost the same per chunk"},
             "rewind": {"metric": "o1_state_back(1) + one-row o1_spec_commit us/pair", "value": back_us,
                        "unit": "us/pair", "higher_is_better": False,
-                       "config": f"{SPEC_CYCLES} pairs on the decode state, captured once in a CUDA graph"},
+                       "config": f"{SPEC_CYCLES} pairs on the decode state, captured once in a CUDA graph",
+                       "gpu_launches_per_pair": 2},
             "speculative": {"metric": "sealed-layer speculative verify + commit us/cycle", "value": spec_us,
                             "unit": "us/cycle", "higher_is_better": False,
                             "accepted_rows_per_s": SPEC_ACC / (spec_us * 1e-6),

@@ -104,6 +104,7 @@ void scratch_args(O1Args &a, void *scratch, const O1Scratch &S) {
     a.nxp = S.nxp;
     a.tc = S.nxp > 0;
     a.Sp = S.cap >= 2 ? (float *)(b + S.Sp) : nullptr;
+    a.wpart = (float *)(b + S.Wp);
 }
 
 // The state the last one-row step on each stream was launched on. A step on

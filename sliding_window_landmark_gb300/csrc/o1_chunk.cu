@@ -1178,11 +1178,69 @@ static int near_small_ks(const O1Args &a) {
 // (numerator in sn relative to c_s; header (c_s, mass)) under one exponent
 // c = max(true window max, c_s) — the pages' c_all — the denominator floored
 // at 1e-30 in those units (o1b_attend), then the gate (dory_gate1).
+// A window split over key ranges (wsplit > 1) adds its other splits'
+// numerators and masses, each from its own reference, under the same c.
+__device__ void merge_splits(const O1Args &a, size_t rh, float4 wh, float4 sh) {
+    const int lane = threadIdx.x & 31, S = a.wsplit, dv4 = a.dv >> 2;
+    const size_t RN = (size_t)a.R * a.nh;
+    const float *hs = a.wpart + (size_t)(S - 1) * RN * a.dv;   // split headers [S-1][R][nh][4]
+    float cc = fmaxf(wh.z, sh.x);
+    for (int s = 1; s < S; ++s) cc = fmaxf(cc, hs[((size_t)(s - 1) * RN + rh) * 4 + 2]);
+    const float al = wh.x > -INFINITY ? expf(wh.x - cc) : 0.f;
+    const float be = sh.x > -INFINITY ? expf(sh.x - cc) : 0.f;
+    float den = al * wh.y + be * sh.y;
+    float4 acc[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c4 = lane + 32 * u;
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c4 >= dv4) continue;
+        const float4 ow = ((const float4 *)(a.out + rh * a.dv))[c4], sw = ((const float4 *)(a.sn + rh * a.dv))[c4];
+        acc[u] = make_float4(al * ow.x + be * sw.x, al * ow.y + be * sw.y, al * ow.z + be * sw.z, al * ow.w + be * sw.w);
+    }
+    for (int s = 1; s < S; ++s) {
+        const float4 h = *(const float4 *)(hs + ((size_t)(s - 1) * RN + rh) * 4);
+        if (!(h.x > -INFINITY)) continue;   // no key of this row in that split
+        const float f = expf(h.x - cc);
+        den += f * h.y;
+        const float4 *on = (const float4 *)(a.wpart + ((size_t)(s - 1) * RN + rh) * a.dv);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c4 = lane + 32 * u;
+            if (c4 >= dv4) continue;
+            const float4 o = on[c4];
+            acc[u].x = fmaf(f, o.x, acc[u].x);
+            acc[u].y = fmaf(f, o.y, acc[u].y);
+            acc[u].z = fmaf(f, o.z, acc[u].z);
+            acc[u].w = fmaf(f, o.w, acc[u].w);
+        }
+    }
+    const float rd = 1.f / fmaxf(den, 1e-30f);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c4 = lane + 32 * u;
+        if (c4 >= dv4) continue;
+        float y[4] = {acc[u].x * rd, acc[u].y * rd, acc[u].z * rd, acc[u].w * rd};
+        if (a.gate) {
+            const float4 gv = ((const float4 *)(a.gate + rh * a.dv))[c4];
+            y[0] = y[0] / (1.f + expf(-gv.x));
+            y[1] = y[1] / (1.f + expf(-gv.y));
+            y[2] = y[2] / (1.f + expf(-gv.z));
+            y[3] = y[3] / (1.f + expf(-gv.w));
+        }
+        ((float4 *)(a.out + rh * a.dv))[c4] = make_float4(y[0], y[1], y[2], y[3]);
+    }
+}
+
 __global__ __launch_bounds__(256) void k_merge(O1Args a) {
     const int lane = threadIdx.x & 31;
     const size_t rh = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (rh >= (size_t)a.R * a.nh) return;
     const float4 wh = *(const float4 *)(a.fh + rh * 4), sh = *(const float4 *)(a.sh + rh * 4);
+    if (a.wsplit > 1) {
+        merge_splits(a, rh, wh, sh);
+        return;
+    }
     const float cc = fmaxf(wh.z, sh.x);
     const float al = expf(wh.x - cc);
     const float be = sh.x > -INFINITY ? expf(sh.x - cc) : 0.f;
@@ -1353,6 +1411,16 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     O1Args a = a_in;
     const int KS = near_small_ks(a);   // > 0: a short pass, its window split over key slices
     if (KS) a.tc = 0;
+    {
+        // window key splits for a tensor-core pass with fewer CTAs than SMs
+        o1_geom gw = {};
+        gw.groups = a.G;
+        gw.heads_per_group = a.hpg;
+        gw.d = a.d;
+        gw.dv = a.dv;
+        gw.window = a.w;
+        a.wsplit = a.tc ? o1_wsplit(gw, a.R) : 1;
+    }
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
     auto begin = [&](int i, cudaStream_t s) {

@@ -31,6 +31,7 @@
 #define O1_MAX_NS 64
 #define O1_MAX_W (1 << 20)
 #define O1_TC_BN 128           // keys per tile of the tensor-core window path
+#define O1_TC_BM 128           // query rows per CTA of the tensor-core window path
 #define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
 // Clock cycles an in-kernel wait may spin before the kernel gives up (about
 // 2 s at the maximum SM clock). Drains of copies or MMAs already in flight
@@ -112,8 +113,11 @@ static inline O1Layout o1_layout(const o1_geom &g) {
 //   Xk  [2][G][nxp][d]    XvT [2][G][dv][nxp]    Qs [2][cap][nh][d]
 // and, for passes of 2 .. O1_SMALL_NQ / hpg rows, the window partials
 //   Sp  [G][O1_SMALL_NS][O1_SMALL_NQ][dv] value sums, then [..][2] (max, sum)
+// and, for tensor-core passes split over key ranges (o1_wsplit), the window
+// numerators and headers of splits 1 .. S-1 (split 0 writes `out` and fh):
+//   Wp  [S-1][R][nh][dv], then [S-1][R][nh][4]
 struct O1Scratch {
-    size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, Sp, total;
+    size_t qr, kr, E, P, Fb, Tp, fh, sh, sn, Xk, XvT, Qs, Sp, Wp, total;
     int cap, ldc, nsub, nxp;
 };
 
@@ -124,6 +128,21 @@ struct O1Scratch {
 // 256..511), and a window wide enough to pay for the panel gather.
 static inline bool o1_tc_supported(const o1_geom &g) {
     return g.d % 64 == 0 && g.d <= 256 && g.dv % 32 == 0 && g.dv <= 256 && g.window >= O1_TC_MIN_WINDOW;
+}
+
+// Key splits of the tensor-core window kernel for a pass of R rows. A pass
+// with fewer CTAs (row blocks x heads) than the GPU has SMs splits each row
+// block's key tiles over up to S CTAs, so that short passes (a 64-row chunk
+// holds one row block a head) still fill the GPU; the splits' partials meet
+// in the merge under one exponent. S stays within the key tiles a row block
+// can have.
+static inline int o1_wsplit(const o1_geom &g, int R) {
+    if (!o1_tc_supported(g) || R < 2) return 1;
+    const int ctas = ((R + O1_TC_BM - 1) / O1_TC_BM) * g.groups * g.heads_per_group;
+    if (ctas >= 148) return 1;
+    const int tmax = (g.window + O1_TC_BM + O1_TC_BN - 1) / O1_TC_BN + 1;
+    const int S = (148 + ctas - 1) / ctas;
+    return S < tmax ? S : tmax;
 }
 
 // Keys per group in the fp16 panels: the ring, the pass's rows, one tile of
@@ -155,6 +174,17 @@ static inline O1Scratch o1_scratch_layout(const o1_geom &g, int cap) {
     // short passes: window partials per (group, key slice, query vector),
     // present from two rows up (a one-row pass never takes that path)
     S.Sp = off;  off += o1_al256(cap >= 2 ? G * O1_SMALL_NS * O1_SMALL_NQ * (dv + 2) * 4 : 0);
+    // split partials: the most (S - 1) x R over the passes this scratch can
+    // run (S falls as the row blocks grow)
+    size_t wrows = 0;
+    for (int nrb = 1; (size_t)(nrb - 1) * O1_TC_BM < c; ++nrb) {
+        const int R = (int)(c < (size_t)nrb * O1_TC_BM ? c : (size_t)nrb * O1_TC_BM);
+        const int Sw = o1_wsplit(g, R);
+        if (Sw <= 1) break;
+        const size_t wr = (size_t)(Sw - 1) * R;
+        wrows = wr > wrows ? wr : wrows;
+    }
+    S.Wp = off;  off += o1_al256(wrows * nh * (dv + 4) * 4);
     S.total = off;
     return S;
 }
@@ -296,6 +326,10 @@ struct O1Args {
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;   // the row stride of E and P (a multiple of 4)
+    // window key splits (o1_wsplit): S, and splits 1 .. S-1's numerators
+    // [S-1][R][nh][dv] followed by their headers [S-1][R][nh][4]
+    int wsplit;
+    float *wpart;
     // tensor-core window path (tc = 1): fp16 panels of nxp keys per group
     unsigned short *Xk, *XvT, *Qs;
     int nxp, tc;

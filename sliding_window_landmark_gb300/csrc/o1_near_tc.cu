@@ -51,7 +51,7 @@
 
 namespace {
 
-constexpr int TC_BM = 128;         // query rows per CTA
+constexpr int TC_BM = O1_TC_BM;    // query rows per CTA
 constexpr int TC_BN = O1_TC_BN;    // keys per tile
 constexpr int TC_SLOT = 32768;     // bytes per ring slot
 constexpr int TC_THREADS = 192;
@@ -187,7 +187,8 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // The CTA's tile schedule; every role derives the same one.
 struct TcPlan {
-    int r0, nr, h, g, kt0, nt, nkc;
+    int r0, nr, h, g, kt0, nkc;
+    int split, jb, nt;   // key split blockIdx.z: tiles jb .. jb + nt - 1 of the row block
     O1Meta mt;
 };
 
@@ -203,7 +204,13 @@ __device__ __forceinline__ TcPlan tc_plan(const O1Args &a) {
     const int lo_first = max(0, p.mt.len0 + p.r0 + 1 - p.mt.wg);
     const int hi_last = p.mt.len0 + p.r0 + p.nr - 1;
     p.kt0 = lo_first & ~7;   // TMA x coordinates of the fp16 value panel: 16-byte aligned
-    p.nt = (hi_last - p.kt0) / TC_BN + 1;
+    // a contiguous run of the row block's key tiles per split (gridDim.z
+    // splits; a split past the last tile has none and writes an empty header)
+    const int ntall = (hi_last - p.kt0) / TC_BN + 1;
+    const int per = (ntall + (int)gridDim.z - 1) / (int)gridDim.z;
+    p.split = blockIdx.z;
+    p.jb = p.split * per;
+    p.nt = max(0, min(ntall, p.jb + per) - p.jb);
     p.nkc = a.d / 64;        // 64 fp16 = one 128-byte swizzle row; one ring slot per d-chunk (hi, lo)
     return p;
 }
@@ -332,7 +339,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
     if (warp == 4) {
         // ---------------------------------------------------- TMA producer
         // (starts at once: the Q tile has its own smem)
-        if (lane == 0) {
+        if (lane == 0 && pl.nt > 0) {
             // the Q tile, fp16 hi and lo, straight into its swizzled slots
             // (rows past R read as zeros)
             mbar_expect_tx(q_ready, 2 * pl.nkc * 16384);
@@ -353,8 +360,8 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                     const int s = next(2 * TC_BN * 128);
                     if (s < 0) return false;
                     for (int hl = 0; hl < 2; ++hl)
-                        tma_3d(sR + (size_t)s * TC_SLOT + hl * (TC_BN * 128), &mk, 64 * c, ybase + pl.kt0 + TC_BN * j, hl,
-                               &full[s]);
+                        tma_3d(sR + (size_t)s * TC_SLOT + hl * (TC_BN * 128), &mk, 64 * c,
+                               ybase + pl.kt0 + TC_BN * (pl.jb + j), hl, &full[s]);
                 }
                 return true;
             };
@@ -363,7 +370,8 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
                     for (int hl = 0; hl < 2; ++hl) {
                         const int s = next(dv * 128);
                         if (s < 0) return false;
-                        tma_3d(sR + (size_t)s * TC_SLOT, &mv, pl.kt0 + TC_BN * j + 64 * kh, pl.g * dv, hl, &full[s]);
+                        tma_3d(sR + (size_t)s * TC_SLOT, &mv, pl.kt0 + TC_BN * (pl.jb + j) + 64 * kh, pl.g * dv, hl,
+                               &full[s]);
                     }
                 return true;
             };
@@ -380,7 +388,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             const uint32_t id_s = idesc_f16(TC_BM, TC_BN), id_o = idesc_f16(TC_BM, dv);
             const uint32_t qh0 = su32(sQh), ql0 = su32(sQl), ra = su32(sR);
             int it = 0;
-            bool ok = mbar_wait(q_ready, 0, abort, wl);
+            bool ok = pl.nt > 0 && mbar_wait(q_ready, 0, abort, wl);
             tc_after();
             // S = Q_hi.K_hi + Q_hi.K_lo + Q_lo.K_hi, one ring slot per d-chunk
             auto issue_s = [&](int j) -> bool {
@@ -452,7 +460,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             if (!ok) break;
             tc_after();
             const uint32_t scol = lane_base + TC_S_COL + TC_BN * (j & 1);
-            const int x0 = pl.kt0 + TC_BN * j;
+            const int x0 = pl.kt0 + TC_BN * (pl.jb + j);
             const bool all_in = valid && x0 >= lo && x0 + TC_BN - 1 <= hi;
             const int a0 = lo - x0, a1 = hi - x0;   // valid columns [a0, a1]
             // pass 1: the tile's row max (scores scaled to log2 units, masked).
@@ -556,9 +564,16 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             // max, natural units) and its numerator O, which goes to `out`
             // through shared memory with coalesced stores; the side readout
             // merges it with the sinks and the far field and applies the gate
+            // (split s > 0 writes the same into its partial, the merge adds
+            // the splits up; a split without tiles writes an empty header)
+            const size_t RN = (size_t)a.R * a.nh;
+            float *hdr = pl.split == 0 ? a.fh : a.wpart + (size_t)(gridDim.z - 1) * RN * dv + (pl.split - 1) * RN * 4;
             if (valid)
-                *(float4 *)(a.fh + ((size_t)r * a.nh + pl.h) * 4) = make_float4(
+                *(float4 *)(hdr + ((size_t)r * a.nh + pl.h) * 4) = make_float4(
                     mref * 0.6931471805599453f, l, mtrue * 0.6931471805599453f, 0.f);
+        }
+        if (ok && pl.nt > 0) {
+            float *onum = pl.split == 0 ? a.out : a.wpart + (pl.split - 1) * (size_t)a.R * a.nh * dv;
             float *so = (float *)sm;   // Q and the ring are free: every MMA has completed
             const int ostride = dv + 4;
             uint32_t o[32];
@@ -576,7 +591,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
             const int n4 = pl.nr * dv4;
             for (int idx = tid; idx < n4; idx += TC_BM) {
                 const int i = idx / dv4, c4 = idx % dv4;
-                *(float4 *)(a.out + ((size_t)(pl.r0 + i) * a.nh + pl.h) * dv + 4 * c4) =
+                *(float4 *)(onum + ((size_t)(pl.r0 + i) * a.nh + pl.h) * dv + 4 * c4) =
                     *(const float4 *)(so + i * ostride + 4 * c4);
             }
         }
@@ -591,7 +606,7 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
     // may still be in flight (the Q tile and the last nslot ring items) before
     // the block's shared memory is given up.
     if (warp == 4 && lane == 0 && *abort) {
-        mbar_drain(q_ready, 0);
+        if (pl.nt > 0) mbar_drain(q_ready, 0);
         for (int i = max(0, issued - nslot); i < issued; ++i) mbar_drain(&full[i % nslot], (i / nslot) & 1);
     }
     __syncthreads();
@@ -677,6 +692,7 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh), TC_THREADS, smem, st>>>(a, mk, mv, mq, NXp, nslot);
+    const int S = a.wsplit > 1 ? a.wsplit : 1;
+    k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh, S), TC_THREADS, smem, st>>>(a, mk, mv, mq, NXp, nslot);
     return cudaGetLastError();
 }

@@ -372,29 +372,64 @@ def our_arm(args, rank, world, local_rank):
     out0 = sets[(args.warmup + args.steps - 1) % N_SETS]["out"]
     assert torch.isfinite(out0).all().item(), "non-finite output"
 
-    # ---- end to end: host buffers in, host output back, through the C ABI
-    host_out = torch.empty((ROWS, sh.nh, sh.dv), dtype=torch.float32).pin_memory()
-    s = sets[0]
+    # ---- end to end: host buffers in, host output back, through the C ABI.
+    # As a serving loop runs it: two device input sets; while step i
+    # computes, step i+1's inputs go up on one copy stream and step i-1's
+    # output comes down on another. Every step still copies its own inputs
+    # from pinned host memory and reads its output back inside the timed
+    # region; events order each buffer's reuse.
+    host_outs = [torch.empty((ROWS, sh.nh, sh.dv), dtype=torch.float32).pin_memory() for _ in range(2)]
+    bufs = [sets[0], sets[1 % N_SETS]]
+    up_st, down_st = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # set b's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # set b's step has computed (inputs free, output ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # set b's output is on the host (buffer free)
+    for b in range(2):
+        ev_done[b].record(stream)
+        ev_out[b].record(stream)
 
-    def e2e_step():
-        for name, h in (("q", hq), ("k", hk), ("v", hv), ("g", hg)):
-            s[name].copy_(h, non_blocking=True)
-        s["state"].copy_(pristine, non_blocking=True)
-        o1.check(o1.o1_chunk_attend(s["state"], g, scratch, s["q"], s["k"], s["v"], s["g"], ROWS, s["out"]),
-                 "chunk")
-        host_out.copy_(s["out"], non_blocking=True)
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_upload(i):
+        b = i % 2
+        up_st.wait_event(ev_done[b])
+        with torch.cuda.stream(up_st):
+            for name, h in (("q", hq), ("k", hk), ("v", hv), ("g", hg)):
+                bufs[b][name].copy_(h, non_blocking=True)
+        ev_in[b].record(up_st)
+
+    def e2e_compute(i):
+        b = i % 2
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])
+        bufs[b]["state"].copy_(pristine, non_blocking=True)
+        o1.check(o1.o1_chunk_attend(bufs[b]["state"], g, scratch, bufs[b]["q"], bufs[b]["k"], bufs[b]["v"],
+                                    bufs[b]["g"], ROWS, bufs[b]["out"]), "chunk")
+        ev_done[b].record(stream)
+        down_st.wait_event(ev_done[b])
+        with torch.cuda.stream(down_st):
+            host_outs[b].copy_(bufs[b]["out"], non_blocking=True)
+        ev_out[b].record(down_st)
+
+    def e2e_run(n):
+        for st_ in (up_st, down_st):   # nothing of the run starts before the start event
+            st_.wait_stream(stream)
+        e2e_upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                e2e_upload(i + 1)
+            e2e_compute(i)
+        stream.wait_event(ev_out[(n - 1) % 2])
+        stream.wait_event(ev_out[n % 2])
+
+    e2e_run(max(1, args.warmup))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
-    d2h = host_out.numel() * 4
+    d2h = host_outs[0].numel() * 4
 
     # ---- comparator: exact causal attention over the same 4096-row prompt
     # (window = the prompt, no sinks, no far field) through o1_window_attend,
@@ -695,7 +730,9 @@ def our_arm(args, rank, world, local_rank):
             "stages_ms": {o1.o1_stage_name(j): float(stage_avg[j]) for j in range(nst)},
             "gpu_launches": launches * args.steps,
             "e2e": {"value": ROWS * args.steps * world / (e2e_ms * 1e-3), "unit": "rows/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "pinned host buffers; two device input sets, the next step's upload and the "
+                            "previous step's download on their own streams beside the current step"},
             "decode": {"metric": "sealed-layer decode us/token", "value": dec_us, "unit": "us/token",
                        "higher_is_better": False,
                        "config": "same layer after an 8192-row prompt; 256 one-row o1_token_attend steps, "

@@ -806,6 +806,206 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     }
 }
 
+// ---------------------------------------------------------- short passes
+
+// A pass of at most O1_SHORT_ROWS rows: the far field and the sinks of head
+// blockIdx.x in one CTA, row after row as the oracle takes them, in place
+// of the 64-row block kernels (k_far_block, k_far_tscan, k_side_readout).
+// Per row: the insert of the key it evicts (o1b_far_e / o1b_far_commit for
+// one key: l_b = scale qt_b . k_e, M' = max(M, l_b), rho, e, Z in
+// float-float, T = rho T + e v_e), then its readout (o1b_attend's far and
+// sink parts): f_a = scale q'.kt_a, F, u_b = sum_a e^{f_a - F} mu[a][b]
+// (rect), c_f = max_b (F + M_b), gains, D = sum_b gain_b Z_b in float-float
+// and the sign decision, numerator sum_b gain_b T_b; sink scores; all under
+// c_s = max(sink max, c_f) into the side header (c_s, side mass) and side
+// numerator, as k_side_readout leaves them. A commit pass
+// (short_no_readout) only inserts. The far state is written back when the
+// pass commits.
+__host__ __device__ inline size_t short_smem_floats(const O1Args &a) {
+    const size_t m = a.m, d = a.d, dv = a.dv, ns = a.ns, R = a.R;
+    return 2 * m * d + (m * m + 3) / 4 * 4 + m * dv + ns * (d + dv) + R * (2 * d + dv) + 3 * 64 + 5 * 64 + dv + 16 +
+           256;
+}
+
+__global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
+    extern __shared__ __align__(16) float sm[];
+    const int h = blockIdx.x, g = h / a.hpg, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = a.m, d = a.d, dv = a.dv, ns = a.ns, R = a.R, nh = a.nh;
+    const O1Meta mt = o1_meta(a, g);
+    const int j0 = mt.wg - mt.len0;   // row r evicts X[r - j0] once r >= j0
+    const bool far_on = !a.exact, readout = !a.short_no_readout;
+    float *skt = sm;                                  // [m][d]   landmark keys of the group
+    float *sqt = skt + (size_t)m * d;                 // [m][d]   landmark queries of the head
+    float *smu = sqt + (size_t)m * d;                 // [m][m]
+    float *sT = smu + (size_t)(m * m + 3) / 4 * 4;    // [m][dv]  far value sums (the running state), 16-byte aligned
+    float *ssk = sT + (size_t)m * dv;                 // [ns][d]
+    float *ssv = ssk + (size_t)ns * d;                // [ns][dv]
+    float *sKe = ssv + (size_t)ns * dv;               // [R][d]   the key each row evicts
+    float *sVe = sKe + (size_t)R * d;                 // [R][dv]  and its value
+    float *sQ = sVe + (size_t)R * dv;                 // [R][d]   the rows' rotated queries
+    float *sM = sQ + (size_t)R * d;                   // [64]
+    float *sZh = sM + 64, *sZl = sZh + 64;            // [64]     far mass, high and low parts
+    float *sL = sZl + 64;                             // [64]     l_b, then f_a
+    float *sS = sL + 64;                              // [64]     sink scores
+    float *sU = sS + 64;                              // [64]     u_b, then gains
+    float *sRho = sU + 64, *sE = sRho + 64;           // [64]     the insert's rescale and weight
+    float *sNum = sE + 64;                            // [dv]     far numerator
+    float *sc = sNum + dv;                            // scalars: F, c_f, D hi, D lo, have
+    float *sUp = sc + 16;                             // [256] partial u_b
+
+    // the head's operands and state, and every row's evicted pair and query:
+    // 16-byte asynchronous copies, all in flight together (rows of d and dv
+    // floats are 16-byte multiples; zero-filled where there is nothing)
+    const int d4 = d >> 2, dv4 = dv >> 2;
+    for (int i = tid; i < m * d4; i += 256) {
+        cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, far_on);
+        cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, far_on);
+    }
+    for (int i = tid; i < m * dv4; i += 256) cp_async16(sT + 4 * i, a.T + (size_t)h * m * dv + 4 * i, far_on);
+    for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, true);
+    for (int i = tid; i < ns * dv4; i += 256) cp_async16(ssv + 4 * i, a.sink_v + (size_t)g * ns * dv + 4 * i, true);
+    for (int i = tid; i < R * d4; i += 256) {
+        const int r = i / d4, j = i - r * d4;
+        const bool ev = far_on && r >= j0;
+        cp_async16(sKe + 4 * i, ev ? o1_key(a, g, r - j0, mt) + 4 * j : a.kt, ev);
+        cp_async16(sQ + 4 * i, readout ? a.qr + ((size_t)r * nh + h) * d + 4 * j : a.kt, readout);
+    }
+    for (int i = tid; i < R * dv4; i += 256) {
+        const int r = i / dv4, j = i - r * dv4;
+        const bool ev = far_on && r >= j0;
+        cp_async16(sVe + 4 * i, ev ? o1_val(a, g, r - j0, mt) + 4 * j : a.kt, ev);
+    }
+    cp_async_commit();
+    for (int i = tid; i < m * m; i += 256) smu[i] = far_on ? a.mu[(size_t)h * m * m + i] : 0.f;
+    for (int b = tid; b < m; b += 256) {
+        sM[b] = far_on ? a.M[(size_t)h * m + b] : -INFINITY;
+        sZh[b] = far_on ? a.Z[(size_t)h * m + b] : 0.f;
+        sZl[b] = far_on ? a.Zlo[(size_t)h * m + b] : 0.f;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // a warp per row of `rows` ([n][ld]), lanes across d: scale x . row -> out
+    auto dots = [&](const float *rows, int n, const float *x, float *out) {
+        float xr[O1_MAX_D / 32];
+#pragma unroll
+        for (int t = 0; t < O1_MAX_D / 32; ++t) xr[t] = lane + 32 * t < d ? x[lane + 32 * t] : 0.f;
+        for (int i = warp; i < n; i += 8) {
+            const float *rw = rows + (size_t)i * d;
+            float acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < O1_MAX_D / 32; ++t)
+                if (lane + 32 * t < d) acc = fmaf(xr[t], rw[lane + 32 * t], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) out[i] = a.scale * acc;
+        }
+    };
+    for (int r = 0; r < R; ++r) {
+        const bool evict = far_on && r >= j0;
+        const int farl = far_on ? mt.farl0 + max(0, r - j0 + 1) : 0;
+        if (evict) {
+            // the insert of the evicted key into every landmark of the head
+            dots(sqt, m, sKe + (size_t)r * d, sL);
+            __syncthreads();
+            if (tid < m) {
+                const float l = sL[tid], Mo = sM[tid];
+                const float Mn = fmaxf(Mo, l);
+                const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
+                const float e = expf(l - Mn);
+                const o1_ff Zn = ff_add_f(ff_mul_f(ff_make(sZh[tid], sZl[tid]), rho), e);
+                sM[tid] = Mn;
+                sZh[tid] = Zn.hi;
+                sZl[tid] = Zn.lo;
+                sRho[tid] = rho;
+                sE[tid] = e;
+            }
+            __syncthreads();
+            const float *ve = sVe + (size_t)r * dv;
+            for (int i = tid; i < m * dv; i += 256) {
+                const int b = i / dv, t = i - b * dv;
+                sT[i] = sRho[b] * sT[i] + sE[b] * ve[t];
+            }
+            __syncthreads();
+        }
+        if (!readout) continue;
+        const float *q = sQ + (size_t)r * d;
+        // far readout of row r
+        if (farl > 0) {
+            dots(skt, m, q, sL);
+            __syncthreads();
+            if (warp == 0) {
+                const float f0 = lane < m ? sL[lane] : -INFINITY, f1 = lane + 32 < m ? sL[lane + 32] : -INFINITY;
+                const float F = warp_max(fmaxf(f0, f1));
+                if (lane < m) sL[lane] = expf(f0 - F);
+                if (lane + 32 < m) sL[lane + 32] = expf(f1 - F);
+                const float c0 = lane < m ? F + sM[lane] : -INFINITY, c1 = lane + 32 < m ? F + sM[lane + 32] : -INFINITY;
+                const float cf = warp_max(fmaxf(c0, c1));
+                if (lane == 0) {
+                    sc[0] = F;
+                    sc[1] = cf;
+                }
+            }
+            __syncthreads();
+            {   // u_b: every thread a share of the landmark keys a for one b
+                const int parts = 256 / m, b = tid % m, pi = tid / m;
+                float u = 0.f;
+                if (pi < parts)
+                    for (int aa = pi; aa < m; aa += parts) u = fmaf(sL[aa], smu[aa * m + b], u);
+                sUp[tid] = u;
+            }
+            __syncthreads();
+            if (tid < m) {   // u_b, then the gain (u_b relative to c_f)
+                float u = 0.f;
+                for (int pi = 0; pi < 256 / m; ++pi) u += sUp[pi * m + tid];
+                if (a.rect) u = fmaxf(u, 0.f);
+                sU[tid] = u * expf(sc[0] + sM[tid] - sc[1]);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                o1_ff D = ff_make(0.f, 0.f);
+                for (int b = lane; b < m; b += 32) D = ff_add(D, ff_mul_f(ff_make(sZh[b], sZl[b]), sU[b]));
+                D = warp_sum(D);
+                if (lane == 0) {
+                    sc[2] = D.hi;
+                    sc[3] = D.lo;
+                    sc[4] = ff_nonneg(D) ? 1.f : 0.f;
+                }
+            }
+            for (int t = tid; t < dv; t += 256) {
+                float acc = 0.f;
+                for (int b = 0; b < m; ++b) acc = fmaf(sU[b], sT[(size_t)b * dv + t], acc);
+                sNum[t] = acc;
+            }
+        }
+        // the row's sink scores
+        dots(ssk, ns, q, sS);
+        __syncthreads();
+        // c_s = max(sink max, c_f); sink weights, side mass and numerator
+        const bool have = farl > 0 && sc[4] > 0.5f;
+        float smax = -INFINITY;
+        for (int x = 0; x < ns; ++x) smax = fmaxf(smax, sS[x]);
+        const float cf = farl > 0 ? sc[1] : -INFINITY;
+        const float cs = fmaxf(smax, cf);
+        const float fs = have ? expf(cf - cs) : 0.f;
+        float side = have ? fs * (sc[2] + sc[3]) : 0.f;
+        for (int x = 0; x < ns; ++x) side += expf(sS[x] - cs);
+        for (int t = tid; t < dv; t += 256) {
+            float acc = have ? fs * sNum[t] : 0.f;
+            for (int x = 0; x < ns; ++x) acc = fmaf(expf(sS[x] - cs), ssv[(size_t)x * dv + t], acc);
+            a.sn[((size_t)r * nh + h) * dv + t] = acc;
+        }
+        if (tid == 0)
+            *(float4 *)(a.sh + ((size_t)r * nh + h) * 4) = make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
+        __syncthreads();   // sL, sS, sU, sNum and the scalars are reused by the next row
+    }
+    if (!a.commit || !far_on) return;   // attend only: the state keeps its far field
+    for (int i = tid; i < m * dv; i += 256) a.T[(size_t)h * m * dv + i] = sT[i];
+    for (int b = tid; b < m; b += 256) {
+        a.M[(size_t)h * m + b] = sM[b];
+        a.Z[(size_t)h * m + b] = sZh[b];
+        a.Zlo[(size_t)h * m + b] = sZl[b];
+    }
+}
+
 // ------------------------------------------------------------------ near
 
 // Block = (rows, group): 32 query slots = floor(32 / hpg) rows x hpg heads,
@@ -1357,6 +1557,7 @@ static void chunk_attrs() {
     cudaFuncSetAttribute(k_far_block<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     cudaFuncSetAttribute(k_far_block<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     cudaFuncSetAttribute(k_near_small, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(k_side_short, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(k_near<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     o1_attrs_done(&done, bit);
@@ -1438,19 +1639,23 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     end(0, st);
     cudaEventRecord(aux->fork, st);
     cudaStreamWaitEvent(sf, aux->fork, 0);
+    // a short pass takes the row-serial far kernel (stages 1 and 2 stay empty)
+    const size_t sfs = short_smem_floats(a) * sizeof(float);
+    const bool short_far = R <= O1_SHORT_ROWS && sfs <= 227 * 1024;
     begin(1, sf);
     const size_t fbs = far_block_smem_floats() * sizeof(float);
-    if (!a.exact) {   // the comparator has no far field
+    if (!a.exact && !short_far) {   // the comparator has no far field
         if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
         else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
     }
     end(1, sf);
     begin(2, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
-    if (!a.exact) k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
+    if (!a.exact && !short_far) k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
     end(2, sf);
     begin(3, sf);
-    if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+    if (short_far) k_side_short<<<a.nh, 256, sfs, sf>>>(a);
+    else if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     end(3, sf);
     cudaEventRecord(aux->join, sf);
@@ -1496,11 +1701,18 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
     k_rope<<<R, 128, 0, st>>>(a);
-    const size_t fbs = far_block_smem_floats() * sizeof(float);
-    if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
-    else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
-    const size_t n = (size_t)a.nh * a.m * a.dv;
-    k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    O1Args as = a;
+    as.short_no_readout = 1;
+    const size_t sfs = short_smem_floats(as) * sizeof(float);
+    if (R <= O1_SHORT_ROWS && sfs <= 227 * 1024) {
+        k_side_short<<<a.nh, 256, sfs, st>>>(as);   // the far inserts of a short commit, row by row
+    } else {
+        const size_t fbs = far_block_smem_floats() * sizeof(float);
+        if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
+        else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
+        const size_t n = (size_t)a.nh * a.m * a.dv;
+        k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+    }
     const int live = R < a.w ? R : a.w;
     k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
     return cudaGetLastError();

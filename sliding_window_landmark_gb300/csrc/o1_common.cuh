@@ -32,6 +32,7 @@
 #define O1_MAX_W (1 << 20)
 #define O1_TC_BN 128           // keys per tile of the tensor-core window path
 #define O1_TC_BM 128           // query rows per CTA of the tensor-core window path
+#define O1_SHORT_ROWS 16       // passes up to this many rows take the row-serial far kernel
 #define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
 // Clock cycles an in-kernel wait may spin before the kernel gives up (about
 // 2 s at the maximum SM clock). Drains of copies or MMAs already in flight
@@ -323,6 +324,7 @@ struct O1Args {
     long long wait_cycles;   // limit of the first waits (o1_set_wait_limit); drains use O1_WAIT_CYCLES_FULL
     int commit;   // 0: attend only, the state is left as it was (speculative verify)
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
+    int short_no_readout;   // short far pass of a commit: inserts only, no side parts
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;   // the row stride of E and P (a multiple of 4)

@@ -318,3 +318,21 @@ def test_timed_stages_and_stream_capture():
     orc = harness.oracle_layer(sh, c)
     orc.rows(q, k, v, g)
     harness.assert_state(cap.read(), orc, "graph replay state")
+
+
+# passes of at most 16 rows take the row-serial far kernel (k_side_short):
+# (shape, calls) with short calls after a prompt that fills the ring, so
+# that every short row evicts, and one set before it fills
+SHORT_CASES = [
+    (synth.Shape(groups=2, heads_per_group=4, d=256, dv=256, sinks=4, window=64, landmarks=32), [100, 2, 16, 5, 9, 1, 3]),
+    (synth.Shape(groups=2, heads_per_group=4, d=128, dv=128, sinks=4, window=48, landmarks=64), [60, 16, 7, 2, 11]),
+    (synth.Shape(groups=1, heads_per_group=2, d=64, dv=64, sinks=0, window=40, landmarks=8), [5, 16, 12, 9, 2]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SHORT_CASES)))
+def test_short_passes(case):
+    """Short passes (the far field and sinks row by row in one CTA a head)
+    against the oracle: outputs of every call and the state after each."""
+    shape, calls = SHORT_CASES[case]
+    _run(shape, 120 + case, calls)

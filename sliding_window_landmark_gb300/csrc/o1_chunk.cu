@@ -820,24 +820,33 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // c_s = max(sink max, c_f) into the side header (c_s, side mass) and side
 // numerator, as k_side_readout leaves them. A commit pass
 // (short_no_readout) only inserts. The far state is written back when the
-// pass commits.
+// pass commits. The value columns are split over gridDim.y CTAs a head
+// (short_col_splits): each repeats the scalars (dots, F, u, gains, D) and
+// takes one slice of T, of the numerators and of the evicted and sink values.
+__host__ __device__ inline int short_col_splits(const O1Args &a) {
+    for (int cs = 4; cs > 1; cs >>= 1)
+        if (a.nh * cs <= 148 && a.dv % (4 * cs) == 0) return cs;
+    return 1;
+}
 __host__ __device__ inline size_t short_smem_floats(const O1Args &a) {
-    const size_t m = a.m, d = a.d, dv = a.dv, ns = a.ns, R = a.R;
-    return 2 * m * d + (m * m + 3) / 4 * 4 + m * dv + ns * (d + dv) + R * (2 * d + dv) + 3 * 64 + 5 * 64 + dv + 16 +
-           256;
+    const size_t m = a.m, d = a.d, dvs = a.dv / short_col_splits(a), ns = a.ns, R = a.R;
+    return 2 * m * d + (m * m + 3) / 4 * 4 + m * dvs + ns * (d + dvs) + R * (2 * d + dvs) + 3 * 64 + 5 * 64 + dvs +
+           16 + 256;
 }
 
 __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     const int h = blockIdx.x, g = h / a.hpg, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m = a.m, d = a.d, dv = a.dv, ns = a.ns, R = a.R, nh = a.nh;
+    const int m = a.m, d = a.d, ns = a.ns, R = a.R, nh = a.nh;
+    const int dvf = a.dv, dv = dvf / (int)gridDim.y, c0 = blockIdx.y * dv;   // this CTA's value columns
+    const bool lead = blockIdx.y == 0;                                       // writes the scalars' results
     const O1Meta mt = o1_meta(a, g);
     const int j0 = mt.wg - mt.len0;   // row r evicts X[r - j0] once r >= j0
     const bool far_on = !a.exact, readout = !a.short_no_readout;
     float *skt = sm;                                  // [m][d]   landmark keys of the group
     float *sqt = skt + (size_t)m * d;                 // [m][d]   landmark queries of the head
     float *smu = sqt + (size_t)m * d;                 // [m][m]
-    float *sT = smu + (size_t)(m * m + 3) / 4 * 4;    // [m][dv]  far value sums (the running state), 16-byte aligned
+    float *sT = smu + (size_t)(m * m + 3) / 4 * 4;    // [m][dv]  far value sums (this slice), 16-byte aligned
     float *ssk = sT + (size_t)m * dv;                 // [ns][d]
     float *ssv = ssk + (size_t)ns * d;                // [ns][dv]
     float *sKe = ssv + (size_t)ns * dv;               // [R][d]   the key each row evicts
@@ -861,9 +870,15 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
         cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, far_on);
         cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, far_on);
     }
-    for (int i = tid; i < m * dv4; i += 256) cp_async16(sT + 4 * i, a.T + (size_t)h * m * dv + 4 * i, far_on);
+    for (int i = tid; i < m * dv4; i += 256) {
+        const int b = i / dv4, j = i - b * dv4;
+        cp_async16(sT + 4 * i, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, far_on);
+    }
     for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, true);
-    for (int i = tid; i < ns * dv4; i += 256) cp_async16(ssv + 4 * i, a.sink_v + (size_t)g * ns * dv + 4 * i, true);
+    for (int i = tid; i < ns * dv4; i += 256) {
+        const int x = i / dv4, j = i - x * dv4;
+        cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, true);
+    }
     for (int i = tid; i < R * d4; i += 256) {
         const int r = i / d4, j = i - r * d4;
         const bool ev = far_on && r >= j0;
@@ -873,7 +888,7 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     for (int i = tid; i < R * dv4; i += 256) {
         const int r = i / dv4, j = i - r * dv4;
         const bool ev = far_on && r >= j0;
-        cp_async16(sVe + 4 * i, ev ? o1_val(a, g, r - j0, mt) + 4 * j : a.kt, ev);
+        cp_async16(sVe + 4 * i, ev ? o1_val(a, g, r - j0, mt) + c0 + 4 * j : a.kt, ev);
     }
     cp_async_commit();
     for (int i = tid; i < m * m; i += 256) smu[i] = far_on ? a.mu[(size_t)h * m * m + i] : 0.f;
@@ -970,9 +985,17 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
                     sc[4] = ff_nonneg(D) ? 1.f : 0.f;
                 }
             }
+            {   // numerator: every thread a share of the landmarks for one column
+                const int parts = 256 / dv, t = tid % dv, pi = tid / dv;
+                float acc = 0.f;
+                if (pi < parts)
+                    for (int b = pi; b < m; b += parts) acc = fmaf(sU[b], sT[(size_t)b * dv + t], acc);
+                sUp[tid] = acc;
+            }
+            __syncthreads();
             for (int t = tid; t < dv; t += 256) {
                 float acc = 0.f;
-                for (int b = 0; b < m; ++b) acc = fmaf(sU[b], sT[(size_t)b * dv + t], acc);
+                for (int pi = 0; pi < 256 / dv; ++pi) acc += sUp[pi * dv + t];
                 sNum[t] = acc;
             }
         }
@@ -991,14 +1014,18 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
         for (int t = tid; t < dv; t += 256) {
             float acc = have ? fs * sNum[t] : 0.f;
             for (int x = 0; x < ns; ++x) acc = fmaf(expf(sS[x] - cs), ssv[(size_t)x * dv + t], acc);
-            a.sn[((size_t)r * nh + h) * dv + t] = acc;
+            a.sn[((size_t)r * nh + h) * dvf + c0 + t] = acc;
         }
-        if (tid == 0)
+        if (tid == 0 && lead)
             *(float4 *)(a.sh + ((size_t)r * nh + h) * 4) = make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
         __syncthreads();   // sL, sS, sU, sNum and the scalars are reused by the next row
     }
     if (!a.commit || !far_on) return;   // attend only: the state keeps its far field
-    for (int i = tid; i < m * dv; i += 256) a.T[(size_t)h * m * dv + i] = sT[i];
+    for (int i = tid; i < m * dv; i += 256) {
+        const int b = i / dv, t = i - b * dv;
+        a.T[((size_t)h * m + b) * dvf + c0 + t] = sT[i];
+    }
+    if (!lead) return;
     for (int b = tid; b < m; b += 256) {
         a.M[(size_t)h * m + b] = sM[b];
         a.Z[(size_t)h * m + b] = sZh[b];
@@ -1654,7 +1681,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     if (!a.exact && !short_far) k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
     end(2, sf);
     begin(3, sf);
-    if (short_far) k_side_short<<<a.nh, 256, sfs, sf>>>(a);
+    if (short_far) k_side_short<<<dim3(a.nh, short_col_splits(a)), 256, sfs, sf>>>(a);
     else if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     end(3, sf);
@@ -1705,7 +1732,7 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     as.short_no_readout = 1;
     const size_t sfs = short_smem_floats(as) * sizeof(float);
     if (R <= O1_SHORT_ROWS && sfs <= 227 * 1024) {
-        k_side_short<<<a.nh, 256, sfs, st>>>(as);   // the far inserts of a short commit, row by row
+        k_side_short<<<dim3(a.nh, short_col_splits(as)), 256, sfs, st>>>(as);   // the far inserts of a short commit
     } else {
         const size_t fbs = far_block_smem_floats() * sizeof(float);
         if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);

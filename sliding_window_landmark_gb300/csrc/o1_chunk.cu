@@ -821,8 +821,9 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // numerator, as k_side_readout leaves them. A commit pass
 // (short_no_readout) only inserts. The far state is written back when the
 // pass commits. The value columns are split over gridDim.y CTAs a head
-// (short_col_splits): each repeats the scalars (dots, F, u, gains, D) and
-// takes one slice of T, of the numerators and of the evicted and sink values.
+// (short_col_splits, up to 4; 8 measured slower): each repeats the scalars
+// (dots, F, u, gains, D) and takes one slice of T, of the numerators and of
+// the evicted and sink values.
 __host__ __device__ inline int short_col_splits(const O1Args &a) {
     for (int cs = 4; cs > 1; cs >>= 1)
         if (a.nh * cs <= 148 && a.dv % (4 * cs) == 0) return cs;
@@ -866,18 +867,18 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     // 16-byte asynchronous copies, all in flight together (rows of d and dv
     // floats are 16-byte multiples; zero-filled where there is nothing)
     const int d4 = d >> 2, dv4 = dv >> 2;
-    for (int i = tid; i < m * d4; i += 256) {
-        cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, far_on);
+    for (int i = tid; i < m * d4; i += 256) {   // (a commit pass reads out nothing: no landmark keys)
+        cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, far_on && readout);
         cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, far_on);
     }
     for (int i = tid; i < m * dv4; i += 256) {
         const int b = i / dv4, j = i - b * dv4;
         cp_async16(sT + 4 * i, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, far_on);
     }
-    for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, true);
+    for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, readout);
     for (int i = tid; i < ns * dv4; i += 256) {
         const int x = i / dv4, j = i - x * dv4;
-        cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, true);
+        cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, readout);
     }
     for (int i = tid; i < R * d4; i += 256) {
         const int r = i / d4, j = i - r * d4;
@@ -891,7 +892,7 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
         cp_async16(sVe + 4 * i, ev ? o1_val(a, g, r - j0, mt) + c0 + 4 * j : a.kt, ev);
     }
     cp_async_commit();
-    for (int i = tid; i < m * m; i += 256) smu[i] = far_on ? a.mu[(size_t)h * m * m + i] : 0.f;
+    for (int i = tid; i < m * m; i += 256) smu[i] = (far_on && readout) ? a.mu[(size_t)h * m * m + i] : 0.f;
     for (int b = tid; b < m; b += 256) {
         sM[b] = far_on ? a.M[(size_t)h * m + b] : -INFINITY;
         sZh[b] = far_on ? a.Z[(size_t)h * m + b] : 0.f;

@@ -46,6 +46,7 @@
 // once (o1_rope_cs: within a few f32 ulp of the pages' f64-then-f32 table)
 // and rotates every query head and every key group with it.
 __global__ void k_rope(O1Args a) {
+    if (a.chain_early) o1_chain_release();
     const int r = blockIdx.x;
     const int half = a.d >> 1;
     const int64_t p = a.hdr->pos + r;
@@ -143,6 +144,8 @@ __host__ __device__ inline size_t far_block_smem_floats() {
 template <int NV>
 __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
     extern __shared__ __align__(16) float sm[];
+    o1_chain_wait();
+    if (a.chain_early) o1_chain_release();
     const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
     const O1Meta mt = o1_meta(a, g);
     const int j0 = mt.wg - mt.len0;
@@ -335,6 +338,8 @@ __global__ __launch_bounds__(256) void k_far_block(O1Args a) {
 // are the new state (o1b_far_e's max / rescale and o1b_far_commit's
 // recurrence, taken as a scan over the blocks).
 __global__ __launch_bounds__(256, 4) void k_far_tscan(O1Args a) {
+    o1_chain_wait();
+    if (a.chain_early) o1_chain_release();
     const size_t n = (size_t)a.nh * a.m * a.dv, nm = (size_t)a.nh * a.m;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= n) return;
@@ -438,6 +443,7 @@ __host__ __device__ inline void side_layout(const O1Args &a, size_t off[6]) {
 template <int NV>
 __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
     extern __shared__ __align__(16) float sm[];
+    o1_chain_wait();
     const int c = blockIdx.x, gh = blockIdx.y, g = gh / a.hpg;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ty = tid >> 4, tx = tid & 15;
@@ -837,6 +843,8 @@ __host__ __device__ inline size_t short_smem_floats(const O1Args &a) {
 
 __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     extern __shared__ __align__(16) float sm[];
+    o1_chain_wait();
+    if (a.chain_early) o1_chain_release();
     const int h = blockIdx.x, g = h / a.hpg, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = a.m, d = a.d, ns = a.ns, R = a.R, nh = a.nh;
     const int dvf = a.dv, dv = dvf / (int)gridDim.y, c0 = blockIdx.y * dv;   // this CTA's value columns
@@ -1046,6 +1054,7 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
 template <int NV>
 __global__ __launch_bounds__(256) void k_near(O1Args a) {
     extern __shared__ float sm[];
+    o1_chain_wait();
     const int dq = a.d + 4, dvq = a.dv + 4;
     float *sQ = sm;
     float *sK = sQ + 32 * dq;
@@ -1219,6 +1228,8 @@ __device__ __forceinline__ void ns_scores(float (&c)[4][4], const float *sQ, con
 
 __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
     extern __shared__ __align__(16) float sm[];
+    o1_chain_wait();
+    if (a.chain_early) o1_chain_release();
     const int s = blockIdx.x, g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ty = tid >> 4, tx = tid & 15;
@@ -1338,6 +1349,7 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
 // them for k_merge.
 __global__ __launch_bounds__(256) void k_near_small_merge(O1Args a, int nsl) {
     __shared__ float smx[4][64], sl[4][64], sacc[4][64];
+    o1_chain_wait();
     const int rh = blockIdx.x, r = rh / a.nh, gh = rh - r * a.nh, g = gh / a.hpg;
     const int q = r * a.hpg + (gh - g * a.hpg);
     const int tid = threadIdx.x, sg = tid >> 6, col = tid & 63, t = blockIdx.y * 64 + col;
@@ -1509,6 +1521,7 @@ __global__ __launch_bounds__(256) void k_merge(O1Args a) {
 // (an atomic ticket, no waiting), every group's meta after R pushes
 // (o1b_meta) and the position.
 __global__ __launch_bounds__(256) void k_commit(O1Args a) {
+    o1_chain_wait();   // ends a pass: releases nothing early
     const int g = blockIdx.y;
     const O1Meta mt = o1_meta(a, g);
     const int rstart = max(0, a.R - mt.wg);
@@ -1673,18 +1686,24 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     begin(1, sf);
     const size_t fbs = far_block_smem_floats() * sizeof(float);
     if (!a.exact && !short_far) {   // the comparator has no far field
-        if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
+        if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);   // behind the fork: plain
         else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, sf>>>(a);
     }
     end(1, sf);
     begin(2, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
-    if (!a.exact && !short_far) k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, sf>>>(a);
+    if (!a.exact && !short_far) o1_launch_chained(k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, sf, a);
     end(2, sf);
     begin(3, sf);
-    if (short_far) k_side_short<<<dim3(a.nh, short_col_splits(a)), 256, sfs, sf>>>(a);
-    else if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
-    else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+    if (short_far) k_side_short<<<dim3(a.nh, short_col_splits(a)), 256, sfs, sf>>>(a);   // behind the fork: plain
+    else if (a.exact) {   // the far branch's first kernel: plain
+        if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+        else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
+    } else if (a.dv <= 128) {
+        o1_launch_chained(k_side_readout<1>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
+    } else {
+        o1_launch_chained(k_side_readout<2>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
+    }
     end(3, sf);
     cudaEventRecord(aux->join, sf);
     begin(4, st);
@@ -1694,15 +1713,15 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     if (e == cudaSuccess) {
         if (KS) {
             const int nsl = (a.w + R - 1 + KS - 1) / KS;
-            k_near_small<<<dim3(nsl, a.G), 256, near_small_smem(a, KS), st>>>(a, KS);
-            k_near_small_merge<<<dim3(R * a.nh, (a.dv + 63) / 64), 256, 0, st>>>(a, nsl);
+            o1_launch_chained(k_near_small, dim3(nsl, a.G), dim3(256), near_small_smem(a, KS), st, a, KS);
+            o1_launch_chained(k_near_small_merge, dim3(R * a.nh, (a.dv + 63) / 64), dim3(256), 0, st, a, nsl);
         } else if (a.tc) {
             e = o1_launch_near_tc(a, st);
         } else {
             const int RB = 32 / a.hpg;
             const dim3 gn((R + RB - 1) / RB, a.G);
-            if (a.dv <= 128) k_near<1><<<gn, 256, near_smem(a), st>>>(a);
-            else k_near<2><<<gn, 256, near_smem(a), st>>>(a);
+            if (a.dv <= 128) o1_launch_chained(k_near<1>, gn, dim3(256), near_smem(a), st, a);
+            else o1_launch_chained(k_near<2>, gn, dim3(256), near_smem(a), st, a);
         }
     }
     end(5, st);
@@ -1715,7 +1734,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     end(6, st);
     begin(7, st);
     const int live = R < a.w ? R : a.w;
-    if (a.commit) k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
+    if (a.commit) o1_launch_chained(k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
     end(7, st);
     return cudaGetLastError();
 }
@@ -1728,21 +1747,23 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     chunk_attrs();
     const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
-    k_rope<<<R, 128, 0, st>>>(a);
     O1Args as = a;
     as.short_no_readout = 1;
     const size_t sfs = short_smem_floats(as) * sizeof(float);
-    if (R <= O1_SHORT_ROWS && sfs <= 227 * 1024) {
-        k_side_short<<<dim3(a.nh, short_col_splits(as)), 256, sfs, st>>>(as);   // the far inserts of a short commit
+    const bool short_far = R <= O1_SHORT_ROWS && sfs <= 227 * 1024;
+    as.chain_early = short_far;   // rotation -> far inserts -> ring, each scheduled under the previous one's end
+    k_rope<<<R, 128, 0, st>>>(as);
+    if (short_far) {
+        o1_launch_chained(k_side_short, dim3(a.nh, short_col_splits(as)), dim3(256), sfs, st, as);   // the far inserts of a short commit
     } else {
         const size_t fbs = far_block_smem_floats() * sizeof(float);
-        if (a.dv <= 128) k_far_block<1><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
-        else k_far_block<2><<<dim3(nblk, a.nh), 256, fbs, st>>>(a);
+        if (a.dv <= 128) o1_launch_chained(k_far_block<1>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
+        else o1_launch_chained(k_far_block<2>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
         const size_t n = (size_t)a.nh * a.m * a.dv;
-        k_far_tscan<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+        o1_launch_chained(k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, a);
     }
     const int live = R < a.w ? R : a.w;
-    k_commit<<<dim3((live + 3) / 4, a.G), 64, 0, st>>>(a);
+    o1_launch_chained(k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
     return cudaGetLastError();
 }
 

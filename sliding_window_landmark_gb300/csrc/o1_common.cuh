@@ -325,6 +325,7 @@ struct O1Args {
     int commit;   // 0: attend only, the state is left as it was (speculative verify)
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     int short_no_readout;   // short far pass of a commit: inserts only, no side parts
+    int chain_early;        // the pass's chained kernels may be scheduled before their predecessor ends
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;   // the row stride of E and P (a multiple of 4)
@@ -533,6 +534,37 @@ static inline bool o1_attrs_needed(const unsigned long long *mask, unsigned long
 }
 static inline void o1_attrs_done(unsigned long long *mask, unsigned long long bit) {
     __atomic_fetch_or(mask, bit, __ATOMIC_RELEASE);
+}
+
+// Chained launches (programmatic dependent launch). A kernel launched by
+// o1_launch_chained may be scheduled while the previous kernel of its stream
+// is still running, so it calls o1_chain_wait() before it touches global
+// memory; the wait returns once that kernel has completed and its writes are
+// visible. Since every chained kernel waits, a chain completes in order. The
+// first kernel of a pass on a stream, and every kernel behind an event wait,
+// is launched plainly. o1_chain_release() lets the next chained kernel be
+// scheduled before this one ends; the kernels that can end a pass never call
+// it, because a one-row step launched after them reads the state ahead of
+// its own wait. Only short commit passes release (O1Args::chain_early): in a
+// prompt-sized pass, dependents scheduled early hold SMs that the other
+// stream's kernels would use.
+__device__ __forceinline__ void o1_chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void o1_chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... P, typename... A>
+static inline void o1_launch_chained(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     A... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 // Launchers (o1_chunk.cu). Each returns cudaGetLastError() after its launches.

@@ -227,6 +227,7 @@ __device__ __forceinline__ TcPlan tc_plan(const O1Args &a) {
 __global__ __launch_bounds__(256) void k_gather_tc(O1Args a, unsigned short *Xk, unsigned short *XvT, int NXp) {
     __shared__ uint32_t sv[32][O1_MAX_DV / 2 + 1];   // [key][t pair]: hi | lo << 16 per element, two passes
     __shared__ unsigned short svl[32][O1_MAX_DV + 2];
+    o1_chain_wait();
     const int g = blockIdx.y, x0 = blockIdx.x * 32;
     const O1Meta mt = o1_meta(a, g);
     const int NX = mt.len0 + a.R;
@@ -332,6 +333,9 @@ __global__ __launch_bounds__(TC_THREADS, 1) void k_near_tc(O1Args a, const __gri
     tc_before();
     __syncthreads();
     tc_after();
+    // the set-up above overlaps the gather's end; the meta read by tc_plan is
+    // written only by the pass's commit, after this kernel
+    o1_chain_wait();
     const uint32_t tmem = *tslot;
     const long long wl = a.wait_cycles;   // limit of every wait but the final drains
     int issued = 0;                      // ring items the producer has issued (its lane 0)
@@ -660,7 +664,7 @@ size_t tc_smem(int d, int *nslot) {
 }  // namespace
 
 cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st) {
-    k_gather_tc<<<dim3((a.nxp + 31) / 32, a.G), 256, 0, st>>>(a, a.Xk, a.XvT, a.nxp);
+    o1_launch_chained(k_gather_tc, dim3((a.nxp + 31) / 32, a.G), dim3(256), 0, st, a, a.Xk, a.XvT, a.nxp);
     return cudaGetLastError();
 }
 
@@ -693,6 +697,7 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
             return cudaErrorInvalidValue;
     }
     const int S = a.wsplit > 1 ? a.wsplit : 1;
-    k_near_tc<<<dim3((a.R + TC_BM - 1) / TC_BM, a.nh, S), TC_THREADS, smem, st>>>(a, mk, mv, mq, NXp, nslot);
+    o1_launch_chained(k_near_tc, dim3((a.R + TC_BM - 1) / TC_BM, a.nh, S), dim3(TC_THREADS), smem, st, a, mk, mv, mq,
+                      NXp, nslot);
     return cudaGetLastError();
 }

@@ -815,231 +815,320 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // ---------------------------------------------------------- short passes
 
 // A pass of at most O1_SHORT_ROWS rows: the far field and the sinks of head
-// blockIdx.x in one CTA, row after row as the oracle takes them, in place
-// of the 64-row block kernels (k_far_block, k_far_tscan, k_side_readout).
-// Per row: the insert of the key it evicts (o1b_far_e / o1b_far_commit for
-// one key: l_b = scale qt_b . k_e, M' = max(M, l_b), rho, e, Z in
-// float-float, T = rho T + e v_e), then its readout (o1b_attend's far and
-// sink parts): f_a = scale q'.kt_a, F, u_b = sum_a e^{f_a - F} mu[a][b]
-// (rect), c_f = max_b (F + M_b), gains, D = sum_b gain_b Z_b in float-float
-// and the sign decision, numerator sum_b gain_b T_b; sink scores; all under
-// c_s = max(sink max, c_f) into the side header (c_s, side mass) and side
-// numerator, as k_side_readout leaves them. A commit pass
-// (short_no_readout) only inserts. The far state is written back when the
-// pass commits. The value columns are split over gridDim.y CTAs a head
-// (short_col_splits, up to 4; 8 measured slower): each repeats the scalars
-// (dots, F, u, gains, D) and takes one slice of T, of the numerators and of
+// blockIdx.x in one CTA, in place of the 64-row block kernels (k_far_block,
+// k_far_tscan, k_side_readout). The rows are taken as the oracle takes them
+// (row r first inserts the key it evicts, o1b_far_e / o1b_far_commit for one
+// key, then reads out, o1b_attend's far and sink parts), but only the
+// recurrence itself runs row after row:
+//   1. every dot product of the pass at once: the insert logits
+//      l_rb = scale qt_b . k_e(r), the far scores f_ra = scale q'_r . kt_a and
+//      the sink scores (a warp per row vector and 8 targets);
+//   2. per row, F_r = max_a f_ra, e^{f_ra - F_r} and u_rb = sum_a e^{f_ra - F_r}
+//      mu[a][b] (rect), a warp per row;
+//   3. one warp runs the recurrence over the rows with M and Z (float-float)
+//      in its registers, two landmarks a lane: M' = max(M, l), rho, e,
+//      Z = rho Z + e; then c_f = max_b (F + M_b), the gains u_b e^{F+M_b-c_f},
+//      D = sum_b gain_b Z_b and its sign, c_s = max(sink max, c_f), the sink
+//      weights and the side header (c_s, side mass);
+//   4. the value sums T = rho T + e v_e and the side numerator
+//      e^{c_f-c_s} sum_b gain_b T_b + sum_x w_x v_x, row after row with no
+//      barrier: each thread owns the entries of T of one value column and
+//      every P-th landmark, and P neighbouring lanes sum a column's parts
+//      by shuffles.
+// A commit pass (short_no_readout) only inserts. The far state is written
+// back when the pass commits. The value columns are split over gridDim.y
+// CTAs a head (short_col_splits, up to 4; 8 measured slower): each repeats
+// the scalars (steps 1-3) and takes one slice of T, of the numerators and of
 // the evicted and sink values.
 __host__ __device__ inline int short_col_splits(const O1Args &a) {
     for (int cs = 4; cs > 1; cs >>= 1)
         if (a.nh * cs <= 148 && a.dv % (4 * cs) == 0) return cs;
     return 1;
 }
-__host__ __device__ inline size_t short_smem_floats(const O1Args &a) {
-    const size_t m = a.m, d = a.d, dvs = a.dv / short_col_splits(a), ns = a.ns, R = a.R;
-    return 2 * m * d + (m * m + 3) / 4 * 4 + m * dvs + ns * (d + dvs) + R * (2 * d + dvs) + 3 * 64 + 5 * 64 + dvs +
-           16 + 256;
+
+// Shared memory of k_side_short, in floats; every part starts on 16 bytes.
+struct ShortLayout {
+    int dvs;   // value columns of this CTA
+    int P;     // threads per value column in step 4 (a power of two, at most 32)
+    int ldT;   // row stride of T: P lanes on P landmarks of one column hit P different banks
+    size_t skt, sqt, smu, sT, ssk, ssv, sKe, sVe, sQ, sL, sF, sU, sRho, sE, sS, sRow, total;
+};
+__host__ __device__ inline size_t short_up4(size_t x) { return (x + 3) / 4 * 4; }
+__host__ __device__ inline ShortLayout short_layout(const O1Args &a) {
+    ShortLayout L;
+    L.dvs = a.dv / short_col_splits(a);
+    L.P = 1;
+    while (L.P < 32 && 2 * L.P * L.dvs <= 256) L.P *= 2;
+    const int off = L.P >= 8 ? 4 : 32 / L.P;   // stride = off (mod 32), a multiple of 4
+    L.ldT = L.dvs + ((off - L.dvs) % 32 + 32) % 32;
+    const size_t m = a.m, d = a.d, dvs = L.dvs, ns = a.ns, R = a.R;
+    size_t o = 0;
+    L.skt = o;  o += m * d;                // [m][d]   landmark keys of the group
+    L.sqt = o;  o += m * d;                // [m][d]   landmark queries of the head
+    L.smu = o;  o += short_up4(m * m);     // [m][m]
+    L.sT = o;   o += m * L.ldT;            // [m][ldT] far value sums (this slice)
+    L.ssk = o;  o += ns * d;               // [ns][d]
+    L.ssv = o;  o += ns * dvs;             // [ns][dvs]
+    L.sKe = o;  o += R * d;                // [R][d]   the key each row evicts
+    L.sVe = o;  o += R * dvs;              // [R][dvs] and its value
+    L.sQ = o;   o += R * d;                // [R][d]   the rows' rotated queries
+    L.sL = o;   o += short_up4(R * m);     // [R][m]   insert logits
+    L.sF = o;   o += short_up4(R * m);     // [R][m]   far scores, then e^{f - F}
+    L.sU = o;   o += short_up4(R * m);     // [R][m]   u, then the gains
+    L.sRho = o; o += short_up4(R * m);     // [R][m]   the inserts' rescales
+    L.sE = o;   o += short_up4(R * m);     //          and weights
+    L.sS = o;   o += short_up4(R * ns);    // [R][ns]  sink scores, then weights
+    L.sRow = o; o += 4 * R;                // [R][4]   F, e^{c_f - c_s} (0: no far part)
+    L.total = o;
+    return L;
 }
+__host__ __device__ inline size_t short_smem_floats(const O1Args &a) { return short_layout(a).total; }
 
 __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     extern __shared__ __align__(16) float sm[];
     o1_chain_wait();
     if (a.chain_early) o1_chain_release();
+    const ShortLayout L = short_layout(a);
     const int h = blockIdx.x, g = h / a.hpg, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = a.m, d = a.d, ns = a.ns, R = a.R, nh = a.nh;
-    const int dvf = a.dv, dv = dvf / (int)gridDim.y, c0 = blockIdx.y * dv;   // this CTA's value columns
-    const bool lead = blockIdx.y == 0;                                       // writes the scalars' results
+    const int dvf = a.dv, dv = L.dvs, c0 = blockIdx.y * dv;   // this CTA's value columns
+    const bool lead = blockIdx.y == 0;                        // writes the scalars' results
     const O1Meta mt = o1_meta(a, g);
     const int j0 = mt.wg - mt.len0;   // row r evicts X[r - j0] once r >= j0
     const bool far_on = !a.exact, readout = !a.short_no_readout;
-    float *skt = sm;                                  // [m][d]   landmark keys of the group
-    float *sqt = skt + (size_t)m * d;                 // [m][d]   landmark queries of the head
-    float *smu = sqt + (size_t)m * d;                 // [m][m]
-    float *sT = smu + (size_t)(m * m + 3) / 4 * 4;    // [m][dv]  far value sums (this slice), 16-byte aligned
-    float *ssk = sT + (size_t)m * dv;                 // [ns][d]
-    float *ssv = ssk + (size_t)ns * d;                // [ns][dv]
-    float *sKe = ssv + (size_t)ns * dv;               // [R][d]   the key each row evicts
-    float *sVe = sKe + (size_t)R * d;                 // [R][dv]  and its value
-    float *sQ = sVe + (size_t)R * dv;                 // [R][d]   the rows' rotated queries
-    float *sM = sQ + (size_t)R * d;                   // [64]
-    float *sZh = sM + 64, *sZl = sZh + 64;            // [64]     far mass, high and low parts
-    float *sL = sZl + 64;                             // [64]     l_b, then f_a
-    float *sS = sL + 64;                              // [64]     sink scores
-    float *sU = sS + 64;                              // [64]     u_b, then gains
-    float *sRho = sU + 64, *sE = sRho + 64;           // [64]     the insert's rescale and weight
-    float *sNum = sE + 64;                            // [dv]     far numerator
-    float *sc = sNum + dv;                            // scalars: F, c_f, D hi, D lo, have
-    float *sUp = sc + 16;                             // [256] partial u_b
+    float *skt = sm + L.skt, *sqt = sm + L.sqt, *smu = sm + L.smu, *sT = sm + L.sT;
+    float *ssk = sm + L.ssk, *ssv = sm + L.ssv, *sKe = sm + L.sKe, *sVe = sm + L.sVe, *sQ = sm + L.sQ;
+    float *sL = sm + L.sL, *sF = sm + L.sF, *sU = sm + L.sU, *sRho = sm + L.sRho, *sE = sm + L.sE;
+    float *sS = sm + L.sS, *sRow = sm + L.sRow;
+    auto farl_of = [&](int r) { return far_on ? mt.farl0 + max(0, r - j0 + 1) : 0; };
 
     // the head's operands and state, and every row's evicted pair and query:
     // 16-byte asynchronous copies, all in flight together (rows of d and dv
-    // floats are 16-byte multiples; zero-filled where there is nothing)
+    // floats are 16-byte multiples)
     const int d4 = d >> 2, dv4 = dv >> 2;
-    for (int i = tid; i < m * d4; i += 256) {   // (a commit pass reads out nothing: no landmark keys)
-        cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, far_on && readout);
-        cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, far_on);
+    if (far_on) {
+        for (int i = tid; i < m * d4; i += 256) {
+            if (readout) cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, true);
+            cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, true);
+        }
+        for (int i = tid; i < m * dv4; i += 256) {
+            const int b = i / dv4, j = i - b * dv4;
+            cp_async16(sT + (size_t)b * L.ldT + 4 * j, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, true);
+        }
+        for (int i = tid; i < R * d4; i += 256) {
+            const int r = i / d4, j = i - r * d4;
+            if (r >= j0) cp_async16(sKe + 4 * i, o1_key(a, g, r - j0, mt) + 4 * j, true);
+        }
+        for (int i = tid; i < R * dv4; i += 256) {
+            const int r = i / dv4, j = i - r * dv4;
+            if (r >= j0) cp_async16(sVe + 4 * i, o1_val(a, g, r - j0, mt) + c0 + 4 * j, true);
+        }
     }
-    for (int i = tid; i < m * dv4; i += 256) {
-        const int b = i / dv4, j = i - b * dv4;
-        cp_async16(sT + 4 * i, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, far_on);
-    }
-    for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, readout);
-    for (int i = tid; i < ns * dv4; i += 256) {
-        const int x = i / dv4, j = i - x * dv4;
-        cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, readout);
-    }
-    for (int i = tid; i < R * d4; i += 256) {
-        const int r = i / d4, j = i - r * d4;
-        const bool ev = far_on && r >= j0;
-        cp_async16(sKe + 4 * i, ev ? o1_key(a, g, r - j0, mt) + 4 * j : a.kt, ev);
-        cp_async16(sQ + 4 * i, readout ? a.qr + ((size_t)r * nh + h) * d + 4 * j : a.kt, readout);
-    }
-    for (int i = tid; i < R * dv4; i += 256) {
-        const int r = i / dv4, j = i - r * dv4;
-        const bool ev = far_on && r >= j0;
-        cp_async16(sVe + 4 * i, ev ? o1_val(a, g, r - j0, mt) + c0 + 4 * j : a.kt, ev);
+    if (readout) {
+        for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, true);
+        for (int i = tid; i < ns * dv4; i += 256) {
+            const int x = i / dv4, j = i - x * dv4;
+            cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, true);
+        }
+        for (int i = tid; i < R * d4; i += 256) {
+            const int r = i / d4, j = i - r * d4;
+            cp_async16(sQ + 4 * i, a.qr + ((size_t)r * nh + h) * d + 4 * j, true);
+        }
+        if (far_on)
+            for (int i = tid; i < m * m; i += 256) smu[i] = a.mu[(size_t)h * m * m + i];
     }
     cp_async_commit();
-    for (int i = tid; i < m * m; i += 256) smu[i] = (far_on && readout) ? a.mu[(size_t)h * m * m + i] : 0.f;
-    for (int b = tid; b < m; b += 256) {
-        sM[b] = far_on ? a.M[(size_t)h * m + b] : -INFINITY;
-        sZh[b] = far_on ? a.Z[(size_t)h * m + b] : 0.f;
-        sZl[b] = far_on ? a.Zlo[(size_t)h * m + b] : 0.f;
-    }
     cp_async_wait<0>();
     __syncthreads();
-    // a warp per row of `rows` ([n][ld]), lanes across d: scale x . row -> out
-    auto dots = [&](const float *rows, int n, const float *x, float *out) {
-        float xr[O1_MAX_D / 32];
+
+    // 1. dot products: task (row, kind, 8 targets); a warp holds the row
+    //    vector in registers, lanes across d
+    {
+        const int nc0 = (m + 7) / 8, nc2 = (ns + 7) / 8, per = 2 * nc0 + nc2;
+        for (int i = warp; i < R * per; i += 8) {
+            const int r = i / per, k = i - r * per;
+            const float *x, *rows;
+            float *out;
+            int n0, n;
+            if (k < nc0) {   // the insert logits of the key row r evicts
+                if (!far_on || r < j0) continue;
+                x = sKe + (size_t)r * d, rows = sqt, out = sL + (size_t)r * m, n0 = 8 * k, n = m;
+            } else if (k < 2 * nc0) {   // row r's far scores
+                if (!readout || farl_of(r) <= 0) continue;
+                x = sQ + (size_t)r * d, rows = skt, out = sF + (size_t)r * m, n0 = 8 * (k - nc0), n = m;
+            } else {   // row r's sink scores
+                if (!readout) continue;
+                x = sQ + (size_t)r * d, rows = ssk, out = sS + (size_t)r * ns, n0 = 8 * (k - 2 * nc0), n = ns;
+            }
+            float4 xr[2];
 #pragma unroll
-        for (int t = 0; t < O1_MAX_D / 32; ++t) xr[t] = lane + 32 * t < d ? x[lane + 32 * t] : 0.f;
-        for (int i = warp; i < n; i += 8) {
-            const float *rw = rows + (size_t)i * d;
-            float acc = 0.f;
+            for (int u = 0; u < 2; ++u)
+                xr[u] = lane + 32 * u < d4 ? ((const float4 *)x)[lane + 32 * u] : make_float4(0.f, 0.f, 0.f, 0.f);
+            float p[8];
 #pragma unroll
-            for (int t = 0; t < O1_MAX_D / 32; ++t)
-                if (lane + 32 * t < d) acc = fmaf(xr[t], rw[lane + 32 * t], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) out[i] = a.scale * acc;
+            for (int j = 0; j < 8; ++j) {
+                p[j] = 0.f;
+                if (n0 + j < n) {
+                    const float4 *rw = (const float4 *)(rows + (size_t)(n0 + j) * d);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (lane + 32 * u < d4) {
+                            const float4 y = rw[lane + 32 * u];
+                            p[j] = fmaf(xr[u].x, y.x, p[j]);
+                            p[j] = fmaf(xr[u].y, y.y, p[j]);
+                            p[j] = fmaf(xr[u].z, y.z, p[j]);
+                            p[j] = fmaf(xr[u].w, y.w, p[j]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) p[j] += __shfl_xor_sync(0xffffffffu, p[j], o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (lane == j && n0 + j < n) out[n0 + j] = a.scale * p[j];
         }
-    };
+    }
+    __syncthreads();
+
+    // 2. per row with a far field: F, e^{f - F} in place, u (rect)
+    if (readout && far_on) {
+        for (int r = warp; r < R; r += 8) {
+            if (farl_of(r) <= 0) continue;
+            float *f = sF + (size_t)r * m;
+            const float f0 = lane < m ? f[lane] : -INFINITY, f1 = lane + 32 < m ? f[lane + 32] : -INFINITY;
+            const float F = warp_max(fmaxf(f0, f1));
+            if (lane < m) f[lane] = expf(f0 - F);
+            if (lane + 32 < m) f[lane + 32] = expf(f1 - F);
+            if (lane == 0) sRow[4 * r] = F;
+            __syncwarp();
+            for (int b = lane; b < m; b += 32) {
+                float u0 = 0.f, u1 = 0.f;
+                int aa = 0;
+                for (; aa + 1 < m; aa += 2) {
+                    u0 = fmaf(f[aa], smu[aa * m + b], u0);
+                    u1 = fmaf(f[aa + 1], smu[(aa + 1) * m + b], u1);
+                }
+                if (aa < m) u0 = fmaf(f[aa], smu[aa * m + b], u0);
+                float u = u0 + u1;
+                if (a.rect) u = fmaxf(u, 0.f);
+                sU[(size_t)r * m + b] = u;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 3. the recurrence over the rows, one warp: landmarks b = lane, lane + 32
+    if (warp == 0) {
+        float Mr[2];
+        o1_ff Zr[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int b = lane + 32 * k;
+            const bool in = far_on && b < m;
+            Mr[k] = in ? a.M[(size_t)h * m + b] : -INFINITY;
+            Zr[k] = in ? ff_make(a.Z[(size_t)h * m + b], a.Zlo[(size_t)h * m + b]) : ff_make(0.f, 0.f);
+        }
+        for (int r = 0; r < R; ++r) {
+            if (far_on && r >= j0) {   // insert the evicted key
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int b = lane + 32 * k;
+                    if (b < m) {
+                        const float l = sL[(size_t)r * m + b], Mo = Mr[k];
+                        const float Mn = fmaxf(Mo, l);
+                        const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
+                        const float e = expf(l - Mn);
+                        Zr[k] = ff_add_f(ff_mul_f(Zr[k], rho), e);
+                        Mr[k] = Mn;
+                        sRho[(size_t)r * m + b] = rho;
+                        sE[(size_t)r * m + b] = e;
+                    }
+                }
+            }
+            if (!readout) continue;
+            float cf = -INFINITY;
+            bool have = false;
+            o1_ff D = ff_make(0.f, 0.f);
+            if (farl_of(r) > 0) {
+                const float F = sRow[4 * r];
+                float c = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (lane + 32 * k < m) c = fmaxf(c, F + Mr[k]);
+                cf = warp_max(c);
+                o1_ff Dp = ff_make(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int b = lane + 32 * k;
+                    if (b < m) {
+                        const float gn = sU[(size_t)r * m + b] * expf(F + Mr[k] - cf);
+                        sU[(size_t)r * m + b] = gn;
+                        Dp = ff_add(Dp, ff_mul_f(Zr[k], gn));
+                    }
+                }
+                D = warp_sum(Dp);
+                have = ff_nonneg(D);
+            }
+            // c_s = max(sink max, c_f); the sink weights, the side mass
+            const float s0 = lane < ns ? sS[(size_t)r * ns + lane] : -INFINITY;
+            const float s1 = lane + 32 < ns ? sS[(size_t)r * ns + lane + 32] : -INFINITY;
+            const float cs = fmaxf(warp_max(fmaxf(s0, s1)), cf);
+            const float fs = have ? expf(cf - cs) : 0.f;
+            const float w0 = lane < ns ? expf(s0 - cs) : 0.f, w1 = lane + 32 < ns ? expf(s1 - cs) : 0.f;
+            if (lane < ns) sS[(size_t)r * ns + lane] = w0;
+            if (lane + 32 < ns) sS[(size_t)r * ns + lane + 32] = w1;
+            const float side = (have ? fs * (D.hi + D.lo) : 0.f) + warp_sum(w0 + w1);
+            if (lane == 0) {
+                sRow[4 * r + 1] = fs;
+                if (lead)
+                    *(float4 *)(a.sh + ((size_t)r * nh + h) * 4) =
+                        make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
+            }
+        }
+        if (a.commit && far_on && lead) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int b = lane + 32 * k;
+                if (b < m) {
+                    a.M[(size_t)h * m + b] = Mr[k];
+                    a.Z[(size_t)h * m + b] = Zr[k].hi;
+                    a.Zlo[(size_t)h * m + b] = Zr[k].lo;
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // 4. value sums and side numerators, row after row: thread (t, pi) owns
+    //    T[b][t] for b = pi, pi + P, ...
+    const int P = L.P, t = tid / P, pi = tid - t * P;
+    const bool act = t < dv;
+    float *Tt = sT + (act ? t : 0);
     for (int r = 0; r < R; ++r) {
-        const bool evict = far_on && r >= j0;
-        const int farl = far_on ? mt.farl0 + max(0, r - j0 + 1) : 0;
-        if (evict) {
-            // the insert of the evicted key into every landmark of the head
-            dots(sqt, m, sKe + (size_t)r * d, sL);
-            __syncthreads();
-            if (tid < m) {
-                const float l = sL[tid], Mo = sM[tid];
-                const float Mn = fmaxf(Mo, l);
-                const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
-                const float e = expf(l - Mn);
-                const o1_ff Zn = ff_add_f(ff_mul_f(ff_make(sZh[tid], sZl[tid]), rho), e);
-                sM[tid] = Mn;
-                sZh[tid] = Zn.hi;
-                sZl[tid] = Zn.lo;
-                sRho[tid] = rho;
-                sE[tid] = e;
-            }
-            __syncthreads();
-            const float *ve = sVe + (size_t)r * dv;
-            for (int i = tid; i < m * dv; i += 256) {
-                const int b = i / dv, t = i - b * dv;
-                sT[i] = sRho[b] * sT[i] + sE[b] * ve[t];
-            }
-            __syncthreads();
+        if (act && far_on && r >= j0) {
+            const float ve = sVe[(size_t)r * dv + t];
+            const float *rho = sRho + (size_t)r * m, *e = sE + (size_t)r * m;
+            for (int b = pi; b < m; b += P) Tt[(size_t)b * L.ldT] = fmaf(rho[b], Tt[(size_t)b * L.ldT], e[b] * ve);
         }
         if (!readout) continue;
-        const float *q = sQ + (size_t)r * d;
-        // far readout of row r
-        if (farl > 0) {
-            dots(skt, m, q, sL);
-            __syncthreads();
-            if (warp == 0) {
-                const float f0 = lane < m ? sL[lane] : -INFINITY, f1 = lane + 32 < m ? sL[lane + 32] : -INFINITY;
-                const float F = warp_max(fmaxf(f0, f1));
-                if (lane < m) sL[lane] = expf(f0 - F);
-                if (lane + 32 < m) sL[lane + 32] = expf(f1 - F);
-                const float c0 = lane < m ? F + sM[lane] : -INFINITY, c1 = lane + 32 < m ? F + sM[lane + 32] : -INFINITY;
-                const float cf = warp_max(fmaxf(c0, c1));
-                if (lane == 0) {
-                    sc[0] = F;
-                    sc[1] = cf;
-                }
+        const float fs = sRow[4 * r + 1];
+        float acc = 0.f;
+        if (act) {
+            if (fs != 0.f) {
+                const float *gn = sU + (size_t)r * m;
+                for (int b = pi; b < m; b += P) acc = fmaf(gn[b], Tt[(size_t)b * L.ldT], acc);
+                acc *= fs;
             }
-            __syncthreads();
-            {   // u_b: every thread a share of the landmark keys a for one b
-                const int parts = 256 / m, b = tid % m, pi = tid / m;
-                float u = 0.f;
-                if (pi < parts)
-                    for (int aa = pi; aa < m; aa += parts) u = fmaf(sL[aa], smu[aa * m + b], u);
-                sUp[tid] = u;
-            }
-            __syncthreads();
-            if (tid < m) {   // u_b, then the gain (u_b relative to c_f)
-                float u = 0.f;
-                for (int pi = 0; pi < 256 / m; ++pi) u += sUp[pi * m + tid];
-                if (a.rect) u = fmaxf(u, 0.f);
-                sU[tid] = u * expf(sc[0] + sM[tid] - sc[1]);
-            }
-            __syncthreads();
-            if (warp == 0) {
-                o1_ff D = ff_make(0.f, 0.f);
-                for (int b = lane; b < m; b += 32) D = ff_add(D, ff_mul_f(ff_make(sZh[b], sZl[b]), sU[b]));
-                D = warp_sum(D);
-                if (lane == 0) {
-                    sc[2] = D.hi;
-                    sc[3] = D.lo;
-                    sc[4] = ff_nonneg(D) ? 1.f : 0.f;
-                }
-            }
-            {   // numerator: every thread a share of the landmarks for one column
-                const int parts = 256 / dv, t = tid % dv, pi = tid / dv;
-                float acc = 0.f;
-                if (pi < parts)
-                    for (int b = pi; b < m; b += parts) acc = fmaf(sU[b], sT[(size_t)b * dv + t], acc);
-                sUp[tid] = acc;
-            }
-            __syncthreads();
-            for (int t = tid; t < dv; t += 256) {
-                float acc = 0.f;
-                for (int pi = 0; pi < 256 / dv; ++pi) acc += sUp[pi * dv + t];
-                sNum[t] = acc;
-            }
+            const float *w = sS + (size_t)r * ns;
+            for (int x = pi; x < ns; x += P) acc = fmaf(w[x], ssv[(size_t)x * dv + t], acc);
         }
-        // the row's sink scores
-        dots(ssk, ns, q, sS);
-        __syncthreads();
-        // c_s = max(sink max, c_f); sink weights, side mass and numerator
-        const bool have = farl > 0 && sc[4] > 0.5f;
-        float smax = -INFINITY;
-        for (int x = 0; x < ns; ++x) smax = fmaxf(smax, sS[x]);
-        const float cf = farl > 0 ? sc[1] : -INFINITY;
-        const float cs = fmaxf(smax, cf);
-        const float fs = have ? expf(cf - cs) : 0.f;
-        float side = have ? fs * (sc[2] + sc[3]) : 0.f;
-        for (int x = 0; x < ns; ++x) side += expf(sS[x] - cs);
-        for (int t = tid; t < dv; t += 256) {
-            float acc = have ? fs * sNum[t] : 0.f;
-            for (int x = 0; x < ns; ++x) acc = fmaf(expf(sS[x] - cs), ssv[(size_t)x * dv + t], acc);
-            a.sn[((size_t)r * nh + h) * dvf + c0 + t] = acc;
-        }
-        if (tid == 0 && lead)
-            *(float4 *)(a.sh + ((size_t)r * nh + h) * 4) = make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
-        __syncthreads();   // sL, sS, sU, sNum and the scalars are reused by the next row
+        for (int o = 1; o < P; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (act && pi == 0) a.sn[((size_t)r * nh + h) * dvf + c0 + t] = acc;
     }
-    if (!a.commit || !far_on) return;   // attend only: the state keeps its far field
-    for (int i = tid; i < m * dv; i += 256) {
-        const int b = i / dv, t = i - b * dv;
-        a.T[((size_t)h * m + b) * dvf + c0 + t] = sT[i];
-    }
-    if (!lead) return;
-    for (int b = tid; b < m; b += 256) {
-        a.M[(size_t)h * m + b] = sM[b];
-        a.Z[(size_t)h * m + b] = sZh[b];
-        a.Zlo[(size_t)h * m + b] = sZl[b];
-    }
+    if (a.commit && far_on && act)   // attend only: the state keeps its far field
+        for (int b = pi; b < m; b += P) a.T[((size_t)h * m + b) * dvf + c0 + t] = Tt[(size_t)b * L.ldT];
 }
 
 // ------------------------------------------------------------------ near

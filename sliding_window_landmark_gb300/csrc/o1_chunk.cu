@@ -819,17 +819,18 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // k_far_tscan, k_side_readout). The rows are taken as the oracle takes them
 // (row r first inserts the key it evicts, o1b_far_e / o1b_far_commit for one
 // key, then reads out, o1b_attend's far and sink parts), but only the
-// recurrence itself runs row after row:
+// recurrence of M and Z runs row after row:
 //   1. every dot product of the pass at once: the insert logits
 //      l_rb = scale qt_b . k_e(r), the far scores f_ra = scale q'_r . kt_a and
-//      the sink scores (a warp per row vector and 8 targets);
-//   2. per row, F_r = max_a f_ra, e^{f_ra - F_r} and u_rb = sum_a e^{f_ra - F_r}
-//      mu[a][b] (rect), a warp per row;
-//   3. one warp runs the recurrence over the rows with M and Z (float-float)
+//      the sink scores (a warp per 4 row vectors and 8 targets);
+//   2. one warp runs the recurrence over the rows with M and Z (float-float)
 //      in its registers, two landmarks a lane: M' = max(M, l), rho, e,
-//      Z = rho Z + e; then c_f = max_b (F + M_b), the gains u_b e^{F+M_b-c_f},
-//      D = sum_b gain_b Z_b and its sign, c_s = max(sink max, c_f), the sink
-//      weights and the side header (c_s, side mass);
+//      Z = rho Z + e, and keeps each row's M and Z; beside it, per row,
+//      F_r = max_a f_ra, e^{f_ra - F_r} and u_rb = sum_a e^{f_ra - F_r} mu[a][b]
+//      (rect);
+//   3. a warp per row: c_f = max_b (F + M_b), the gains u_b e^{F+M_b-c_f},
+//      D = sum_b gain_b Z_b in float-float and its sign, c_s = max(sink max,
+//      c_f), the sink weights and the side header (c_s, side mass);
 //   4. the value sums T = rho T + e v_e and the side numerator
 //      e^{c_f-c_s} sum_b gain_b T_b + sum_x w_x v_x, row after row with no
 //      barrier: each thread owns the entries of T of one value column and
@@ -851,7 +852,7 @@ struct ShortLayout {
     int dvs;   // value columns of this CTA
     int P;     // threads per value column in step 4 (a power of two, at most 32)
     int ldT;   // row stride of T: P lanes on P landmarks of one column hit P different banks
-    size_t skt, sqt, smu, sT, ssk, ssv, sKe, sVe, sQ, sL, sF, sU, sRho, sE, sS, sRow, total;
+    size_t skt, sqt, smu, sT, ssk, ssv, sKe, sVe, sQ, sL, sF, sU, sRho, sE, sMr, sZh, sZl, sS, sRow, total;
 };
 __host__ __device__ inline size_t short_up4(size_t x) { return (x + 3) / 4 * 4; }
 __host__ __device__ inline ShortLayout short_layout(const O1Args &a) {
@@ -877,6 +878,9 @@ __host__ __device__ inline ShortLayout short_layout(const O1Args &a) {
     L.sU = o;   o += short_up4(R * m);     // [R][m]   u, then the gains
     L.sRho = o; o += short_up4(R * m);     // [R][m]   the inserts' rescales
     L.sE = o;   o += short_up4(R * m);     //          and weights
+    L.sMr = o;  o += short_up4(R * m);     // [R][m]   M after each row's insert
+    L.sZh = o;  o += short_up4(R * m);     //          and Z, high
+    L.sZl = o;  o += short_up4(R * m);     //          and low part
     L.sS = o;   o += short_up4(R * ns);    // [R][ns]  sink scores, then weights
     L.sRow = o; o += 4 * R;                // [R][4]   F, e^{c_f - c_s} (0: no far part)
     L.total = o;
@@ -899,6 +903,7 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     float *skt = sm + L.skt, *sqt = sm + L.sqt, *smu = sm + L.smu, *sT = sm + L.sT;
     float *ssk = sm + L.ssk, *ssv = sm + L.ssv, *sKe = sm + L.sKe, *sVe = sm + L.sVe, *sQ = sm + L.sQ;
     float *sL = sm + L.sL, *sF = sm + L.sF, *sU = sm + L.sU, *sRho = sm + L.sRho, *sE = sm + L.sE;
+    float *sMr = sm + L.sMr, *sZh = sm + L.sZh, *sZl = sm + L.sZl;
     float *sS = sm + L.sS, *sRow = sm + L.sRow;
     auto farl_of = [&](int r) { return far_on ? mt.farl0 + max(0, r - j0 + 1) : 0; };
 
@@ -941,60 +946,114 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     cp_async_wait<0>();
     __syncthreads();
 
-    // 1. dot products: task (row, kind, 8 targets); a warp holds the row
-    //    vector in registers, lanes across d
+    // 1. dot products: task (kind, 4 rows, 8 targets); a warp holds the 4
+    //    row vectors in registers, lanes across d, and leaves the 32 dots
+    //    through one reduce-scatter (lane l: row l / 8, target l % 8)
     {
-        const int nc0 = (m + 7) / 8, nc2 = (ns + 7) / 8, per = 2 * nc0 + nc2;
-        for (int i = warp; i < R * per; i += 8) {
-            const int r = i / per, k = i - r * per;
+        const int nc0 = (m + 7) / 8, nc2 = (ns + 7) / 8, per = 2 * nc0 + nc2, nrg = (R + 3) / 4;
+        for (int i = warp; i < nrg * per; i += 8) {
+            const int rg = i / per, k = i - rg * per, r0 = 4 * rg, rl = min(R, r0 + 4) - 1;
             const float *x, *rows;
             float *out;
             int n0, n;
-            if (k < nc0) {   // the insert logits of the key row r evicts
-                if (!far_on || r < j0) continue;
-                x = sKe + (size_t)r * d, rows = sqt, out = sL + (size_t)r * m, n0 = 8 * k, n = m;
-            } else if (k < 2 * nc0) {   // row r's far scores
-                if (!readout || farl_of(r) <= 0) continue;
-                x = sQ + (size_t)r * d, rows = skt, out = sF + (size_t)r * m, n0 = 8 * (k - nc0), n = m;
-            } else {   // row r's sink scores
+            if (k < nc0) {   // the insert logits of the keys rows r0.. evict
+                if (!far_on || rl < j0) continue;
+                x = sKe, rows = sqt, out = sL, n0 = 8 * k, n = m;
+            } else if (k < 2 * nc0) {   // the far scores of rows r0..
+                if (!readout || farl_of(rl) <= 0) continue;
+                x = sQ, rows = skt, out = sF, n0 = 8 * (k - nc0), n = m;
+            } else {   // their sink scores
                 if (!readout) continue;
-                x = sQ + (size_t)r * d, rows = ssk, out = sS + (size_t)r * ns, n0 = 8 * (k - 2 * nc0), n = ns;
+                x = sQ, rows = ssk, out = sS, n0 = 8 * (k - 2 * nc0), n = ns;
             }
-            float4 xr[2];
+            float4 xr[4][2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
-                xr[u] = lane + 32 * u < d4 ? ((const float4 *)x)[lane + 32 * u] : make_float4(0.f, 0.f, 0.f, 0.f);
-            float p[8];
+            for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    xr[ri][u] = (r0 + ri < R && lane + 32 * u < d4)
+                                    ? ((const float4 *)(x + (size_t)(r0 + ri) * d))[lane + 32 * u]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            float p[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p[j] = 0.f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                p[j] = 0.f;
                 if (n0 + j < n) {
                     const float4 *rw = (const float4 *)(rows + (size_t)(n0 + j) * d);
 #pragma unroll
                     for (int u = 0; u < 2; ++u)
                         if (lane + 32 * u < d4) {
                             const float4 y = rw[lane + 32 * u];
-                            p[j] = fmaf(xr[u].x, y.x, p[j]);
-                            p[j] = fmaf(xr[u].y, y.y, p[j]);
-                            p[j] = fmaf(xr[u].z, y.z, p[j]);
-                            p[j] = fmaf(xr[u].w, y.w, p[j]);
+#pragma unroll
+                            for (int ri = 0; ri < 4; ++ri) {
+                                float &pp = p[8 * ri + j];
+                                pp = fmaf(xr[ri][u].x, y.x, pp);
+                                pp = fmaf(xr[ri][u].y, y.y, pp);
+                                pp = fmaf(xr[ri][u].z, y.z, pp);
+                                pp = fmaf(xr[ri][u].w, y.w, pp);
+                            }
                         }
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) p[j] += __shfl_xor_sync(0xffffffffu, p[j], o);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (lane == j && n0 + j < n) out[n0 + j] = a.scale * p[j];
+            warp_reduce_scatter32(p);
+            const int r = r0 + (lane >> 3), b = n0 + (lane & 7);
+            if (r < R && b < n) out[(size_t)r * n + b] = a.scale * p[0];
         }
     }
     __syncthreads();
 
-    // 2. per row with a far field: F, e^{f - F} in place, u (rect)
-    if (readout && far_on) {
-        for (int r = warp; r < R; r += 8) {
+    // 2. warp 0: the recurrence of M and Z (float-float) over the rows in its
+    //    registers, landmarks b = lane, lane + 32, each row's rescale and
+    //    weight kept for the value sums and its M, Z for its readout.
+    //    Warps 1..7 meanwhile, per row with a far field: F, e^{f - F} in
+    //    place, u (rect).
+    if (warp == 0) {
+        if (far_on) {
+            float Mr[2];
+            o1_ff Zr[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int b = lane + 32 * k;
+                Mr[k] = b < m ? a.M[(size_t)h * m + b] : -INFINITY;
+                Zr[k] = b < m ? ff_make(a.Z[(size_t)h * m + b], a.Zlo[(size_t)h * m + b]) : ff_make(0.f, 0.f);
+            }
+            for (int r = 0; r < R; ++r) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int b = lane + 32 * k;
+                    if (b >= m) continue;
+                    if (r >= j0) {   // insert the evicted key
+                        const float l = sL[(size_t)r * m + b], Mo = Mr[k];
+                        const float Mn = fmaxf(Mo, l);
+                        const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
+                        const float e = expf(l - Mn);
+                        Zr[k] = ff_add_f(ff_mul_f(Zr[k], rho), e);
+                        Mr[k] = Mn;
+                        sRho[(size_t)r * m + b] = rho;
+                        sE[(size_t)r * m + b] = e;
+                    }
+                    if (readout) {
+                        sMr[(size_t)r * m + b] = Mr[k];
+                        sZh[(size_t)r * m + b] = Zr[k].hi;
+                        sZl[(size_t)r * m + b] = Zr[k].lo;
+                    }
+                }
+            }
+            if (a.commit && lead) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int b = lane + 32 * k;
+                    if (b < m) {
+                        a.M[(size_t)h * m + b] = Mr[k];
+                        a.Z[(size_t)h * m + b] = Zr[k].hi;
+                        a.Zlo[(size_t)h * m + b] = Zr[k].lo;
+                    }
+                }
+            }
+        }
+    } else if (readout && far_on) {
+        for (int r = warp - 1; r < R; r += 7) {
             if (farl_of(r) <= 0) continue;
             float *f = sF + (size_t)r * m;
             const float f0 = lane < m ? f[lane] : -INFINITY, f1 = lane + 32 < m ? f[lane + 32] : -INFINITY;
@@ -1019,35 +1078,11 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     }
     __syncthreads();
 
-    // 3. the recurrence over the rows, one warp: landmarks b = lane, lane + 32
-    if (warp == 0) {
-        float Mr[2];
-        o1_ff Zr[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int b = lane + 32 * k;
-            const bool in = far_on && b < m;
-            Mr[k] = in ? a.M[(size_t)h * m + b] : -INFINITY;
-            Zr[k] = in ? ff_make(a.Z[(size_t)h * m + b], a.Zlo[(size_t)h * m + b]) : ff_make(0.f, 0.f);
-        }
-        for (int r = 0; r < R; ++r) {
-            if (far_on && r >= j0) {   // insert the evicted key
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int b = lane + 32 * k;
-                    if (b < m) {
-                        const float l = sL[(size_t)r * m + b], Mo = Mr[k];
-                        const float Mn = fmaxf(Mo, l);
-                        const float rho = (Mn == Mo) ? 1.f : expf(Mo - Mn);
-                        const float e = expf(l - Mn);
-                        Zr[k] = ff_add_f(ff_mul_f(Zr[k], rho), e);
-                        Mr[k] = Mn;
-                        sRho[(size_t)r * m + b] = rho;
-                        sE[(size_t)r * m + b] = e;
-                    }
-                }
-            }
-            if (!readout) continue;
+    // 3. each row's readout scalars, a warp per row: c_f = max_b (F + M_b),
+    //    the gains, D and its sign, c_s = max(sink max, c_f), the sink
+    //    weights, the side header (c_s, side mass)
+    if (readout) {
+        for (int r = warp; r < R; r += 8) {
             float cf = -INFINITY;
             bool have = false;
             o1_ff D = ff_make(0.f, 0.f);
@@ -1056,22 +1091,22 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
                 float c = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
-                    if (lane + 32 * k < m) c = fmaxf(c, F + Mr[k]);
+                    if (lane + 32 * k < m) c = fmaxf(c, F + sMr[(size_t)r * m + lane + 32 * k]);
                 cf = warp_max(c);
                 o1_ff Dp = ff_make(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int b = lane + 32 * k;
                     if (b < m) {
-                        const float gn = sU[(size_t)r * m + b] * expf(F + Mr[k] - cf);
-                        sU[(size_t)r * m + b] = gn;
-                        Dp = ff_add(Dp, ff_mul_f(Zr[k], gn));
+                        const size_t o = (size_t)r * m + b;
+                        const float gn = sU[o] * expf(F + sMr[o] - cf);
+                        sU[o] = gn;
+                        Dp = ff_add(Dp, ff_mul_f(ff_make(sZh[o], sZl[o]), gn));
                     }
                 }
                 D = warp_sum(Dp);
                 have = ff_nonneg(D);
             }
-            // c_s = max(sink max, c_f); the sink weights, the side mass
             const float s0 = lane < ns ? sS[(size_t)r * ns + lane] : -INFINITY;
             const float s1 = lane + 32 < ns ? sS[(size_t)r * ns + lane + 32] : -INFINITY;
             const float cs = fmaxf(warp_max(fmaxf(s0, s1)), cf);
@@ -1087,40 +1122,49 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
                         make_float4(cs, cs > -INFINITY ? side : 0.f, 0.f, 0.f);
             }
         }
-        if (a.commit && far_on && lead) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int b = lane + 32 * k;
-                if (b < m) {
-                    a.M[(size_t)h * m + b] = Mr[k];
-                    a.Z[(size_t)h * m + b] = Zr[k].hi;
-                    a.Zlo[(size_t)h * m + b] = Zr[k].lo;
-                }
-            }
-        }
     }
     __syncthreads();
 
     // 4. value sums and side numerators, row after row: thread (t, pi) owns
-    //    T[b][t] for b = pi, pi + P, ...
+    //    T[b][t] for b = pi, pi + P, ..., eight of them in registers at a time
     const int P = L.P, t = tid / P, pi = tid - t * P;
     const bool act = t < dv;
     float *Tt = sT + (act ? t : 0);
+    const int nb = act ? (m - pi + P - 1) / P : 0;   // the thread's landmarks
     for (int r = 0; r < R; ++r) {
-        if (act && far_on && r >= j0) {
-            const float ve = sVe[(size_t)r * dv + t];
-            const float *rho = sRho + (size_t)r * m, *e = sE + (size_t)r * m;
-            for (int b = pi; b < m; b += P) Tt[(size_t)b * L.ldT] = fmaf(rho[b], Tt[(size_t)b * L.ldT], e[b] * ve);
+        const bool ins = far_on && r >= j0;
+        const float fs = readout ? sRow[4 * r + 1] : 0.f;
+        float acc = 0.f;
+        if (ins || fs != 0.f) {
+            const float ve = ins && act ? sVe[(size_t)r * dv + t] : 0.f;
+            const float *rho = sRho + (size_t)r * m, *e = sE + (size_t)r * m, *gn = sU + (size_t)r * m;
+            for (int j = 0; j < nb; j += 8) {
+                float tv[8], rv[8], ev[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int b = pi + (j + u) * P;
+                    const bool in = j + u < nb;
+                    tv[u] = in ? Tt[(size_t)b * L.ldT] : 0.f;
+                    rv[u] = in && ins ? rho[b] : 1.f;
+                    ev[u] = in && ins ? e[b] : 0.f;
+                }
+                if (ins) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) tv[u] = fmaf(rv[u], tv[u], ev[u] * ve);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (j + u < nb) Tt[(size_t)(pi + (j + u) * P) * L.ldT] = tv[u];
+                }
+                if (fs != 0.f) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (j + u < nb) acc = fmaf(gn[pi + (j + u) * P], tv[u], acc);
+                }
+            }
+            acc *= fs;
         }
         if (!readout) continue;
-        const float fs = sRow[4 * r + 1];
-        float acc = 0.f;
         if (act) {
-            if (fs != 0.f) {
-                const float *gn = sU + (size_t)r * m;
-                for (int b = pi; b < m; b += P) acc = fmaf(gn[b], Tt[(size_t)b * L.ldT], acc);
-                acc *= fs;
-            }
             const float *w = sS + (size_t)r * ns;
             for (int x = pi; x < ns; x += P) acc = fmaf(w[x], ssv[(size_t)x * dv + t], acc);
         }
@@ -1295,23 +1339,67 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
 // rows, the 64 x 64 score tile as 4 x 4 per thread over float4 k steps (only
 // the query row groups the pass has), P.V as 16 query rows x 4 columns per
 // thread. Smem: queries [64][d + 4], keys [64][d + 4], values [64][dv + 4],
-// scores [64][65].
+// scores [64][65], the copies' mbarrier.
 constexpr int NS_LD = 65;
 static size_t near_small_smem(const O1Args &a, int KS) {
     (void)KS;
-    return ((size_t)128 * (a.d + 4) + (size_t)64 * (a.dv + 4) + 64 * NS_LD) * sizeof(float);
+    // + the copies' mbarrier (no static shared memory: the limit is all dynamic)
+    return ((size_t)128 * (a.d + 4) + (size_t)64 * (a.dv + 4) + 64 * NS_LD) * sizeof(float) + 16;
 }
 
-template <int NI>
+template <int NI, int NJ>
 __device__ __forceinline__ void ns_scores(float (&c)[4][4], const float *sQ, const float *sK, int ld, int d4) {
     const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll 2
     for (int k4 = 0; k4 < d4; ++k4) {
         float4 av[4], bv[4];
 #pragma unroll
         for (int i = 0; i < NI; ++i) av[i] = *(const float4 *)(sQ + (ty + 16 * i) * ld + 4 * k4);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bv[j] = *(const float4 *)(sK + (tx + 16 * j) * ld + 4 * k4);
-        fma_k4<NI, 4>(c, av, bv);
+        for (int j = 0; j < NJ; ++j) bv[j] = *(const float4 *)(sK + (tx + 16 * j) * ld + 4 * k4);
+        fma_k4<NI, NJ>(c, av, bv);
+    }
+}
+// the NJ key tiles of 16 that hold the slice's keys
+template <int NI>
+__device__ __forceinline__ void ns_scores_j(float (&c)[4][4], const float *sQ, const float *sK, int ld, int d4, int nj) {
+    switch (nj) {
+        case 1: ns_scores<NI, 1>(c, sQ, sK, ld, d4); break;
+        case 2: ns_scores<NI, 2>(c, sQ, sK, ld, d4); break;
+        case 3: ns_scores<NI, 3>(c, sQ, sK, ld, d4); break;
+        default: ns_scores<NI, 4>(c, sQ, sK, ld, d4); break;
+    }
+}
+// Bulk copies of a short pass's rows into shared memory on one mbarrier:
+// each lane of the issuing warp adds its copies' bytes and issues them; lane
+// 0 arrives once after the warp's issue. Waits are bounded: on expiry the
+// flag is raised and the copies still in flight are waited for once more
+// with the full limit.
+__device__ __forceinline__ uint32_t ns_su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void ns_bulk(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(ns_su32(bar)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     ns_su32(dst)),
+                 "l"((uint64_t)src), "r"(bytes), "r"(ns_su32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ bool ns_try(uint64_t *bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(ns_su32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+__device__ __forceinline__ void ns_wait(const O1Args &a, uint64_t *bar) {
+    if (!ns_try(bar, 0, a.wait_cycles)) {
+        if (threadIdx.x == 0) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_WAIT_EXPIRED);
+        ns_try(bar, 0, O1_WAIT_CYCLES_FULL);
     }
 }
 
@@ -1344,35 +1432,40 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
     float *sV = sK + 64 * ld;         // [64][ldv]
     float *sS = sV + 64 * ldv;        // [64][NS_LD]
     // the pass's rotated queries of this group (query q = row q / hpg, head
-    // q % hpg; rows up to 16 ngi, the ones past nq zero) and the slice's keys
-    // and values (the 64 rows, the ones past cnt zero)
-    for (int idx = tid; idx < 16 * ngi * d4; idx += blockDim.x) {
-        const int q = idx / d4, c4 = idx - q * d4, r = q / hpg, h = q - r * hpg;
-        const bool ok = q < nq;
-        cp_async16(sQ + q * ld + 4 * c4, ok ? a.qr + ((size_t)r * a.nh + g * hpg + h) * d + 4 * c4 : a.qr, ok);
+    // q % hpg) and the slice's keys and values, a bulk copy per row (rows of
+    // d and dv floats, 16-byte multiples). The rows past nq and past cnt are
+    // not loaded: their scores are never read.
+    uint64_t &s_bar = *(uint64_t *)(sS + 64 * NS_LD);   // 8-byte aligned: every part above is an even float count
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ns_su32(&s_bar)), "r"(1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int idx = tid; idx < 64 * d4; idx += blockDim.x) {
-        const int i = idx / d4, c4 = idx - i * d4;
-        const bool ok = i < cnt;
-        cp_async16(sK + i * ld + 4 * c4, ok ? o1_key(a, g, x0 + i, mt) + 4 * c4 : a.qr, ok);
-    }
-    for (int idx = tid; idx < 64 * dv4; idx += blockDim.x) {
-        const int i = idx / dv4, c4 = idx - i * dv4;
-        const bool ok = i < cnt;
-        cp_async16(sV + i * ldv + 4 * c4, ok ? o1_val(a, g, x0 + i, mt) + 4 * c4 : a.qr, ok);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
     __syncthreads();
+    if (warp == 0) {
+        for (int i = lane; i < nq + 2 * cnt; i += 32) {
+            if (i < nq) {
+                const int r = i / hpg, hh = i - r * hpg;
+                ns_bulk(sQ + i * ld, a.qr + ((size_t)r * a.nh + g * hpg + hh) * d, (uint32_t)d * 4, &s_bar);
+            } else if (i < nq + cnt) {
+                ns_bulk(sK + (i - nq) * ld, o1_key(a, g, x0 + i - nq, mt), (uint32_t)d * 4, &s_bar);
+            } else {
+                ns_bulk(sV + (i - nq - cnt) * ldv, o1_val(a, g, x0 + i - nq - cnt, mt), (uint32_t)dv * 4, &s_bar);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ns_su32(&s_bar)) : "memory");
+    }
+    ns_wait(a, &s_bar);
     // scores, masked to each query row's window, into sS
     {
         float c[4][4];
         blk_zero(c);
+        const int nj = (cnt + 15) >> 4;
         switch (ngi) {
-            case 1: ns_scores<1>(c, sQ, sK, ld, d4); break;
-            case 2: ns_scores<2>(c, sQ, sK, ld, d4); break;
-            case 3: ns_scores<3>(c, sQ, sK, ld, d4); break;
-            default: ns_scores<4>(c, sQ, sK, ld, d4); break;
+            case 1: ns_scores_j<1>(c, sQ, sK, ld, d4, nj); break;
+            case 2: ns_scores_j<2>(c, sQ, sK, ld, d4, nj); break;
+            case 3: ns_scores_j<3>(c, sQ, sK, ld, d4, nj); break;
+            default: ns_scores_j<4>(c, sQ, sK, ld, d4, nj); break;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -1403,18 +1496,19 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
         }
     }
     __syncthreads();
-    // value sums: thread = (group of 16 query rows, 4 columns), 64 accumulators
+    // value sums: thread = (group of 8 query vectors, 4 columns), 32 accumulators
     {
-        const int qg = tid >> 6, c4 = tid & 63;
-        if (qg < ngi && c4 < dv4) {
-            float acc[16][4];
+        const int c4 = tid & 63;
+        for (int qg = tid >> 6; 8 * qg < nq; qg += 4) {
+            if (c4 >= dv4) break;
+            float acc[8][4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+            for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
             for (int key = 0; key < cnt; ++key) {
                 const float4 v = *(const float4 *)(sV + key * ldv + 4 * c4);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float w = sS[(16 * qg + i) * NS_LD + key];
+                for (int i = 0; i < 8; ++i) {
+                    const float w = sS[(8 * qg + i) * NS_LD + key];
                     acc[i][0] = fmaf(w, v.x, acc[i][0]);
                     acc[i][1] = fmaf(w, v.y, acc[i][1]);
                     acc[i][2] = fmaf(w, v.z, acc[i][2]);
@@ -1422,8 +1516,8 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int q = 16 * qg + i;
+            for (int i = 0; i < 8; ++i) {
+                const int q = 8 * qg + i;
                 if (q < nq)
                     *(float4 *)(pv + (size_t)q * dv + 4 * c4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             }

@@ -9,10 +9,10 @@ calls), or `--tokens` one-row calls after a prompt of `--rows` rows.
 Launches per chunk call: rope, then far_block, far_tscan, side_readout on a
 second stream beside [gather_tc], near, then merge, commit;
 per one-row call: k_tok (one launch); per speculative cycle (`--spec
-DRAFT,ACCEPTED`): the attend-only pass of the draft (no commit kernel; the
-key-slice window kernels for a short draft), then the commit pass of the
-accepted rows (rope, far_block, far_tscan, commit). The library must already
-be built.
+DRAFT,ACCEPTED`): the attend-only pass of the draft (no commit kernel; for a
+draft of at most 16 rows the key-slice window kernels beside the short far
+kernel), then the commit pass of the accepted rows (rope, the short far
+kernel or far_block + far_tscan, commit). The library must already be built.
 """
 from __future__ import annotations
 

@@ -97,6 +97,10 @@ __device__ __forceinline__ void cp_async16(float *dst, const float *src, bool va
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
+__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -916,31 +920,26 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
             if (readout) cp_async16(skt + 4 * i, a.kt + (size_t)g * m * d + 4 * i, true);
             cp_async16(sqt + 4 * i, a.qt + (size_t)h * m * d + 4 * i, true);
         }
-        for (int i = tid; i < m * dv4; i += 256) {
-            const int b = i / dv4, j = i - b * dv4;
-            cp_async16(sT + (size_t)b * L.ldT + 4 * j, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, true);
-        }
-        for (int i = tid; i < R * d4; i += 256) {
-            const int r = i / d4, j = i - r * d4;
-            if (r >= j0) cp_async16(sKe + 4 * i, o1_key(a, g, r - j0, mt) + 4 * j, true);
-        }
-        for (int i = tid; i < R * dv4; i += 256) {
-            const int r = i / dv4, j = i - r * dv4;
-            if (r >= j0) cp_async16(sVe + 4 * i, o1_val(a, g, r - j0, mt) + c0 + 4 * j, true);
+        // a warp per row, lanes across it: T's rows, the evicted keys and values
+        for (int b = warp; b < m; b += 8)
+            for (int j = lane; j < dv4; j += 32)
+                cp_async16(sT + (size_t)b * L.ldT + 4 * j, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, true);
+        for (int r = max(j0, 0) + warp; r < R; r += 8) {
+            const float *ke = o1_key(a, g, r - j0, mt), *ve = o1_val(a, g, r - j0, mt) + c0;
+            for (int j = lane; j < d4; j += 32) cp_async16(sKe + (size_t)r * d + 4 * j, ke + 4 * j, true);
+            for (int j = lane; j < dv4; j += 32) cp_async16(sVe + (size_t)r * dv + 4 * j, ve + 4 * j, true);
         }
     }
     if (readout) {
         for (int i = tid; i < ns * d4; i += 256) cp_async16(ssk + 4 * i, a.sink_k + (size_t)g * ns * d + 4 * i, true);
-        for (int i = tid; i < ns * dv4; i += 256) {
-            const int x = i / dv4, j = i - x * dv4;
-            cp_async16(ssv + 4 * i, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, true);
-        }
-        for (int i = tid; i < R * d4; i += 256) {
-            const int r = i / d4, j = i - r * d4;
-            cp_async16(sQ + 4 * i, a.qr + ((size_t)r * nh + h) * d + 4 * j, true);
-        }
+        for (int x = warp; x < ns; x += 8)
+            for (int j = lane; j < dv4; j += 32)
+                cp_async16(ssv + (size_t)x * dv + 4 * j, a.sink_v + ((size_t)g * ns + x) * dvf + c0 + 4 * j, true);
+        for (int r = warp; r < R; r += 8)
+            for (int j = lane; j < d4; j += 32)
+                cp_async16(sQ + (size_t)r * d + 4 * j, a.qr + ((size_t)r * nh + h) * d + 4 * j, true);
         if (far_on)
-            for (int i = tid; i < m * m; i += 256) smu[i] = a.mu[(size_t)h * m * m + i];
+            for (int i = tid; i < m * m; i += 256) cp_async4(smu + i, a.mu + (size_t)h * m * m + i);
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -1339,12 +1338,11 @@ __global__ __launch_bounds__(256) void k_near(O1Args a) {
 // rows, the 64 x 64 score tile as 4 x 4 per thread over float4 k steps (only
 // the query row groups the pass has), P.V as 16 query rows x 4 columns per
 // thread. Smem: queries [64][d + 4], keys [64][d + 4], values [64][dv + 4],
-// scores [64][65], the copies' mbarrier.
+// scores [64][65].
 constexpr int NS_LD = 65;
 static size_t near_small_smem(const O1Args &a, int KS) {
     (void)KS;
-    // + the copies' mbarrier (no static shared memory: the limit is all dynamic)
-    return ((size_t)128 * (a.d + 4) + (size_t)64 * (a.dv + 4) + 64 * NS_LD) * sizeof(float) + 16;
+    return ((size_t)128 * (a.d + 4) + (size_t)64 * (a.dv + 4) + 64 * NS_LD) * sizeof(float);
 }
 
 template <int NI, int NJ>
@@ -1370,40 +1368,8 @@ __device__ __forceinline__ void ns_scores_j(float (&c)[4][4], const float *sQ, c
         default: ns_scores<NI, 4>(c, sQ, sK, ld, d4); break;
     }
 }
-// Bulk copies of a short pass's rows into shared memory on one mbarrier:
-// each lane of the issuing warp adds its copies' bytes and issues them; lane
-// 0 arrives once after the warp's issue. Waits are bounded: on expiry the
-// flag is raised and the copies still in flight are waited for once more
-// with the full limit.
-__device__ __forceinline__ uint32_t ns_su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void ns_bulk(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(ns_su32(bar)), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     ns_su32(dst)),
-                 "l"((uint64_t)src), "r"(bytes), "r"(ns_su32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ bool ns_try(uint64_t *bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(ns_su32(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (clock64() - t0 > limit) return false;
-    }
-}
-__device__ __forceinline__ void ns_wait(const O1Args &a, uint64_t *bar) {
-    if (!ns_try(bar, 0, a.wait_cycles)) {
-        if (threadIdx.x == 0) atomicOr(&a.hdr->flags, (uint32_t)O1_FLAG_WAIT_EXPIRED);
-        ns_try(bar, 0, O1_WAIT_CYCLES_FULL);
-    }
-}
 
-__global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
+__global__ __launch_bounds__(256, 1) void k_near_small(O1Args a, int KS) {
     extern __shared__ __align__(16) float sm[];
     o1_chain_wait();
     if (a.chain_early) o1_chain_release();
@@ -1432,30 +1398,26 @@ __global__ __launch_bounds__(256) void k_near_small(O1Args a, int KS) {
     float *sV = sK + 64 * ld;         // [64][ldv]
     float *sS = sV + 64 * ldv;        // [64][NS_LD]
     // the pass's rotated queries of this group (query q = row q / hpg, head
-    // q % hpg) and the slice's keys and values, a bulk copy per row (rows of
-    // d and dv floats, 16-byte multiples). The rows past nq and past cnt are
-    // not loaded: their scores are never read.
-    uint64_t &s_bar = *(uint64_t *)(sS + 64 * NS_LD);   // 8-byte aligned: every part above is an even float count
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ns_su32(&s_bar)), "r"(1) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    if (warp == 0) {
-        for (int i = lane; i < nq + 2 * cnt; i += 32) {
-            if (i < nq) {
-                const int r = i / hpg, hh = i - r * hpg;
-                ns_bulk(sQ + i * ld, a.qr + ((size_t)r * a.nh + g * hpg + hh) * d, (uint32_t)d * 4, &s_bar);
-            } else if (i < nq + cnt) {
-                ns_bulk(sK + (i - nq) * ld, o1_key(a, g, x0 + i - nq, mt), (uint32_t)d * 4, &s_bar);
-            } else {
-                ns_bulk(sV + (i - nq - cnt) * ldv, o1_val(a, g, x0 + i - nq - cnt, mt), (uint32_t)dv * 4, &s_bar);
-            }
+    // q % hpg) and the slice's keys and values: a warp per row, 16-byte
+    // asynchronous copies across its lanes. The rows past nq and past cnt
+    // are not loaded: their scores are never read.
+    for (int i = warp; i < nq + 2 * cnt; i += 8) {
+        const float *src;
+        float *dst;
+        int n4;
+        if (i < nq) {
+            const int r = i / hpg, hh = i - r * hpg;
+            src = a.qr + ((size_t)r * a.nh + g * hpg + hh) * d, dst = sQ + i * ld, n4 = d4;
+        } else if (i < nq + cnt) {
+            src = o1_key(a, g, x0 + i - nq, mt), dst = sK + (i - nq) * ld, n4 = d4;
+        } else {
+            src = o1_val(a, g, x0 + i - nq - cnt, mt), dst = sV + (i - nq - cnt) * ldv, n4 = dv4;
         }
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ns_su32(&s_bar)) : "memory");
+        for (int c = lane; c < n4; c += 32) cp_async16(dst + 4 * c, src + 4 * c, true);
     }
-    ns_wait(a, &s_bar);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
     // scores, masked to each query row's window, into sS
     {
         float c[4][4];

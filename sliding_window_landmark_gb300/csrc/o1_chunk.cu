@@ -925,8 +925,16 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
             for (int j = lane; j < dv4; j += 32)
                 cp_async16(sT + (size_t)b * L.ldT + 4 * j, a.T + ((size_t)h * m + b) * dvf + c0 + 4 * j, true);
         for (int r = max(j0, 0) + warp; r < R; r += 8) {
-            const float *ke = o1_key(a, g, r - j0, mt), *ve = o1_val(a, g, r - j0, mt) + c0;
-            for (int j = lane; j < d4; j += 32) cp_async16(sKe + (size_t)r * d + 4 * j, ke + 4 * j, true);
+            const int x = r - j0;
+            const float *ve = o1_val(a, g, x, mt) + c0;
+            if (a.commit_rotates && x >= mt.len0) {   // one of the pass's own keys, rotated here
+                const float *kraw = a.k + ((size_t)(x - mt.len0) * a.G + g) * d;
+                for (int j = lane; j < d4; j += 32)
+                    *(float4 *)(sKe + (size_t)r * d + 4 * j) = o1_rot_chunk(a, kraw, j, a.hdr->pos + (x - mt.len0));
+            } else {
+                const float *ke = o1_key(a, g, x, mt);
+                for (int j = lane; j < d4; j += 32) cp_async16(sKe + (size_t)r * d + 4 * j, ke + 4 * j, true);
+            }
             for (int j = lane; j < dv4; j += 32) cp_async16(sVe + (size_t)r * dv + 4 * j, ve + 4 * j, true);
         }
     }
@@ -1660,6 +1668,36 @@ __global__ __launch_bounds__(256) void k_merge(O1Args a) {
 
 // --------------------------------------------------------------- commit
 
+// Every block of a ring push arrives once its rows are written; the last to
+// arrive (an atomic ticket, no waiting) advances every group's meta by R
+// pushes (o1b_meta) and the position.
+__device__ __forceinline__ void commit_meta(const O1Args &a) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned total = gridDim.x * gridDim.y;
+        const unsigned t = atomicAdd(&a.hdr->ticket, 1u);
+        if (t == total - 1) {
+            __threadfence();
+            for (int gg = 0; gg < a.G; ++gg) {
+                const long long len0 = a.meta[gg * 4 + 0], head0 = a.meta[gg * 4 + 1];
+                const long long wg = a.meta[gg * 4 + 3];
+                const long long tot = len0 + a.R;
+                if (tot <= wg) {
+                    a.meta[gg * 4 + 0] = (uint32_t)tot;
+                } else {
+                    const long long ev = tot - wg;
+                    a.meta[gg * 4 + 0] = (uint32_t)wg;
+                    a.meta[gg * 4 + 1] = (uint32_t)((head0 + ev) % wg);
+                    a.meta[gg * 4 + 2] = a.meta[gg * 4 + 2] + (uint32_t)ev;
+                }
+            }
+            a.hdr->pos += a.R;
+            a.hdr->ticket = 0u;
+        }
+    }
+}
+
 // The pass's rotated keys and values into the ring (o1b_ring_commit: row j
 // to slot (head0 + len0 + j) % wg), only the last wg rows since earlier ones
 // would be overwritten within the pass; then, by the last block to arrive
@@ -1693,30 +1731,36 @@ __global__ __launch_bounds__(256) void k_commit(O1Args a) {
             if (c4 < dv4) ((float4 *)(a.ring_v + ((size_t)g * a.w + slot) * a.dv))[c4] = vv[i];
         }
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned total = gridDim.x * gridDim.y;
-        const unsigned t = atomicAdd(&a.hdr->ticket, 1u);
-        if (t == total - 1) {
-            __threadfence();
-            for (int gg = 0; gg < a.G; ++gg) {
-                const long long len0 = a.meta[gg * 4 + 0], head0 = a.meta[gg * 4 + 1];
-                const long long wg = a.meta[gg * 4 + 3];
-                const long long tot = len0 + a.R;
-                if (tot <= wg) {
-                    a.meta[gg * 4 + 0] = (uint32_t)tot;
-                } else {
-                    const long long ev = tot - wg;
-                    a.meta[gg * 4 + 0] = (uint32_t)wg;
-                    a.meta[gg * 4 + 1] = (uint32_t)((head0 + ev) % wg);
-                    a.meta[gg * 4 + 2] = a.meta[gg * 4 + 2] + (uint32_t)ev;
-                }
-            }
-            a.hdr->pos += a.R;
-            a.hdr->ticket = 0u;
+    commit_meta(a);
+}
+
+// The ring push of a short commit pass that runs without the rotation
+// kernel: block (row, group), thread j rotates pair (j, j + d/2) of the row's
+// raw key to its position as k_rope does and writes it, with the value, to
+// the row's ring slot; then the meta and position as k_commit.
+__global__ __launch_bounds__(128) void k_commit_rot(O1Args a) {
+    o1_chain_wait();   // ends a pass: releases nothing early
+    const int g = blockIdx.y;
+    const O1Meta mt = o1_meta(a, g);
+    const int r = max(0, a.R - mt.wg) + (int)blockIdx.x;
+    if (r < a.R) {
+        const int slot = (int)(((long long)mt.head0 + mt.len0 + r) % mt.wg);
+        const float *kraw = a.k + ((size_t)r * a.G + g) * a.d;
+        float *rk = a.ring_k + ((size_t)g * a.w + slot) * a.d;
+        const int half = a.d >> 1;
+        const long long p = a.hdr->pos + r;
+        for (int j = threadIdx.x; j < half; j += blockDim.x) {
+            float c = 1.f, s = 0.f;
+            if (a.rotate) o1_rope_cs(a.hdr->inv_freq[j], p, c, s);
+            const float x0 = kraw[j], x1 = kraw[j + half];
+            rk[j] = x0 * c - x1 * s;
+            rk[j + half] = x1 * c + x0 * s;
         }
+        const float4 *vs = (const float4 *)(a.v + ((size_t)r * a.G + g) * a.dv);
+        float4 *vd = (float4 *)(a.ring_v + ((size_t)g * a.w + slot) * a.dv);
+        for (int c4 = threadIdx.x; c4 < (a.dv >> 2); c4 += blockDim.x) vd[c4] = vs[c4];
     }
+    commit_meta(a);
 }
 
 // ------------------------------------------------------------- launchers
@@ -1796,8 +1840,12 @@ cudaError_t o1_aux(O1Aux **out) {
 cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t const *ev) {
     chunk_attrs();
     O1Args a = a_in;
+    const int R = a.R;
     const int KS = near_small_ks(a);   // > 0: a short pass, its window split over key slices
     if (KS) a.tc = 0;
+    // a short pass's window kernels are scheduled under their predecessors'
+    // ends (its CTAs fit beside the far branch's few)
+    if (KS && R <= O1_SHORT_ROWS) a.chain_early = 1;
     {
         // window key splits for a tensor-core pass with fewer CTAs than SMs
         o1_geom gw = {};
@@ -1808,7 +1856,6 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
         gw.window = a.w;
         a.wsplit = a.tc ? o1_wsplit(gw, a.R) : 1;
     }
-    const int R = a.R;
     const int nblk = (R + O1_SUB - 1) / O1_SUB;
     auto begin = [&](int i, cudaStream_t s) {
         if (ev) cudaEventRecord(ev[2 * i], s);
@@ -1887,7 +1934,9 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
 // The state-advancing stages of a pass, without the attention: keys
 // rotated, the far insert of every key the rows evict (block partials and
 // the scan), the surviving rows into the ring, meta and position. Launched
-// on one stream; a.commit must be set and a.tc clear.
+// on one stream; a.commit must be set and a.tc clear. A short pass is two
+// launches: the short far kernel, then the ring push, each rotating the
+// pass's keys it reads.
 cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     chunk_attrs();
     const int R = a.R;
@@ -1896,11 +1945,17 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
     as.short_no_readout = 1;
     const size_t sfs = short_smem_floats(as) * sizeof(float);
     const bool short_far = R <= O1_SHORT_ROWS && sfs <= 227 * 1024;
-    as.chain_early = short_far;   // rotation -> far inserts -> ring, each scheduled under the previous one's end
-    k_rope<<<R, 128, 0, st>>>(as);
     if (short_far) {
-        o1_launch_chained(k_side_short, dim3(a.nh, short_col_splits(as)), dim3(256), sfs, st, as);   // the far inserts of a short commit
-    } else {
+        // far inserts, then the ring push scheduled under their end
+        as.chain_early = 1;
+        as.commit_rotates = 1;
+        k_side_short<<<dim3(a.nh, short_col_splits(as)), 256, sfs, st>>>(as);
+        const int live = R < a.w ? R : a.w;
+        o1_launch_chained(k_commit_rot, dim3(live, a.G), dim3(128), 0, st, as);
+        return cudaGetLastError();
+    }
+    k_rope<<<R, 128, 0, st>>>(a);
+    {
         const size_t fbs = far_block_smem_floats() * sizeof(float);
         if (a.dv <= 128) o1_launch_chained(k_far_block<1>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
         else o1_launch_chained(k_far_block<2>, dim3(nblk, a.nh), dim3(256), fbs, st, a);

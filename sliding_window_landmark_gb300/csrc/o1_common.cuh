@@ -326,6 +326,7 @@ struct O1Args {
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     int short_no_readout;   // short far pass of a commit: inserts only, no side parts
     int chain_early;        // the pass's chained kernels may be scheduled before their predecessor ends
+    int commit_rotates;     // a short commit pass without the rotation kernel: the keys are rotated where read
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;   // the row stride of E and P (a multiple of 4)
@@ -362,6 +363,23 @@ __device__ __forceinline__ void o1_rope_cs(float inv, long long p, float &c, flo
     sincosf(rf, &sf, &cf);
     c = cf - sf * rl;
     s = sf + cf * rl;
+}
+
+// Float4 chunk c4 of key row `row` (raw, from the caller's k) rotated to
+// position p: the rotation k_rope applies, pair (j, j + d/2), done where the
+// key is read.
+__device__ __forceinline__ float4 o1_rot_chunk(const O1Args &a, const float *row, int c4, long long p) {
+    const int half = a.d >> 1;
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int j = 4 * c4 + e, lo = j < half ? j : j - half;
+        float c = 1.f, s = 0.f;
+        if (a.rotate) o1_rope_cs(a.hdr->inv_freq[lo], p, c, s);
+        const float x0 = row[lo], x1 = row[lo + half];
+        y[e] = j < half ? x0 * c - x1 * s : x1 * c + x0 * s;
+    }
+    return make_float4(y[0], y[1], y[2], y[3]);
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -545,7 +563,8 @@ static inline void o1_attrs_done(unsigned long long *mask, unsigned long long bi
 // is launched plainly. o1_chain_release() lets the next chained kernel be
 // scheduled before this one ends; the kernels that can end a pass never call
 // it, because a one-row step launched after them reads the state ahead of
-// its own wait. Only short commit passes release (O1Args::chain_early): in a
+// its own wait. Only short passes release (O1Args::chain_early: commit passes
+// and key-slice window passes of at most O1_SHORT_ROWS rows): in a
 // prompt-sized pass, dependents scheduled early hold SMs that the other
 // stream's kernels would use.
 __device__ __forceinline__ void o1_chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

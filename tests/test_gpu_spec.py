@@ -47,6 +47,10 @@ SPEC_CASES = [
     # inside a committed draft
     (synth.Shape(groups=1, heads_per_group=4, d=32, dv=32, sinks=0, window=64, landmarks=4), 40,
      [(30, 30), (20, 11)], 64),
+    # group windows narrower than a short commit: the commit evicts its own
+    # rows, whose keys the far insert rotates where it reads them
+    (synth.Shape(groups=2, heads_per_group=2, d=64, dv=64, sinks=2, window=12, landmarks=4, group_windows=(6, 12)), 30,
+     [(16, 14), (10, 9), (4, 1)], 32),
 ]
 
 

@@ -799,7 +799,9 @@ def our_arm(args, rank, world, local_rank):
                             "config": f"after the decode steps: {SPEC_DRAFT}-row drafts through "
                                       f"o1_chunk_attend_spec, {SPEC_ACC} rows of each through o1_spec_commit; "
                                       f"{SPEC_CYCLES} cycles captured once in a CUDA graph and replayed",
-                            "gpu_launches_per_cycle": nst - 1 + 4},
+                            # verify: rotation, short far kernel, key-slice window kernel and
+                            # its slice merge, merge; commit: short far kernel, ring push
+                            "gpu_launches_per_cycle": 7},
             "peaks": {"source": src, **{k2: pk_[k2] for k2 in ("hbm_gbs", "bf16_tflops") if k2 in pk_}},
             "clocks": clk.summary()}
     if rank == 0 and world == 1:

@@ -1047,14 +1047,19 @@ __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
                     }
                 }
             }
+            // the new M, Z go to scratch, not to the state: the head's other
+            // column-slice CTAs may not have read the old ones yet. The
+            // pass's ring push stores them (far_copy).
             if (a.commit && lead) {
+                const size_t nm = (size_t)nh * m;
+                float *out = a.Fb + (size_t)O1_FB_PLANES * nm * a.nsub;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int b = lane + 32 * k;
                     if (b < m) {
-                        a.M[(size_t)h * m + b] = Mr[k];
-                        a.Z[(size_t)h * m + b] = Zr[k].hi;
-                        a.Zlo[(size_t)h * m + b] = Zr[k].lo;
+                        out[(size_t)h * m + b] = Mr[k];
+                        out[nm + (size_t)h * m + b] = Zr[k].hi;
+                        out[2 * nm + (size_t)h * m + b] = Zr[k].lo;
                     }
                 }
             }
@@ -1670,8 +1675,18 @@ __global__ __launch_bounds__(256) void k_merge(O1Args a) {
 
 // Every block of a ring push arrives once its rows are written; the last to
 // arrive (an atomic ticket, no waiting) advances every group's meta by R
-// pushes (o1b_meta) and the position.
+// pushes (o1b_meta) and the position. After a short far kernel (far_copy)
+// block (0, 0) first stores the new M, Z, Zlo it left in scratch.
 __device__ __forceinline__ void commit_meta(const O1Args &a) {
+    if (a.far_copy && blockIdx.x == 0 && blockIdx.y == 0) {
+        const size_t nm = (size_t)a.nh * a.m;
+        const float *src = a.Fb + (size_t)O1_FB_PLANES * nm * a.nsub;
+        for (size_t i = threadIdx.x; i < nm; i += blockDim.x) {
+            a.M[i] = src[i];
+            a.Z[i] = src[nm + i];
+            a.Zlo[i] = src[2 * nm + i];
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1875,6 +1890,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     // a short pass takes the row-serial far kernel (stages 1 and 2 stay empty)
     const size_t sfs = short_smem_floats(a) * sizeof(float);
     const bool short_far = R <= O1_SHORT_ROWS && sfs <= 227 * 1024;
+    a.far_copy = short_far && a.commit && !a.exact;
     begin(1, sf);
     const size_t fbs = far_block_smem_floats() * sizeof(float);
     if (!a.exact && !short_far) {   // the comparator has no far field
@@ -1949,6 +1965,7 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
         // far inserts, then the ring push scheduled under their end
         as.chain_early = 1;
         as.commit_rotates = 1;
+        as.far_copy = !a.exact;
         k_side_short<<<dim3(a.nh, short_col_splits(as)), 256, sfs, st>>>(as);
         const int live = R < a.w ? R : a.w;
         o1_launch_chained(k_commit_rot, dim3(live, a.G), dim3(128), 0, st, as);

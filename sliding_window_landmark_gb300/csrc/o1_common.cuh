@@ -327,6 +327,7 @@ struct O1Args {
     int short_no_readout;   // short far pass of a commit: inserts only, no side parts
     int chain_early;        // the pass's chained kernels may be scheduled before their predecessor ends
     int commit_rotates;     // a short commit pass without the rotation kernel: the keys are rotated where read
+    int far_copy;           // the short far kernel left the new M, Z, Zlo in Fb's entering planes; the ring push stores them
     // scratch
     float *qr, *kr, *E, *P, *Fb, *Tp, *fh, *sh, *sn;
     int cap;   // the row stride of E and P (a multiple of 4)

@@ -1900,7 +1900,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     end(1, sf);
     begin(2, sf);
     const size_t n = (size_t)a.nh * a.m * a.dv;
-    if (!a.exact && !short_far) o1_launch_chained(k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, sf, a);
+    if (!a.exact && !short_far) o1_launch_chained(a.chain_early, k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, sf, a);
     end(2, sf);
     begin(3, sf);
     if (short_far) k_side_short<<<dim3(a.nh, short_col_splits(a)), 256, sfs, sf>>>(a);   // behind the fork: plain
@@ -1908,9 +1908,9 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
         if (a.dv <= 128) k_side_readout<1><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
         else k_side_readout<2><<<dim3(nblk, a.nh), 256, readout_smem(a), sf>>>(a);
     } else if (a.dv <= 128) {
-        o1_launch_chained(k_side_readout<1>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
+        o1_launch_chained(a.chain_early, k_side_readout<1>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
     } else {
-        o1_launch_chained(k_side_readout<2>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
+        o1_launch_chained(a.chain_early, k_side_readout<2>, dim3(nblk, a.nh), dim3(256), readout_smem(a), sf, a);
     }
     end(3, sf);
     cudaEventRecord(aux->join, sf);
@@ -1921,15 +1921,15 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     if (e == cudaSuccess) {
         if (KS) {
             const int nsl = (a.w + R - 1 + KS - 1) / KS;
-            o1_launch_chained(k_near_small, dim3(nsl, a.G), dim3(256), near_small_smem(a, KS), st, a, KS);
-            o1_launch_chained(k_near_small_merge, dim3(R * a.nh, (a.dv + 63) / 64), dim3(256), 0, st, a, nsl);
+            o1_launch_chained(a.chain_early, k_near_small, dim3(nsl, a.G), dim3(256), near_small_smem(a, KS), st, a, KS);
+            o1_launch_chained(a.chain_early, k_near_small_merge, dim3(R * a.nh, (a.dv + 63) / 64), dim3(256), 0, st, a, nsl);
         } else if (a.tc) {
             e = o1_launch_near_tc(a, st);
         } else {
             const int RB = 32 / a.hpg;
             const dim3 gn((R + RB - 1) / RB, a.G);
-            if (a.dv <= 128) o1_launch_chained(k_near<1>, gn, dim3(256), near_smem(a), st, a);
-            else o1_launch_chained(k_near<2>, gn, dim3(256), near_smem(a), st, a);
+            if (a.dv <= 128) o1_launch_chained(a.chain_early, k_near<1>, gn, dim3(256), near_smem(a), st, a);
+            else o1_launch_chained(a.chain_early, k_near<2>, gn, dim3(256), near_smem(a), st, a);
         }
     }
     end(5, st);
@@ -1942,7 +1942,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     end(6, st);
     begin(7, st);
     const int live = R < a.w ? R : a.w;
-    if (a.commit) o1_launch_chained(k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
+    if (a.commit) o1_launch_chained(a.chain_early, k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
     end(7, st);
     return cudaGetLastError();
 }
@@ -1968,19 +1968,19 @@ cudaError_t o1_launch_commit_pass(const O1Args &a, cudaStream_t st) {
         as.far_copy = !a.exact;
         k_side_short<<<dim3(a.nh, short_col_splits(as)), 256, sfs, st>>>(as);
         const int live = R < a.w ? R : a.w;
-        o1_launch_chained(k_commit_rot, dim3(live, a.G), dim3(128), 0, st, as);
+        o1_launch_chained(as.chain_early, k_commit_rot, dim3(live, a.G), dim3(128), 0, st, as);
         return cudaGetLastError();
     }
     k_rope<<<R, 128, 0, st>>>(a);
     {
         const size_t fbs = far_block_smem_floats() * sizeof(float);
-        if (a.dv <= 128) o1_launch_chained(k_far_block<1>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
-        else o1_launch_chained(k_far_block<2>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
+        if (a.dv <= 128) o1_launch_chained(a.chain_early, k_far_block<1>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
+        else o1_launch_chained(a.chain_early, k_far_block<2>, dim3(nblk, a.nh), dim3(256), fbs, st, a);
         const size_t n = (size_t)a.nh * a.m * a.dv;
-        o1_launch_chained(k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, a);
+        o1_launch_chained(a.chain_early, k_far_tscan, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, a);
     }
     const int live = R < a.w ? R : a.w;
-    o1_launch_chained(k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
+    o1_launch_chained(a.chain_early, k_commit, dim3((live + 3) / 4, a.G), dim3(64), 0, st, a);
     return cudaGetLastError();
 }
 

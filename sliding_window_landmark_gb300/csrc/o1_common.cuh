@@ -325,7 +325,7 @@ struct O1Args {
     int commit;   // 0: attend only, the state is left as it was (speculative verify)
     int exact;    // 1: sinks + window only, no far field (the exact-attention comparator)
     int short_no_readout;   // short far pass of a commit: inserts only, no side parts
-    int chain_early;        // the pass's chained kernels may be scheduled before their predecessor ends
+    int chain_early;        // a short pass: its kernels are chained and scheduled before their predecessor ends
     int commit_rotates;     // a short commit pass without the rotation kernel: the keys are rotated where read
     int far_copy;           // the short far kernel left the new M, Z, Zlo in Fb's entering planes; the ring push stores them
     // scratch
@@ -555,25 +555,27 @@ static inline void o1_attrs_done(unsigned long long *mask, unsigned long long bi
     __atomic_fetch_or(mask, bit, __ATOMIC_RELEASE);
 }
 
-// Chained launches (programmatic dependent launch). A kernel launched by
-// o1_launch_chained may be scheduled while the previous kernel of its stream
-// is still running, so it calls o1_chain_wait() before it touches global
-// memory; the wait returns once that kernel has completed and its writes are
-// visible. Since every chained kernel waits, a chain completes in order. The
-// first kernel of a pass on a stream, and every kernel behind an event wait,
-// is launched plainly. o1_chain_release() lets the next chained kernel be
-// scheduled before this one ends; the kernels that can end a pass never call
-// it, because a one-row step launched after them reads the state ahead of
-// its own wait. Only short passes release (O1Args::chain_early: commit passes
-// and key-slice window passes of at most O1_SHORT_ROWS rows): in a
-// prompt-sized pass, dependents scheduled early hold SMs that the other
-// stream's kernels would use.
+// Chained launches (programmatic dependent launch), used in short passes
+// (at most O1_SHORT_ROWS rows: the key-slice window kernels, the short
+// commit pass; O1Args::chain_early). A kernel launched by o1_launch_chained
+// with `chained` set may be scheduled while the previous kernel of its
+// stream is still running, so every kernel that can be launched that way
+// calls o1_chain_wait() before it touches global memory; the wait returns
+// once that kernel has completed and its writes are visible (and at once
+// after a plain launch). Since every chained kernel waits, a chain completes
+// in order. The first kernel of a pass on a stream, and every kernel behind
+// an event wait, is launched plainly. o1_chain_release() lets the next
+// chained kernel be scheduled before this one ends; the kernels that can
+// end a pass never call it, because a one-row step launched after them reads
+// the state ahead of its own wait. Longer passes launch plainly: chaining
+// them measured slower (a 24-layer stack of 64-row chunks 40.7 -> 48.9 ms,
+// a 4096-row prompt with early release 0.370 -> 0.396 ms).
 __device__ __forceinline__ void o1_chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void o1_chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... P, typename... A>
-static inline void o1_launch_chained(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                     A... args) {
+static inline void o1_launch_chained(bool chained, void (*k)(P...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, A... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -583,7 +585,7 @@ static inline void o1_launch_chained(void (*k)(P...), dim3 grid, dim3 block, siz
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = chained ? 1 : 0;
     cudaLaunchKernelEx(&cfg, k, args...);
 }
 

@@ -664,7 +664,7 @@ size_t tc_smem(int d, int *nslot) {
 }  // namespace
 
 cudaError_t o1_launch_gather_tc(const O1Args &a, cudaStream_t st) {
-    o1_launch_chained(k_gather_tc, dim3((a.nxp + 31) / 32, a.G), dim3(256), 0, st, a, a.Xk, a.XvT, a.nxp);
+    o1_launch_chained(a.chain_early, k_gather_tc, dim3((a.nxp + 31) / 32, a.G), dim3(256), 0, st, a, a.Xk, a.XvT, a.nxp);
     return cudaGetLastError();
 }
 
@@ -697,7 +697,7 @@ cudaError_t o1_launch_near_tc(const O1Args &a, cudaStream_t st) {
             return cudaErrorInvalidValue;
     }
     const int S = a.wsplit > 1 ? a.wsplit : 1;
-    o1_launch_chained(k_near_tc, dim3((a.R + TC_BM - 1) / TC_BM, a.nh, S), dim3(TC_THREADS), smem, st, a, mk, mv, mq,
+    o1_launch_chained(a.chain_early, k_near_tc, dim3((a.R + TC_BM - 1) / TC_BM, a.nh, S), dim3(TC_THREADS), smem, st, a, mk, mv, mq,
                       NXp, nslot);
     return cudaGetLastError();
 }

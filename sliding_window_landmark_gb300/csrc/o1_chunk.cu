@@ -845,52 +845,7 @@ __global__ __launch_bounds__(256, 2) void k_side_readout(O1Args a) {
 // CTAs a head (short_col_splits, up to 4; 8 measured slower): each repeats
 // the scalars (steps 1-3) and takes one slice of T, of the numerators and of
 // the evicted and sink values.
-__host__ __device__ inline int short_col_splits(const O1Args &a) {
-    for (int cs = 4; cs > 1; cs >>= 1)
-        if (a.nh * cs <= 148 && a.dv % (4 * cs) == 0) return cs;
-    return 1;
-}
-
-// Shared memory of k_side_short, in floats; every part starts on 16 bytes.
-struct ShortLayout {
-    int dvs;   // value columns of this CTA
-    int P;     // threads per value column in step 4 (a power of two, at most 32)
-    int ldT;   // row stride of T: P lanes on P landmarks of one column hit P different banks
-    size_t skt, sqt, smu, sT, ssk, ssv, sKe, sVe, sQ, sL, sF, sU, sRho, sE, sMr, sZh, sZl, sS, sRow, total;
-};
-__host__ __device__ inline size_t short_up4(size_t x) { return (x + 3) / 4 * 4; }
-__host__ __device__ inline ShortLayout short_layout(const O1Args &a) {
-    ShortLayout L;
-    L.dvs = a.dv / short_col_splits(a);
-    L.P = 1;
-    while (L.P < 32 && 2 * L.P * L.dvs <= 256) L.P *= 2;
-    const int off = L.P >= 8 ? 4 : 32 / L.P;   // stride = off (mod 32), a multiple of 4
-    L.ldT = L.dvs + ((off - L.dvs) % 32 + 32) % 32;
-    const size_t m = a.m, d = a.d, dvs = L.dvs, ns = a.ns, R = a.R;
-    size_t o = 0;
-    L.skt = o;  o += m * d;                // [m][d]   landmark keys of the group
-    L.sqt = o;  o += m * d;                // [m][d]   landmark queries of the head
-    L.smu = o;  o += short_up4(m * m);     // [m][m]
-    L.sT = o;   o += m * L.ldT;            // [m][ldT] far value sums (this slice)
-    L.ssk = o;  o += ns * d;               // [ns][d]
-    L.ssv = o;  o += ns * dvs;             // [ns][dvs]
-    L.sKe = o;  o += R * d;                // [R][d]   the key each row evicts
-    L.sVe = o;  o += R * dvs;              // [R][dvs] and its value
-    L.sQ = o;   o += R * d;                // [R][d]   the rows' rotated queries
-    L.sL = o;   o += short_up4(R * m);     // [R][m]   insert logits
-    L.sF = o;   o += short_up4(R * m);     // [R][m]   far scores, then e^{f - F}
-    L.sU = o;   o += short_up4(R * m);     // [R][m]   u, then the gains
-    L.sRho = o; o += short_up4(R * m);     // [R][m]   the inserts' rescales
-    L.sE = o;   o += short_up4(R * m);     //          and weights
-    L.sMr = o;  o += short_up4(R * m);     // [R][m]   M after each row's insert
-    L.sZh = o;  o += short_up4(R * m);     //          and Z, high
-    L.sZl = o;  o += short_up4(R * m);     //          and low part
-    L.sS = o;   o += short_up4(R * ns);    // [R][ns]  sink scores, then weights
-    L.sRow = o; o += 4 * R;                // [R][4]   F, e^{c_f - c_s} (0: no far part)
-    L.total = o;
-    return L;
-}
-__host__ __device__ inline size_t short_smem_floats(const O1Args &a) { return short_layout(a).total; }
+// short_col_splits and the shared-memory layout (ShortLayout) are in o1_common.cuh.
 
 __global__ __launch_bounds__(256, 1) void k_side_short(O1Args a) {
     extern __shared__ __align__(16) float sm[];

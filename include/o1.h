@@ -222,7 +222,10 @@ O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size
  * the first call on each host thread and device (make that call before a
  * stream capture) and live until that thread exits. A stage that does not apply to the geometry
  * (the fp16 panel gather outside the tensor-core window path) launches
- * nothing and times as empty. */
+ * nothing and times as empty. A pass of at most 16 rows runs its far field
+ * and sinks as one short kernel (timed as side_readout; far_block and
+ * far_tscan stay empty) and, from 2 rows, its window as key-slice kernels
+ * (timed as near). */
 #define O1_NUM_STAGES 8
 
 /* o1_chunk_attend that also records caller-created CUDA events (cudaEvent_t

@@ -208,7 +208,9 @@ O1_API int o1_window_attend(void *state, const o1_geom *geom, void *scratch, siz
  * near partials split across blocks, the far part, a merge, the commit).
  *   q [G*hpg][d], k [G][d], v [G][dv], gate [G*hpg][dv] or NULL, out [G*hpg][dv]
  *   scratch  device, at least o1_scratch_bytes(geom, 1) bytes
- * Asynchronous. */
+ * Where that path's shared memory would exceed a block's (windows of a few
+ * hundred thousand keys and more), the row runs as a one-row chunk pass,
+ * with the same result. Asynchronous. */
 O1_API int o1_token_attend(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
                     const float *q, const float *k, const float *v, const float *gate,
                     float *out, void *stream);

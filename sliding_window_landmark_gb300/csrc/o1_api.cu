@@ -175,8 +175,12 @@ int chunk(void *state, const o1_geom *geom, void *scratch, size_t scratch_bytes,
             a.gate = gate ? gate + (size_t)r0 * nh * g.dv : nullptr;
             a.out = out + (size_t)r0 * nh * g.dv;
             a.R = 1;
-            if (o1_launch_token(a, st) != cudaSuccess) return O1_ERR_CUDA;
-            continue;
+            const cudaError_t te = o1_launch_token(a, st);
+            if (te == cudaSuccess) continue;
+            // cudaErrorInvalidConfiguration: the one-row kernel's shared
+            // memory exceeds a block's for this geometry (windows of a few
+            // hundred thousand keys); the row takes a one-row pass instead
+            if (te != cudaErrorInvalidConfiguration) return O1_ERR_CUDA;
         }
         const O1Scratch S = o1_scratch_layout(g, R);
         scratch_args(a, scratch, S);
@@ -344,7 +348,11 @@ int o1_spec_commit(void *state, const o1_geom *geom, void *scratch, size_t scrat
         a.k = k;
         a.v = v;
         a.R = 1;
-        return o1_launch_token(a, st) == cudaSuccess ? O1_OK : O1_ERR_CUDA;
+        const cudaError_t te = o1_launch_token(a, st);
+        if (te == cudaSuccess) return O1_OK;
+        // the one-row kernel does not fit this geometry: a one-row commit pass
+        if (te != cudaErrorInvalidConfiguration) return O1_ERR_CUDA;
+        a = state_args(state, g);
     }
     for (int r0 = 0; r0 < rows; r0 += cap) {
         const int R = rows - r0 < cap ? rows - r0 : cap;

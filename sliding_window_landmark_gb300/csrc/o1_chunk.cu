@@ -1842,7 +1842,7 @@ cudaError_t o1_launch_pass(const O1Args &a_in, cudaStream_t st, cudaEvent_t cons
     end(0, st);
     cudaEventRecord(aux->fork, st);
     cudaStreamWaitEvent(sf, aux->fork, 0);
-    // a short pass takes the row-serial far kernel (stages 1 and 2 stay empty)
+    // a short pass takes the short far kernel (stages 1 and 2 stay empty)
     const size_t sfs = short_smem_floats(a) * sizeof(float);
     const bool short_far = R <= O1_SHORT_ROWS && sfs <= 227 * 1024;
     a.far_copy = short_far && a.commit && !a.exact;

@@ -32,7 +32,7 @@
 #define O1_MAX_W (1 << 20)
 #define O1_TC_BN 128           // keys per tile of the tensor-core window path
 #define O1_TC_BM 128           // query rows per CTA of the tensor-core window path
-#define O1_SHORT_ROWS 16       // passes up to this many rows take the row-serial far kernel
+#define O1_SHORT_ROWS 16       // passes up to this many rows take the short far kernel
 #define O1_TC_MIN_WINDOW 512   // narrower windows take the fp32 window kernel
 // Clock cycles an in-kernel wait may spin before the kernel gives up (about
 // 2 s at the maximum SM clock). Drains of copies or MMAs already in flight

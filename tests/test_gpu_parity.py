@@ -320,7 +320,7 @@ def test_timed_stages_and_stream_capture():
     harness.assert_state(cap.read(), orc, "graph replay state")
 
 
-# passes of at most 16 rows take the row-serial far kernel (k_side_short):
+# passes of at most 16 rows take the short far kernel (k_side_short):
 # (shape, calls) with short calls after a prompt that fills the ring, so
 # that every short row evicts, and one set before it fills
 SHORT_CASES = [
